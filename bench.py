@@ -1,0 +1,396 @@
+"""Benchmark of the INT4 per-(token, head) KV cache on GB300; prints ONE JSON line (rank 0).
+
+A step is one pass of the whole hot path over one batch of the GQA decode workload
+(32 sequences with lengths uniform in [512, 4096], 32 q / 8 kv heads, head size 128, block 16,
+bf16, 4 loud K channels per kv head): write the step's 32 new tokens into the paged INT4 cache
+(rotation, quantisation, packing), then run causal paged attention of the 32 queries over the
+whole cache.
+
+  value   packed-KV GB/s of the decode step: bytes of packed K/V rows (codes + scales) the
+          attention reads, plus Q and O, per step, over the device-timed step (write included).
+  e2e     the same bytes over a step timed through the public API from pinned host buffers:
+          each step copies its new K/V, slots, queries and tables host->device and the output
+          device->host.
+  write   the write-throughput workload (65536 tokens, 8 kv heads, d 128, bf16, per-token
+          magnitudes 10^U(-2,2), random slots over 8192 blocks): tokens/s and GB/s.
+  roofline  for the dominant kernel call (the attention: decode kernel + segment combine), bytes
+          per launch over its CUDA-event time on the launching stream, against the measured HBM
+          copy bandwidth; ``traffic`` is the ncu DRAM byte count of the decode kernel when a
+          summary with it is committed under profiles/, else null.
+
+L2 (129 MB) is defeated by rotating the steps over several independent cache replicas whose total
+exceeds twice the L2 size.  Runs as N independent replicas under torchrun (the path does not
+shard across GPUs; each rank runs the same workload, no collective on the data path).
+``--impl reference`` times the CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn packed-KV GB/s (% HBM peak) at 1 GB300; write tokens/s"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary (profiles/traffic.json), if present."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        return t.get(kernel_key)
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, polled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------------- GPU arm
+
+def _decode_setup(torch, kv, wl, dev, replicas):
+    """Cache replicas holding every sequence's history, and the step's device inputs."""
+    H, d = wl.num_kv_heads, wl.head_size
+    signs = torch.from_numpy(wl.signs).to(dev)
+    hist = wl.history_token_rows()
+    new = wl.new_token_rows()
+    caches = []
+    for _ in range(replicas):
+        c = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, wl.block_size, H, d), dtype=torch.uint8, device=dev)
+        kv.kv_int4_write(wl.key[hist].to(dev), wl.value[hist].to(dev),
+                         torch.from_numpy(wl.slot_mapping[hist]).to(dev), signs, c)
+        caches.append(c)
+    host = {
+        "k": wl.key[new].contiguous().pin_memory(),
+        "v": wl.value[new].contiguous().pin_memory(),
+        "slots": torch.from_numpy(wl.slot_mapping[new].copy()).pin_memory(),
+        "q": wl.query.contiguous().pin_memory(),
+        "tables": torch.from_numpy(wl.block_tables.copy()).pin_memory(),
+        "lens": torch.from_numpy(wl.seq_lens.copy()).pin_memory(),
+        "qsl": torch.from_numpy(wl.query_start_loc.copy()).pin_memory(),
+    }
+    devt = {k: v.to(dev) for k, v in host.items()}
+    devt["signs"] = signs
+    return caches, host, devt
+
+
+def _gpu_arm(args):
+    import torch
+
+    import int4_token_head_kv_gb300 as kv
+    import workloads
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    wl = workloads.gqa_decode_batch(seed=args.seed)
+    H, d, Hq = wl.num_kv_heads, wl.head_size, wl.num_q_heads
+    rb = kv.kv_int4_row_bytes(d)
+    cache_bytes = wl.num_blocks * 2 * 16 * H * rb
+    replicas = max(2, -(-2 * L2_BYTES // cache_bytes))
+    caches, host, t = _decode_setup(torch, kv, wl, dev, replicas)
+    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, wl.segment_len)
+    nseg = -(-wl.max_seq_len // seg)
+    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(wl.query.shape[0], Hq, d, len(wl.seq_lens),
+                                                                 wl.max_seq_len, seg)), dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.query.shape[0], Hq, d), dtype=wl.query.dtype, device=dev)
+    kv_bytes = int(wl.seq_lens.sum()) * 2 * H * rb
+    qo_bytes = 2 * wl.query.numel() * wl.query.element_size()
+    attn_bytes = kv_bytes + qo_bytes
+    launches_per_step = 1 + 1 + (1 if nseg > 1 else 0)
+
+    def write(i):
+        kv.kv_int4_write(t["k"], t["v"], t["slots"], t["signs"], caches[i % replicas])
+
+    def attend(i):
+        kv.kv_int4_paged_attention(t["q"], caches[i % replicas], t["tables"], t["lens"], t["qsl"], wl.softmax_scale,
+                                   t["signs"], max_query_len=1, max_seq_len=wl.max_seq_len, out=out,
+                                   segment_len=seg, workspace=ws)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        write(i)
+        attend(i)
+    # ---- device-timed steps, with the attention call timed separately for the roofline
+    n_ev = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_ev + 1)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.06)
+    barrier()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        write(i)
+        ev[2 * i + 1].record(stream)
+        attend(i)
+        ev[2 * i + 2].record(stream)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = ev[0].elapsed_time(ev[-1])
+    attn_ms = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps)]
+    ms_step = total_ms / args.steps
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    value = attn_bytes * world / (ms_step * 1e-3) / 1e9
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+
+    # ---- end to end through the public API from pinned host buffers
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d2h = host_out.numel() * host_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for i in range(args.steps):
+        for k in host:
+            t[k].copy_(host[k], non_blocking=True)
+        write(i)
+        attend(i)
+        host_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_value = attn_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    # ---- write-throughput workload
+    wres = _write_bench(torch, kv, workloads, dev, stream, args)
+
+    peak, peak_kind = _peaks()
+    roof_achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic = _traffic("decode_gqa_batch")
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4-kv/f16-mma/f32", "data": "synthetic",
+        "config": {"workload": "gqa_decode_batch: 32 seqs, seq_len U[512,4096] (sum %d), 32 q / 8 kv heads, "
+                               "head 128, block 16, bf16 N(0,1) with 4 K channels x10 per kv head, "
+                               "permuted blocks; step = write 32 new tokens + decode attention"
+                               % int(wl.seq_lens.sum()),
+                   "segment_len": seg, "segments_max": nseg, "packed_kv_bytes_per_step": kv_bytes,
+                   "qo_bytes_per_step": qo_bytes,
+                   "l2": f"{replicas} cache replicas rotated per step ({replicas * cache_bytes / 2**20:.0f} MiB "
+                         f"> 2 x 129 MB L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5)},
+        "roofline": {"bound": "hbm", "achieved": round(roof_achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(roof_achieved / peak, 4), "traffic": traffic,
+                     "kernel": "attention call (decode kernel + segment combine)", "peak_source": peak_kind,
+                     "bytes_per_launch": attn_bytes, "avg_ms": round(attn_avg_ms, 5)},
+        "write": wres,
+        "gpu_launches": launches_per_step * args.steps + wres["launches"] * (1 if rank == 0 else 0),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = _cpu_baseline("decode", args)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def _write_bench(torch, kv, workloads, dev, stream, args):
+    wl = workloads.write_throughput(seed=args.seed)
+    H, d = wl.num_kv_heads, wl.head_size
+    signs = torch.from_numpy(wl.signs).to(dev)
+    k, v = wl.key.to(dev), wl.value.to(dev)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    cache = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+    per_tok = 2 * H * d * k.element_size() + 2 * H * kv.kv_int4_row_bytes(d) + 8
+    nbytes = wl.num_tokens * per_tok
+    reps = max(3, args.steps // 4)
+    for _ in range(max(3, args.warmup)):
+        kv.kv_int4_write(k, v, slots, signs, cache)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        kv.kv_int4_write(k, v, slots, signs, cache)   # inputs (268 MB) exceed L2
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    peak, kind = _peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "write_throughput: 65536 tokens, 8 kv heads, head 128, bf16, magnitudes 10^U(-2,2), "
+                        "random slots over 8192 blocks of 16",
+            "tokens_per_s": round(wl.num_tokens / (ms * 1e-3), 1), "GB/s": round(gbs, 1), "ms_per_call": round(ms, 5),
+            "bytes_per_call": nbytes, "launches": reps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": _traffic("write_throughput"),
+                         "peak_source": kind}}
+
+
+# ------------------------------------------------------------------------------- CPU oracle
+
+def _cpu_baseline(kind, args, nsample=None):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    n = nsample if nsample is not None else (2 if kind == "decode" else 2048)
+    res = subprocess.run([sys.executable, "-m", "oracle.timing", kind, str(n), str(args.seed)], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=900)
+    if res.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": res.stderr[-400:]}
+    r = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": round(r["bytes"] / r["seconds"] / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{r['what']} of the GQA decode workload (write their tokens + attention), "
+                      f"{r['seconds']:.2f} s single-threaded" if kind == "decode" else r["what"],
+            "seconds": round(r["seconds"], 3)}
+
+
+def _reference_arm(args):
+    """The CPU oracle, as it stands, on the GPU arm's workload and metric.  Each step is a bounded
+    sample: one (sequence, kv head) of the GQA decode batch, round-robin, truncated to the first n
+    tokens so that warm-up + steps take about two minutes whatever --steps is.  A step writes the
+    sample's tokens into the oracle's cache and runs the oracle attention for that kv head's query
+    heads; its bytes are the packed K/V rows (+ Q/O) it covers."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    wl = workloads.gqa_decode_batch(seed=args.seed)
+    S, H, G, d = len(wl.seq_lens), wl.num_kv_heads, wl.num_q_heads // wl.num_kv_heads, wl.head_size
+    rb = d // 2 + 4
+
+    def one(i, ntok):
+        b, h = i % S, (i // S) % H
+        L = min(int(wl.seq_lens[b]), ntok)
+        rows = np.arange(wl.token_start[b], wl.token_start[b] + L)
+        nb = (L + 15) // 16
+        table = np.arange(nb, dtype=np.int32)[None]
+        cache = np.zeros(oracle.cache_shape(nb, 16, 1, d), np.uint8)
+        q = wl.query[b:b + 1, h * G:(h + 1) * G]
+        t0 = time.perf_counter()
+        oracle.write(wl.key[rows, h:h + 1], wl.value[rows, h:h + 1], np.arange(L, dtype=np.int64), wl.signs, cache)
+        oracle.paged_attention(q, cache, table, np.array([L], np.int32), np.array([0, 1], np.int32),
+                               wl.softmax_scale, wl.signs)
+        return time.perf_counter() - t0, L * 2 * rb + 2 * G * d * 2
+
+    t_start = time.perf_counter()
+    dt, _ = one(0, 4096)
+    per_tok = dt / min(int(wl.seq_lens[0]), 4096)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    ntok = int(max(16, min(4096, budget / max(per_tok, 1e-9))))
+    for i in range(args.warmup):
+        one(i, ntok)
+    secs, nbytes = 0.0, 0
+    for i in range(args.steps):
+        s_, b_ = one(i, ntok)
+        secs += s_
+        nbytes += b_
+    value = nbytes / secs / 1e9
+    sample = f"1 (sequence, kv head) of the GQA decode batch per step, first {ntok} tokens, round-robin"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 write / f64 attention",
+            "data": "synthetic",
+            "config": {"workload": "gqa_decode_batch (the GPU arm's workload); oracle on a bounded sample per step",
+                       "sample_tokens": ntok},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - t_start, 2)}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        # the oracle runs single-threaded; fix BLAS threads before numpy loads
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        _reference_arm(args)
+    else:
+        _gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

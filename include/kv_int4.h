@@ -1,0 +1,175 @@
+/*
+ * kv_int4.h -- C ABI of the INT4 per-(token, head) KV-cache library for NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, both asynchronous on the caller's CUDA stream:
+ *
+ *   kv_int4_write            rotate, quantise and pack new K/V head vectors into a paged cache;
+ *   kv_int4_paged_attention  causal attention of queries over that cache (decode, split-KV
+ *                            segments, chunked prefill).
+ *
+ * The caller owns every buffer.  The library never allocates device or host memory: the
+ * attention's split-KV partials live in a caller-provided workspace whose size
+ * kv_int4_attention_workspace_bytes() reports.  All pointers are DEVICE pointers unless a
+ * comment says otherwise, and must stay valid until the stream reaches the launched work.
+ *
+ * Errors: every entry point validates its arguments on the host and returns a status without
+ * launching anything when they are wrong.  Problems only visible on the device (a slot or block
+ * id past the end of the cache, a query chunk longer than its sequence, a sign that is not
+ * +-1, a pipeline wait that ran out of time) never trap: the element is skipped, and a counter
+ * in a device-resident status array is incremented (kv_int4_read_device_status).
+ *
+ * The method (page titles and sections of the sources):
+ *  - "[Feature] Triton INT4 / INT2 per-token-head KV cache quantization" (vLLM PR #40633),
+ *    description: random Hadamard pre-rotation, asymmetric 4-bit codes with one fp32 scale per
+ *    (token, head), the 4-bit zero-point hidden in the low 4 mantissa bits of that scale, the
+ *    asymmetry corrected on the score side, packed K/V read with split dot products;
+ *    review notes: head size must be a power of two, quantise with the truncated scale.
+ *  - "PR #40835 report", get_kv_cache_shape: cache shape
+ *    (num_blocks, 2, block_size, num_kv_heads, head_size / 2 + 4), uint8.
+ *  - "tests/quantization/test_per_token_kv_cache.py": the write call
+ *    (key, value, caches, slot_mapping; slot < 0 = padding, skipped) and the unified-attention
+ *    call (q, cache, cu_seqlens_q, seqused_k, max_seqlen_q, max_seqlen_k, softmax_scale,
+ *    causal=True, block_table, split-KV segment buffers).
+ */
+#ifndef KV_INT4_H
+#define KV_INT4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* kv_int4_stream_t;
+
+typedef enum {
+    KV_INT4_OK = 0,
+    KV_INT4_EINVAL = 1,        /* null pointer, negative or inconsistent size                  */
+    KV_INT4_EUNSUPPORTED = 2,  /* head size, block size, head grouping or dtype not built        */
+    KV_INT4_EALIGN = 3,        /* a pointer is not 16-byte aligned                               */
+    KV_INT4_EWORKSPACE = 4,    /* workspace missing or smaller than the reported size            */
+    KV_INT4_ECUDA = 5          /* a CUDA runtime or driver call failed (launch, attribute, ...)  */
+} kv_int4_status;
+
+typedef enum { KV_INT4_F16 = 0, KV_INT4_BF16 = 1, KV_INT4_F32 = 2 } kv_int4_dtype;
+
+/* Indices into the device status array (kv_int4_read_device_status). */
+enum {
+    KV_INT4_STAT_SLOT_OUT_OF_RANGE = 0,  /* write: slot >= num_blocks * block_size (row skipped)      */
+    KV_INT4_STAT_BLOCK_OUT_OF_RANGE = 1, /* attention: block id outside [0, num_blocks) (block skipped) */
+    KV_INT4_STAT_BAD_SEQUENCE = 2,       /* attention: query chunk longer than its sequence, or a
+                                            sequence longer than its block table                        */
+    KV_INT4_STAT_WAIT_TIMEOUT = 3,       /* a pipeline wait gave up; the CTA's output is not valid      */
+    KV_INT4_STAT_BAD_SIGN = 4,           /* a rotation sign that is not exactly +1.0f or -1.0f           */
+    KV_INT4_STAT_COUNT = 8
+};
+
+/* Bytes of one cached (token, head) row: head_size/2 bytes of codes, then the fp32 scale word. */
+int32_t kv_int4_row_bytes(int32_t head_size);
+
+/*
+ * kv_int4_write -- encode num_tokens new K and V head vectors into the paged cache.
+ *
+ * For every token t with slot = slot_mapping[t] >= 0, every kv head h, and plane p (0 = K, 1 = V)
+ * with x = the input vector upcast exactly to fp32:
+ *   1. y = c * H_d * (D x): D = diag(rht_signs), H_d the natural-order (Sylvester) Walsh-Hadamard
+ *      matrix, c = fp32(1/sqrt(head_size)); butterflies at strides 1, 2, ..., head_size/2 in fp32
+ *      round-to-nearest-even, then one multiply by c per element;
+ *   2. s = max(fp32((max y - min y) / 15), 1e-6); s' = s with the low 4 mantissa bits cleared;
+ *   3. zp = clamp(rint(fp32(-min y / s')), 0, 15);
+ *   4. code_i = clamp(nearest-even integer of the exact value y_i * fp32(1/s') + zp, 0, 15);
+ *   5. row byte j = code_{2j} | code_{2j+1} << 4 (j < head_size/2), then the 32-bit word
+ *      bits(s') | zp little-endian, stored at cache[slot / block_size][p][slot % block_size][h].
+ * The bytes written are bit-exact with that definition.
+ *
+ * k, v          [num_tokens, num_kv_heads, head_size] contiguous, dtype F16 or BF16; 16-B aligned.
+ * slot_mapping  [num_tokens] int64; < 0 = padding token (skipped); >= num_blocks*block_size is
+ *               skipped and counted (KV_INT4_STAT_SLOT_OUT_OF_RANGE).
+ * rht_signs     [head_size] float, each exactly +1.0f or -1.0f (only the sign bit is used; other
+ *               values are counted as KV_INT4_STAT_BAD_SIGN).  The same vector must be passed to
+ *               kv_int4_paged_attention.
+ * cache         (num_blocks, 2, block_size, num_kv_heads, head_size/2 + 4) uint8, 16-B aligned.
+ * Supported: head_size in {64, 128}; block_size 16; num_kv_heads in 1..64.
+ * num_tokens == 0 launches nothing and returns KV_INT4_OK.
+ */
+kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
+                             const float* rht_signs, uint8_t* cache, int64_t num_blocks,
+                             int32_t block_size, kv_int4_stream_t stream);
+
+/*
+ * Bytes of workspace kv_int4_paged_attention needs for these sizes (same arguments as the
+ * attention call; segment_len 0 = the library's choice).  Returns 0 when the arguments are invalid
+ * or no workspace is needed.
+ */
+size_t kv_int4_attention_workspace_bytes(int64_t num_q_tokens, int32_t num_q_heads,
+                                         int32_t head_size, int32_t num_seqs, int32_t max_seq_len,
+                                         int32_t segment_len);
+
+/*
+ * The KV-token length of one split-KV segment that kv_int4_paged_attention uses for these sizes
+ * (segment_len 0 = the library's choice; otherwise segment_len itself).  0 if invalid.
+ */
+int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len);
+
+/*
+ * kv_int4_paged_attention -- causal attention over the INT4 cache.
+ *
+ * Sequence b has seq_lens[b] cached tokens (this step's tokens already written) and the query
+ * rows query_start_loc[b] .. query_start_loc[b+1]-1 (like cu_seqlens_q); its t-th query sits at
+ * position seq_lens[b] - q_len_b + t and sees keys 0 .. that position.  Query head g reads kv
+ * head g / (num_q_heads / num_kv_heads).  With x_K, x_V the cached rows decoded as
+ * (code - zp) * s' and un-rotated, out = softmax(softmax_scale * q . x_K) x_V.
+ *
+ * Computation: Q is rotated once (q' = R q); scores are dot products of q' with the raw codes
+ * in the rotated domain, the zero-point is subtracted from the codes and the scale s' applied per
+ * key; an online softmax accumulates P V in the rotated domain and the result is un-rotated
+ * (out = R^T o).  Sequences with one query token take the decode kernel, which splits long
+ * contexts into segments of segment_len tokens and combines the per-segment partials; sequences
+ * with more than one query token take the chunked-prefill kernel.
+ *
+ * q                [num_q_tokens, num_q_heads, head_size], q_dtype F16 or BF16, 16-B aligned.
+ * cache            as written by kv_int4_write.
+ * block_tables     [num_seqs, max_blocks_per_seq] int32.
+ * seq_lens         [num_seqs] int32; query_start_loc [num_seqs + 1] int32 (cumulative).
+ * max_query_len    host int: max over b of q_len_b (1 for a pure decode batch).
+ * max_seq_len      host int: >= max over b of seq_lens[b]; sizes the segment grid.
+ * rht_signs        the vector passed to kv_int4_write.
+ * segment_len      KV tokens per split-KV segment, a multiple of 16; 0 = library's choice.
+ * out              [num_q_tokens, num_q_heads, head_size], out_dtype F16, BF16 or F32.
+ * workspace        >= kv_int4_attention_workspace_bytes(...) bytes, 16-B aligned; may be NULL
+ *                  when that size is 0.  Overlapping calls must not share a workspace.
+ * Supported: head_size in {64, 128}; block_size 16; num_kv_heads in {1, 2, 4, 8};
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}.  An empty context (seq_len 0) yields zeros.
+ */
+kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                       int32_t num_q_heads, const uint8_t* cache,
+                                       int64_t num_blocks, int32_t num_kv_heads,
+                                       int32_t head_size, int32_t block_size,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, const int32_t* query_start_loc,
+                                       int32_t num_seqs, int32_t max_query_len,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       const float* rht_signs, int32_t segment_len, void* out,
+                                       kv_int4_dtype out_dtype, void* workspace,
+                                       size_t workspace_bytes, kv_int4_stream_t stream);
+
+/*
+ * Copy the current device's status counters (KV_INT4_STAT_COUNT uint32 values) to the HOST array
+ * counts.  Synchronises the stream first.  The counters keep counting until cleared.
+ */
+kv_int4_status kv_int4_read_device_status(uint32_t* counts, kv_int4_stream_t stream);
+
+/* Zero the current device's status counters (asynchronous on the stream). */
+kv_int4_status kv_int4_clear_device_status(kv_int4_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* kv_int4_status_string(kv_int4_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV_INT4_H */

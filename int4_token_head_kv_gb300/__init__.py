@@ -1,0 +1,169 @@
+"""INT4 per-(token, head) KV cache for NVIDIA GB300: Python binding of the C ABI in include/kv_int4.h.
+
+The functions below have the C entry points' names.  They only marshal arguments: check that the
+torch tensors are CUDA, contiguous and of the right dtype and shape, then pass raw device pointers
+and the current CUDA stream to ``libkv_int4.so``.  Every step of the write and of the attention
+runs in that library's kernels; there is no fallback.  Importing this package fails loudly when the
+library has not been built (``python -m int4_token_head_kv_gb300._build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libkv_int4.so")
+
+KV_INT4_F16, KV_INT4_BF16, KV_INT4_F32 = 0, 1, 2
+STAT_NAMES = ["slot_out_of_range", "block_out_of_range", "bad_sequence", "wait_timeout", "bad_sign"]
+_STAT_COUNT = 8
+_DTYPES = {torch.float16: KV_INT4_F16, torch.bfloat16: KV_INT4_BF16, torch.float32: KV_INT4_F32}
+
+
+class KVInt4Error(RuntimeError):
+    """A non-OK status returned by the C library."""
+
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn}: {message} (status {status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m int4_token_head_kv_gb300._build` "
+                          "(the CUDA library is required; there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, szt = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.kv_int4_row_bytes.argtypes = [i32]
+    lib.kv_int4_row_bytes.restype = i32
+    lib.kv_int4_status_string.argtypes = [ctypes.c_int]
+    lib.kv_int4_status_string.restype = ctypes.c_char_p
+    lib.kv_int4_write.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, vp, vp, i64, i32, vp]
+    lib.kv_int4_write.restype = ctypes.c_int
+    lib.kv_int4_attention_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.kv_int4_attention_workspace_bytes.restype = szt
+    lib.kv_int4_attention_segment_len.argtypes = [i32, i32, i32]
+    lib.kv_int4_attention_segment_len.restype = i32
+    lib.kv_int4_paged_attention.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp,
+                                            i32, i32, i32, f32, vp, i32, vp, ctypes.c_int, vp, szt, vp]
+    lib.kv_int4_paged_attention.restype = ctypes.c_int
+    lib.kv_int4_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.kv_int4_read_device_status.restype = ctypes.c_int
+    lib.kv_int4_clear_device_status.argtypes = [vp]
+    lib.kv_int4_clear_device_status.restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise KVInt4Error(fn, status, _lib.kv_int4_status_string(status).decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _cuda(t: torch.Tensor, name: str, dtypes=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    return t
+
+
+def kv_int4_row_bytes(head_size: int) -> int:
+    return int(_lib.kv_int4_row_bytes(head_size))
+
+
+def kv_int4_cache_shape(num_blocks: int, block_size: int, num_kv_heads: int, head_size: int):
+    """Shape of the packed cache: (num_blocks, 2, block_size, num_kv_heads, head_size/2 + 4) uint8."""
+    return (num_blocks, 2, block_size, num_kv_heads, kv_int4_row_bytes(head_size))
+
+
+def kv_int4_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor, rht_signs: torch.Tensor,
+                  kv_cache: torch.Tensor, stream=None) -> None:
+    """Rotate, quantise and pack ``key``/``value`` [T, H, d] into ``kv_cache`` at ``slot_mapping``."""
+    _cuda(key, "key", (torch.float16, torch.bfloat16))
+    _cuda(value, "value", (key.dtype,))
+    _cuda(slot_mapping, "slot_mapping", (torch.int64,))
+    _cuda(rht_signs, "rht_signs", (torch.float32,))
+    _cuda(kv_cache, "kv_cache", (torch.uint8,))
+    if key.dim() != 3 or value.shape != key.shape:
+        raise ValueError("key and value must both be [num_tokens, num_kv_heads, head_size]")
+    T, H, d = key.shape
+    if slot_mapping.shape != (T,) or rht_signs.shape != (d,):
+        raise ValueError("slot_mapping must be [num_tokens] and rht_signs [head_size]")
+    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.shape[3] != H or \
+            kv_cache.shape[4] != kv_int4_row_bytes(d):
+        raise ValueError(f"kv_cache must be {kv_int4_cache_shape('NB', 'bs', H, d)}")
+    st = _lib.kv_int4_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
+                            rht_signs.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2],
+                            _stream(stream))
+    _check("kv_int4_write", st)
+
+
+def kv_int4_attention_segment_len(num_seqs: int, max_seq_len: int, segment_len: int = 0) -> int:
+    return int(_lib.kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len))
+
+
+def kv_int4_attention_workspace_bytes(num_q_tokens: int, num_q_heads: int, head_size: int, num_seqs: int,
+                                      max_seq_len: int, segment_len: int = 0) -> int:
+    return int(_lib.kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
+                                                      max_seq_len, segment_len))
+
+
+def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,
+                            seq_lens: torch.Tensor, query_start_loc: torch.Tensor, softmax_scale: float,
+                            rht_signs: torch.Tensor, max_query_len: int, max_seq_len: int, out=None,
+                            out_dtype=None, segment_len: int = 0, workspace=None, stream=None) -> torch.Tensor:
+    """Causal paged attention of ``query`` [Nq, Hq, d] over the INT4 cache; returns ``out``."""
+    _cuda(query, "query", (torch.float16, torch.bfloat16))
+    _cuda(kv_cache, "kv_cache", (torch.uint8,))
+    _cuda(block_tables, "block_tables", (torch.int32,))
+    _cuda(seq_lens, "seq_lens", (torch.int32,))
+    _cuda(query_start_loc, "query_start_loc", (torch.int32,))
+    _cuda(rht_signs, "rht_signs", (torch.float32,))
+    Nq, Hq, d = query.shape
+    NB, two, bs, H, rb = kv_cache.shape
+    S = seq_lens.shape[0]
+    if two != 2 or rb != kv_int4_row_bytes(d) or rht_signs.shape != (d,):
+        raise ValueError("kv_cache / rht_signs do not match the query's head size")
+    if query_start_loc.shape != (S + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and query_start_loc [num_seqs + 1]")
+    if out is None:
+        out = torch.empty((Nq, Hq, d), dtype=out_dtype or query.dtype, device=query.device)
+    _cuda(out, "out", tuple(_DTYPES))
+    if out.shape != query.shape:
+        raise ValueError("out must have the query's shape")
+    need = kv_int4_attention_workspace_bytes(Nq, Hq, d, S, max_seq_len, segment_len)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.kv_int4_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H,
+                                      d, bs, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+                                      query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
+                                      float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(),
+                                      _DTYPES[out.dtype], ws_ptr, ws_bytes, _stream(stream))
+    _check("kv_int4_paged_attention", st)
+    return out
+
+
+def kv_int4_read_device_status(stream=None) -> dict:
+    """Synchronise the stream and return the device's status counters by name."""
+    buf = (ctypes.c_uint32 * _STAT_COUNT)()
+    _check("kv_int4_read_device_status", _lib.kv_int4_read_device_status(buf, _stream(stream)))
+    return {name: int(buf[i]) for i, name in enumerate(STAT_NAMES)}
+
+
+def kv_int4_clear_device_status(stream=None) -> None:
+    _check("kv_int4_clear_device_status", _lib.kv_int4_clear_device_status(_stream(stream)))

@@ -1,0 +1,223 @@
+// The C ABI declared in include/kv_int4.h: argument validation on the host, the device status
+// counters, the split-KV segment policy, and kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "../../include/kv_int4.h"
+#include "internal.h"
+
+namespace kvi4 {
+
+// Device status counters (KV_INT4_STAT_*): module-scope device memory, one copy per device that
+// loads the library.  Kernels add to them; the host reads and clears them through the ABI.
+__device__ uint32_t g_status[KV_INT4_STAT_COUNT];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+uint32_t* status_ptr() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<uint32_t*>(ptr);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype_16(kv_int4_dtype d) { return d == KV_INT4_F16 || d == KV_INT4_BF16; }
+
+bool is_pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+kv_int4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KV_INT4_OK : KV_INT4_ECUDA; }
+
+}  // namespace
+
+int num_sms() {
+    const int dev = current_device();
+    if (dev < 0) return 152;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+}  // namespace kvi4
+
+using namespace kvi4;
+
+extern "C" {
+
+int32_t kv_int4_row_bytes(int32_t head_size) { return head_size > 0 ? head_size / 2 + 4 : 0; }
+
+const char* kv_int4_status_string(kv_int4_status s) {
+    switch (s) {
+        case KV_INT4_OK: return "ok";
+        case KV_INT4_EINVAL: return "invalid argument (null pointer, negative or inconsistent size)";
+        case KV_INT4_EUNSUPPORTED: return "unsupported head size, block size, head grouping or dtype";
+        case KV_INT4_EALIGN: return "pointer not 16-byte aligned";
+        case KV_INT4_EWORKSPACE: return "workspace missing or too small";
+        case KV_INT4_ECUDA: return "CUDA call failed";
+    }
+    return "unknown status";
+}
+
+kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
+                             const float* rht_signs, uint8_t* cache, int64_t num_blocks, int32_t block_size,
+                             kv_int4_stream_t stream) {
+    if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0) return KV_INT4_EINVAL;
+    if (head_size != 64 && head_size != 128) return KV_INT4_EUNSUPPORTED;
+    if (block_size != kBlockSize || num_kv_heads > 64 || !valid_dtype_16(dtype)) return KV_INT4_EUNSUPPORTED;
+    if (num_tokens == 0) return KV_INT4_OK;
+    if (!k || !v || !slot_mapping || !rht_signs || !cache) return KV_INT4_EINVAL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(cache)) return KV_INT4_EALIGN;
+    WriteParams p;
+    p.k = k;
+    p.v = v;
+    p.slots = slot_mapping;
+    p.signs = rht_signs;
+    p.cache = cache;
+    p.status = status_ptr();
+    p.num_tokens = num_tokens;
+    p.num_slots = num_blocks * block_size;
+    p.H = num_kv_heads;
+    p.c = (float)(1.0 / std::sqrt((double)head_size));
+    return from_cuda(launch_write(p, head_size, dtype == KV_INT4_BF16 ? DType::BF16 : DType::F16,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
+    if (num_seqs < 0 || max_seq_len < 0 || segment_len < 0) return 0;
+    if (segment_len > 0) return (segment_len % kBlockSize == 0) ? segment_len : 0;
+    // Enough (sequence, segment) CTAs to keep two per SM busy, in multiples of 256 tokens.
+    const int64_t target = 2ll * num_sms();
+    const int64_t work = (int64_t)num_seqs * (int64_t)max_seq_len;
+    int64_t seg = (work + target - 1) / (target > 0 ? target : 1);
+    seg = ((seg + 255) / 256) * 256;
+    if (seg < 256) seg = 256;
+    if (seg > (1 << 20)) seg = 1 << 20;
+    return (int32_t)seg;
+}
+
+size_t kv_int4_attention_workspace_bytes(int64_t num_q_tokens, int32_t num_q_heads, int32_t head_size,
+                                         int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
+    if (num_q_tokens < 0 || num_q_heads <= 0 || head_size <= 0 || num_seqs < 0 || max_seq_len < 0) return 0;
+    const int32_t seg = kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len);
+    if (seg <= 0) return 0;
+    const int64_t nseg = ((int64_t)max_seq_len + seg - 1) / seg;
+    if (nseg <= 1) return 0;
+    // partial outputs [num_seqs, Hq, nseg, D] then (max, sum) pairs [num_seqs, Hq, nseg, 2]
+    const int64_t units = (int64_t)num_seqs * num_q_heads * nseg;
+    const size_t o_bytes = (size_t)units * head_size * 4;
+    return ((o_bytes + 255) & ~(size_t)255) + (size_t)units * 2 * 4;
+}
+
+kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                       int32_t num_q_heads, const uint8_t* cache, int64_t num_blocks,
+                                       int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                                       int32_t max_query_len, int32_t max_seq_len, float softmax_scale,
+                                       const float* rht_signs, int32_t segment_len, void* out,
+                                       kv_int4_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                       kv_int4_stream_t stream) {
+    if (num_q_tokens < 0 || num_seqs < 0 || num_blocks < 0 || max_query_len < 0 || max_seq_len < 0 ||
+        max_blocks_per_seq < 0 || segment_len < 0)
+        return KV_INT4_EINVAL;
+    if (head_size != 64 && head_size != 128) return KV_INT4_EUNSUPPORTED;
+    if (block_size != kBlockSize) return KV_INT4_EUNSUPPORTED;
+    if (!is_pow2_in(num_kv_heads, 1, 8) || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return KV_INT4_EUNSUPPORTED;
+    const int G = num_q_heads / num_kv_heads;
+    if (!is_pow2_in(G, 1, 8)) return KV_INT4_EUNSUPPORTED;
+    if (!valid_dtype_16(q_dtype) || !(valid_dtype_16(out_dtype) || out_dtype == KV_INT4_F32))
+        return KV_INT4_EUNSUPPORTED;
+    if (segment_len % kBlockSize != 0 || num_seqs > 65535) return KV_INT4_EUNSUPPORTED;
+    if (!(softmax_scale == softmax_scale)) return KV_INT4_EINVAL;
+    if (num_q_tokens == 0 || num_seqs == 0) return KV_INT4_OK;
+    if (!q || !cache || !block_tables || !seq_lens || !query_start_loc || !rht_signs || !out) return KV_INT4_EINVAL;
+    if (max_query_len < 1 || max_blocks_per_seq < 1) return KV_INT4_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(cache)) return KV_INT4_EALIGN;
+
+    const int32_t seg = kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len);
+    if (seg <= 0) return KV_INT4_EINVAL;
+    const int64_t nseg = max_seq_len > 0 ? ((int64_t)max_seq_len + seg - 1) / seg : 1;
+    if (nseg > 65535ll * 1024) return KV_INT4_EUNSUPPORTED;
+    const size_t need = kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
+                                                          max_seq_len, segment_len);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KV_INT4_EWORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return KV_INT4_EALIGN;
+
+    AttnParams p;
+    p.q = q;
+    p.cache = cache;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.qsl = query_start_loc;
+    p.signs = rht_signs;
+    p.out = out;
+    const int64_t units = (int64_t)num_seqs * num_q_heads * nseg;
+    p.ws_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
+    p.ws_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                  (((size_t)units * head_size * 4 + 255) & ~(size_t)255))
+                       : nullptr;
+    p.status = status_ptr();
+    p.num_blocks = num_blocks;
+    p.num_q_tokens = num_q_tokens;
+    p.num_seqs = num_seqs;
+    p.max_query_len = max_query_len;
+    p.H = num_kv_heads;
+    p.G = G;
+    p.Hq = num_q_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.seg_len = seg;
+    p.nseg_max = (int)nseg;
+    p.softmax_scale = softmax_scale;
+    p.c = (float)(1.0 / std::sqrt((double)head_size));
+
+    const DType qd = q_dtype == KV_INT4_BF16 ? DType::BF16 : DType::F16;
+    const DType od = out_dtype == KV_INT4_BF16 ? DType::BF16 : (out_dtype == KV_INT4_F16 ? DType::F16 : DType::F32);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode(p, head_size, qd, od, s);
+    if (e == cudaSuccess && nseg > 1) e = launch_combine(p, head_size, od, s);
+    if (e == cudaSuccess && max_query_len > 1) e = launch_prefill(p, head_size, max_query_len, qd, od, s);
+    return from_cuda(e);
+}
+
+kv_int4_status kv_int4_read_device_status(uint32_t* counts, kv_int4_stream_t stream) {
+    if (!counts) return KV_INT4_EINVAL;
+    uint32_t* ptr = status_ptr();
+    if (!ptr) return KV_INT4_ECUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KV_INT4_ECUDA;
+    return from_cuda(cudaMemcpy(counts, ptr, sizeof(uint32_t) * KV_INT4_STAT_COUNT, cudaMemcpyDeviceToHost));
+}
+
+kv_int4_status kv_int4_clear_device_status(kv_int4_stream_t stream) {
+    uint32_t* ptr = status_ptr();
+    if (!ptr) return KV_INT4_ECUDA;
+    return from_cuda(cudaMemsetAsync(ptr, 0, sizeof(uint32_t) * KV_INT4_STAT_COUNT,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

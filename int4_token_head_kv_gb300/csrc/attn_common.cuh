@@ -1,0 +1,118 @@
+// Pieces shared by the decode and prefill attention kernels over the INT4 cache.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "device.cuh"
+
+namespace kvi4 {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegBig = -1.0e30f;   // "no key seen yet" running max (finite, so exp2 never sees inf - inf)
+
+template <typename T>
+__device__ __forceinline__ float load_elem(const void* base, int64_t i);
+template <>
+__device__ __forceinline__ float load_elem<__half>(const void* base, int64_t i) {
+    return __half2float(static_cast<const __half*>(base)[i]);
+}
+template <>
+__device__ __forceinline__ float load_elem<__nv_bfloat16>(const void* base, int64_t i) {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_elem(void* base, int64_t i, float x);
+template <>
+__device__ __forceinline__ void store_elem<__half>(void* base, int64_t i, float x) {
+    static_cast<__half*>(base)[i] = __float2half_rn(x);
+}
+template <>
+__device__ __forceinline__ void store_elem<__nv_bfloat16>(void* base, int64_t i, float x) {
+    static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ void store_elem<float>(void* base, int64_t i, float x) {
+    static_cast<float*>(base)[i] = x;
+}
+
+// Walsh-Hadamard transform (unnormalised, natural order) of a D-vector spread over a warp:
+// lane l holds x[k] = v[l + 32 k].  Strides below 32 pair lanes, larger strides pair slots.
+template <int D>
+__device__ __forceinline__ void warp_fwht(float (&x)[D / 32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[k], h);
+            x[k] = (lane & h) ? (o - x[k]) : (x[k] + o);
+        }
+    }
+#pragma unroll
+    for (int h = 1; h < D / 32; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+            if (k & h) continue;
+            const float a = x[k], b = x[k + h];
+            x[k] = a + b;
+            x[k + h] = a - b;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// Power-of-two prescale that brings max|x| into [2^14, 2^15), so the fp16 copy of the rotated
+// query neither overflows nor loses precision to subnormals.  Returns the exponent e (x * 2^e).
+__device__ __forceinline__ int prescale_exponent(float maxabs) {
+    if (!(maxabs > 0.0f)) return 0;
+    const int ex = (int)((__float_as_uint(maxabs) >> 23) & 0xFF) - 127;
+    int e = 14 - ex;
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Rotate one query vector q (original domain) for the packed read path:
+//   v = H_d (D q) (unnormalised), e = prescale exponent, qh = fp16(v * 2^e),
+//   alpha = c * 2^-e * softmax_scale * log2(e)  (raw score -> log2-domain logit, before the
+//   key's scale s' is applied).
+// The warp writes qh (D halves) to shared memory and returns alpha (all lanes).
+template <int D, typename QT>
+__device__ __forceinline__ float rotate_query(const void* q, int64_t qoff, const float* sgn, __half* qh, float c,
+                                              float softmax_scale) {
+    const int lane = threadIdx.x & 31;
+    float x[D / 32];
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) x[k] = load_elem<QT>(q, qoff + lane + 32 * k) * sgn[lane + 32 * k];
+    warp_fwht<D>(x);
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) m = fmaxf(m, fabsf(x[k]));
+    const int e = prescale_exponent(warp_max(m));
+    const float sc = exp2i(e);
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) qh[lane + 32 * k] = __float2half_rn(x[k] * sc);
+    return c * exp2i(-e) * softmax_scale * kLog2e;
+}
+
+// Un-rotate an accumulated output vector held by a warp (lane l: x[k] = o[l + 32 k]) and store it:
+// out = c * D * H_d * (o * inv_l).
+template <int D, typename OT>
+__device__ __forceinline__ void unrotate_store(float (&x)[D / 32], float inv_l, const float* sgn, float c, void* out,
+                                               int64_t ooff) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) x[k] *= inv_l;
+    warp_fwht<D>(x);
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) store_elem<OT>(out, ooff + lane + 32 * k, x[k] * c * sgn[lane + 32 * k]);
+}
+
+}  // namespace kvi4

@@ -1,0 +1,450 @@
+// Decode attention over the INT4 cache (one query token per sequence), with split-KV segments.
+//
+// Method ("[Feature] Triton INT4 / INT2 per-token-head KV cache quantization", description of the
+// packed read path): Q is rotated with the same random Hadamard transform as K and V, scores are
+// dot products of the rotated query with the raw 4-bit codes, the asymmetry (zero-point) is
+// corrected per key and the per-key scale applied, an online softmax accumulates P V in the
+// rotated domain, and the output is un-rotated.  Long contexts are split into segments whose
+// (max, sum, accumulator) partials are combined afterwards ("3D" segment reduction of the
+// unified-attention interface, test_triton_unified_attention_per_token_head_scale).
+//
+// GB300 design:
+//  * One CTA per (sequence, segment) covers ALL kv heads, so each 16-token block is one
+//    contiguous 16-byte-aligned region (K plane then V plane, 2 * 16 * H * (D/2+4) bytes) that a
+//    producer warp streams into a 4-stage shared-memory ring with 1-D bulk async copies
+//    (cp.async.bulk + mbarrier transaction counts, L2 evict-first).
+//  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block when H < 8).
+//    Scores S^T[16 tokens x 8 heads] = (K - zp)[16 x D] . Q'^T come from mma.sync m16n8k16 on
+//    fp16 operands built straight from the packed bytes (codes and code - zp are exact in fp16);
+//    the zero-point is subtracted while unpacking, which is the sum(Q) * zp correction folded in.
+//  * P^T is transposed in registers (movmatrix) into the B operand of O^T[D x 8] += (V - zp)^T P^T.
+//    V's per-key scale is folded into P (w = p * s'_V * 2^-E, E a running max exponent, so the fp16
+//    weights never overflow).
+#include "attn_common.cuh"
+
+namespace kvi4 {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 4;
+
+struct DecodeSmem {
+    uint32_t stage_bytes;   // one block (K + V planes)
+    uint32_t state_off;     // start of barriers etc. (after the ring / epilogue state overlay)
+    uint32_t total;
+};
+
+template <int D>
+__host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
+    DecodeSmem s;
+    s.stage_bytes = 2u * kBlockSize * (uint32_t)H * Geo<D>::RB;
+    const uint32_t ring = kStages * s.stage_bytes;
+    const uint32_t state = kConsumerWarps * 8u * D * 4u;
+    s.state_off = ((ring > state ? ring : state) + 127u) & ~127u;
+    const uint32_t tail = 2u * kStages * 8u      // full / empty barriers
+                          + kStages * 4u + 16u     // valid flags, abort flag
+                          + D * 4u                 // signs
+                          + (uint32_t)Hq * 4u      // alpha
+                          + 2u * kConsumerWarps * 8u * 4u  // per-warp (m, l)
+                          + (uint32_t)Hq * D * 2u;  // rotated fp16 queries
+    s.total = s.state_off + ((tail + 127u) & ~127u);
+    return s;
+}
+
+template <int D, typename QT, typename OT>
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ AttnParams p) {
+    using Gm = Geo<D>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int seg = blockIdx.x, seq = blockIdx.y;
+    const int q0 = __ldg(p.qsl + seq);
+    if (__ldg(p.qsl + seq + 1) - q0 != 1) return;   // not a decode sequence
+    if (q0 < 0 || (int64_t)q0 >= p.num_q_tokens) {
+        if (seg == 0 && threadIdx.x == 0) count_status(p.status, 2);
+        return;
+    }
+    const int H = p.H, G = p.G, Hq = p.Hq;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int L = __ldg(p.seq_lens + seq);
+    const int Lmax = min(p.max_blocks_per_seq * kBlockSize, p.nseg_max * p.seg_len);
+    if (L > Lmax) {   // longer than its block table or than the max_seq_len the grid was sized for
+        if (seg == 0 && threadIdx.x == 0) count_status(p.status, 2);
+        L = Lmax;
+    }
+    if (L <= 0) {   // empty context: zero output
+        if (seg == 0) {
+            for (int i = threadIdx.x; i < Hq * D; i += blockDim.x) store_elem<OT>(p.out, (int64_t)q0 * Hq * D + i, 0.0f);
+        }
+        return;
+    }
+    const int S = p.seg_len;
+    const int tok_begin = seg * S;
+    if (tok_begin >= L) return;
+    const int tok_end = min(L, tok_begin + S);
+    const int nseg = (L + S - 1) / S;
+    const int blk_first = tok_begin / kBlockSize;
+    const int nblk = (tok_end + kBlockSize - 1) / kBlockSize - blk_first;
+
+    const DecodeSmem lay = decode_smem_layout<D>(H, Hq);
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.state_off);
+    uint64_t* empty = full + kStages;
+    int* valid = reinterpret_cast<int*>(empty + kStages);
+    int* abort_flag = valid + kStages;
+    float* sgn = reinterpret_cast<float*>(abort_flag + 4);
+    float* alpha = sgn + D;
+    float* st_m = alpha + Hq;
+    float* st_l = st_m + kConsumerWarps * 8;
+    __half* qh = reinterpret_cast<__half*>(st_l + kConsumerWarps * 8);
+    float* st_o = reinterpret_cast<float*>(smem);   // epilogue overlay of the ring
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
+    __syncthreads();
+
+    const uint8_t* seq_cache = p.cache;
+    const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + blk_first;
+    const uint32_t stage_bytes = lay.stage_bytes;
+    uint64_t policy = 0;
+    int issued = 0;
+    auto produce = [&](int i) {
+        const int st = i % kStages;
+        const int blk = __ldg(table + i);
+        const bool ok = blk >= 0 && (int64_t)blk < p.num_blocks;
+        valid[st] = ok ? 1 : 0;
+        if (ok) {
+            mbar_arrive_expect_tx(&full[st], stage_bytes);
+            bulk_copy_g2s(ring + (size_t)st * stage_bytes, seq_cache + (int64_t)blk * stage_bytes, stage_bytes, &full[st],
+                          policy);
+        } else {
+            count_status(p.status, 1);
+            mbar_arrive(&full[st]);
+        }
+    };
+    if (warp == kConsumerWarps && lane == 0) {
+        policy = policy_evict_first();
+        for (; issued < min(kStages, nblk); ++issued) produce(issued);
+    }
+
+    // Rotate this sequence's query (all Hq heads) into fp16 + per-head logit multiplier.
+    if (warp < kConsumerWarps) {
+        for (int v = warp; v < Hq; v += kConsumerWarps) {
+            const float a = rotate_query<D, QT>(p.q, ((int64_t)q0 * Hq + v) * D, sgn, qh + v * D, p.c, p.softmax_scale);
+            if (lane == 0) alpha[v] = a;
+        }
+    }
+    __syncthreads();
+
+    // consumer state (lives across the role split so that the barriers below are uniform)
+    float o[Gm::MT][4];
+#pragma unroll
+    for (int i = 0; i < Gm::MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    float m0 = kNegBig, m1 = kNegBig, l0 = 0.0f, l1 = 0.0f;
+    uint32_t eref = 0;   // running max biased exponent of V scales seen so far
+    const int g = lane >> 2, t = lane & 3;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            for (; issued < nblk; ++issued) {
+                const int st = issued % kStages;
+                if (!mbar_wait(&empty[st], ((issued / kStages) - 1) & 1)) {
+                    count_status(p.status, 3);
+                    atomicExch(abort_flag, 1);
+                    break;
+                }
+                if (*(volatile int*)abort_flag) break;
+                produce(issued);
+            }
+            // make sure no copy is still landing in the ring before it is reused / the CTA exits
+            for (int i = max(0, issued - kStages); i < issued; ++i) mbar_wait(&full[i % kStages], (i / kStages) & 1);
+        }
+    } else {
+        // ------------------------------------------------------------------ consumers
+        const int h = warp % H;
+        const int wph = kConsumerWarps / H;
+        const int sub = warp / H;
+        const int tk0 = block_token(g), tk1 = block_token(g + 8);
+
+        // B fragments of Q' for the 16-deep k-steps (see the k-slot mapping in the header comment)
+        uint32_t qb[Gm::KSTEPS][2];
+        {
+            const bool live = g < G;
+            const __half* qv = qh + (h * G + (live ? g : 0)) * D;
+#pragma unroll
+            for (int j = 0; j < Gm::KWPT; ++j) {
+                const int W = t + 4 * j;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int d0 = 8 * W + 2 * hh;
+                    const __half z = __float2half(0.0f);
+                    __half2 b0 = live ? __halves2half2(qv[d0], qv[d0 + 4]) : __halves2half2(z, z);
+                    __half2 b1 = live ? __halves2half2(qv[d0 + 1], qv[d0 + 5]) : __halves2half2(z, z);
+                    qb[2 * j + hh][0] = *reinterpret_cast<uint32_t*>(&b0);
+                    qb[2 * j + hh][1] = *reinterpret_cast<uint32_t*>(&b1);
+                }
+            }
+        }
+        const float al0 = (2 * t < G) ? alpha[h * G + 2 * t] : 0.0f;
+        const float al1 = (2 * t + 1 < G) ? alpha[h * G + 2 * t + 1] : 0.0f;
+
+        for (int i = 0; i < nblk; ++i) {
+            const int st = i % kStages;
+            if (!mbar_wait(&full[st], (i / kStages) & 1)) {
+                if (lane == 0) {
+                    count_status(p.status, 3);
+                    atomicExch(abort_flag, 1);
+                }
+                break;
+            }
+            if ((i % wph) == sub && valid[st]) {
+                const uint8_t* kp = ring + (size_t)st * stage_bytes;
+                const uint8_t* vp = kp + (size_t)kBlockSize * H * Gm::RB;
+                const int tokbase = (blk_first + i) * kBlockSize;
+                const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp + (tk0 * H + h) * Gm::RB);
+                const uint32_t* kr1 = reinterpret_cast<const uint32_t*>(kp + (tk1 * H + h) * Gm::RB);
+                const uint32_t ks0 = kr0[Gm::KW], ks1 = kr1[Gm::KW];
+                // ---- S^T = (K - zp) Q'^T
+                float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                {
+                    const uint32_t z0l = zp_lo_half(ks0 & 15u), z0h = zp_hi_half(ks0 & 15u);
+                    const uint32_t z1l = zp_lo_half(ks1 & 15u), z1h = zp_hi_half(ks1 & 15u);
+                    const uint32_t zl0 = z0l | (z0l << 16), zh0 = z0h | (z0h << 16);
+                    const uint32_t zl1 = z1l | (z1l << 16), zh1 = z1h | (z1h << 16);
+#pragma unroll
+                    for (int j = 0; j < Gm::KWPT; ++j) {
+                        uint32_t a0[4], a1[4];
+                        unpack_word(kr0[t + 4 * j], zl0, zh0, a0);
+                        unpack_word(kr1[t + 4 * j], zl1, zh1, a1);
+                        mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * j][0], qb[2 * j][1]);
+                        mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][0], qb[2 * j + 1][1]);
+                    }
+                }
+                // ---- logits (log2 units), masking, online softmax for heads 2t, 2t+1
+                const bool v0 = tokbase + tk0 < tok_end, v1 = tokbase + tk1 < tok_end;
+                const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
+                const float x0 = v0 ? c[0] * sk0 * al0 : -INFINITY;
+                const float x1 = v0 ? c[1] * sk0 * al1 : -INFINITY;
+                const float x2 = v1 ? c[2] * sk1 * al0 : -INFINITY;
+                const float x3 = v1 ? c[3] * sk1 * al1 : -INFINITY;
+                float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                const float r0 = fast_exp2(m0 - mn0), r1 = fast_exp2(m1 - mn1);
+                const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+                const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                l0 = l0 * r0 + (p0 + p2);
+                l1 = l1 * r1 + (p1 + p3);
+                // ---- V scales: exponent reference so the fp16 weights stay in range
+                const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp + (tk0 * H + h) * Gm::RB);
+                const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp + (tk1 * H + h) * Gm::RB);
+                const uint32_t vs0 = vg0[Gm::KW], vs1 = vg1[Gm::KW];
+                const uint32_t e0 = v0 ? (vs0 >> 23) & 0xFFu : 0u, e1 = v1 ? (vs1 >> 23) & 0xFFu : 0u;
+                const uint32_t eblk = __reduce_max_sync(0xffffffffu, max(e0, e1));
+                float escale = 1.0f;
+                if (eblk > eref) {
+                    // 2^(eref - eblk); 0 when nothing was accumulated yet or the jump underflows
+                    escale = (eref == 0u || eblk - eref > 126u) ? 0.0f : __uint_as_float((127u + eref - eblk) << 23);
+                    eref = eblk;
+                }
+                const float f0 = r0 * escale, f1 = r1 * escale;
+                if (__any_sync(0xffffffffu, f0 != 1.0f || f1 != 1.0f)) {
+#pragma unroll
+                    for (int mt = 0; mt < Gm::MT; ++mt) {
+                        o[mt][0] *= f0;
+                        o[mt][1] *= f1;
+                        o[mt][2] *= f0;
+                        o[mt][3] *= f1;
+                    }
+                }
+                const float wsc = __uint_as_float((254u - eref) << 23);   // 2^(127 - eref)
+                const float sv0 = __uint_as_float(vs0 & 0xFFFFFFF0u) * wsc, sv1 = __uint_as_float(vs1 & 0xFFFFFFF0u) * wsc;
+                const uint32_t xlo = pack_f16x2(v0 ? p0 * sv0 : 0.0f, v0 ? p1 * sv0 : 0.0f);
+                const uint32_t xhi = pack_f16x2(v1 ? p2 * sv1 : 0.0f, v1 ? p3 * sv1 : 0.0f);
+                const uint32_t b0 = movmatrix_trans(xlo), b1 = movmatrix_trans(xhi);
+                // ---- O^T += (V - zp)^T P^T
+                const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp + ((t)*H + h) * Gm::RB);
+                const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp + ((t + 4) * H + h) * Gm::RB);
+                const uint32_t* vr2 = reinterpret_cast<const uint32_t*>(vp + ((t + 8) * H + h) * Gm::RB);
+                const uint32_t* vr3 = reinterpret_cast<const uint32_t*>(vp + ((t + 12) * H + h) * Gm::RB);
+                const uint32_t w0 = vr0[Gm::KW], w1 = vr1[Gm::KW], w2 = vr2[Gm::KW], w3 = vr3[Gm::KW];
+                const uint32_t zl01 = zp_lo_half(w0 & 15u) | (zp_lo_half(w1 & 15u) << 16);
+                const uint32_t zh01 = zp_hi_half(w0 & 15u) | (zp_hi_half(w1 & 15u) << 16);
+                const uint32_t zl23 = zp_lo_half(w2 & 15u) | (zp_lo_half(w3 & 15u) << 16);
+                const uint32_t zh23 = zp_hi_half(w2 & 15u) | (zp_hi_half(w3 & 15u) << 16);
+                if constexpr (D == 128) {
+                    uint32_t ua[8], ub[8], uc[8], ud[8];
+                    unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);           // d = 8g + i, tokens t, t+4
+                    unpack_word_pair(vr0[g + 8], vr1[g + 8], zl01, zh01, ub);   // d = 64 + 8g + i
+                    unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);           // tokens t+8, t+12
+                    unpack_word_pair(vr2[g + 8], vr3[g + 8], zl23, zh23, ud);
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0, b1);
+                } else {
+                    uint32_t ua[8], uc[8];
+                    unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);   // d = 8g + i
+                    unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0, b1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+    }
+    // ---- per-warp state to shared memory, once the ring is drained
+    __syncthreads();
+    if (warp < kConsumerWarps) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const float es = eref ? __uint_as_float(eref << 23) : 0.0f;   // 2^(eref - 127)
+        float* so = st_o + warp * 8 * D;
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            const int dlo = 8 * g + mt;
+            const int dhi = (D == 128) ? 64 + 8 * g + mt : 8 * g + 4 + mt;
+            so[(2 * t) * D + dlo] = o[mt][0] * es;
+            so[(2 * t + 1) * D + dlo] = o[mt][1] * es;
+            so[(2 * t) * D + dhi] = o[mt][2] * es;
+            so[(2 * t + 1) * D + dhi] = o[mt][3] * es;
+        }
+        if (g == 0) {
+            st_m[warp * 8 + 2 * t] = m0;
+            st_m[warp * 8 + 2 * t + 1] = m1;
+            st_l[warp * 8 + 2 * t] = l0;
+            st_l[warp * 8 + 2 * t + 1] = l1;
+        }
+    }
+    __syncthreads();
+
+    // ---- merge the warps of each kv head, then finish (single segment) or store the partial
+    const int wph = kConsumerWarps / H;
+    for (int v = warp; v < Hq; v += kConsumerWarps + 1) {
+        const int h = v / G, col = v % G;
+        float M = kNegBig;
+        for (int s = 0; s < wph; ++s) M = fmaxf(M, st_m[(h + s * H) * 8 + col]);
+        float Lsum = 0.0f;
+        float acc[D / 32];
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
+        for (int s = 0; s < wph; ++s) {
+            const int w = h + s * H;
+            const float wt = fast_exp2(st_m[w * 8 + col] - M);
+            Lsum += wt * st_l[w * 8 + col];
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) acc[k] += wt * st_o[(w * 8 + col) * D + lane + 32 * k];
+        }
+        if (nseg == 1) {
+            unrotate_store<D, OT>(acc, Lsum > 0.0f ? 1.0f / Lsum : 0.0f, sgn, p.c, p.out, ((int64_t)q0 * Hq + v) * D);
+        } else {
+            const int64_t pi = ((int64_t)seq * Hq + v) * p.nseg_max + seg;
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) p.ws_o[pi * D + lane + 32 * k] = acc[k];
+            if (lane == 0) {
+                p.ws_ml[pi * 2] = M;
+                p.ws_ml[pi * 2 + 1] = Lsum;
+            }
+        }
+    }
+}
+
+// Combine the per-segment partials of every decode sequence that spans more than one segment.
+template <int D, typename OT>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p) {
+    __shared__ float sgn[D];
+    for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
+    __syncthreads();
+    const int seq = blockIdx.x;
+    const int v = blockIdx.y * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (v >= p.Hq) return;
+    const int q0 = __ldg(p.qsl + seq);
+    if (__ldg(p.qsl + seq + 1) - q0 != 1) return;
+    if (q0 < 0 || (int64_t)q0 >= p.num_q_tokens) return;
+    const int L = min(__ldg(p.seq_lens + seq), min(p.max_blocks_per_seq * kBlockSize, p.nseg_max * p.seg_len));
+    const int nseg = (L + p.seg_len - 1) / p.seg_len;
+    if (nseg <= 1) return;
+    const int64_t base = ((int64_t)seq * p.Hq + v) * p.nseg_max;
+    float M = kNegBig;
+    for (int s = 0; s < nseg; ++s) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
+    float Lsum = 0.0f;
+    float acc[D / 32];
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
+    for (int s = 0; s < nseg; ++s) {
+        const float wt = fast_exp2(p.ws_ml[(base + s) * 2] - M);
+        Lsum += wt * p.ws_ml[(base + s) * 2 + 1];
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) acc[k] += wt * p.ws_o[(base + s) * D + lane + 32 * k];
+    }
+    unrotate_store<D, OT>(acc, Lsum > 0.0f ? 1.0f / Lsum : 0.0f, sgn, p.c, p.out, ((int64_t)q0 * p.Hq + v) * D);
+}
+
+template <int D, typename QT, typename OT>
+cudaError_t launch_decode_t(const AttnParams& p, cudaStream_t stream) {
+    const DecodeSmem lay = decode_smem_layout<D>(p.H, p.Hq);
+    auto kern = decode_kernel<D, QT, OT>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total);
+    if (err != cudaSuccess) return err;
+    dim3 grid(p.nseg_max, p.num_seqs);
+    kern<<<grid, kDecodeThreads, lay.total, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, typename OT>
+cudaError_t launch_combine_t(const AttnParams& p, cudaStream_t stream) {
+    dim3 grid(p.num_seqs, (p.Hq + 7) / 8);
+    combine_kernel<D, OT><<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, typename QT>
+cudaError_t decode_by_out(const AttnParams& p, DType out_dt, cudaStream_t s) {
+    switch (out_dt) {
+        case DType::F16: return launch_decode_t<D, QT, __half>(p, s);
+        case DType::BF16: return launch_decode_t<D, QT, __nv_bfloat16>(p, s);
+        default: return launch_decode_t<D, QT, float>(p, s);
+    }
+}
+
+template <int D>
+cudaError_t combine_by_out(const AttnParams& p, DType out_dt, cudaStream_t s) {
+    switch (out_dt) {
+        case DType::F16: return launch_combine_t<D, __half>(p, s);
+        case DType::BF16: return launch_combine_t<D, __nv_bfloat16>(p, s);
+        default: return launch_combine_t<D, float>(p, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const AttnParams& p, int head_size, DType q_dt, DType out_dt, cudaStream_t stream) {
+    if (head_size == 128)
+        return q_dt == DType::BF16 ? decode_by_out<128, __nv_bfloat16>(p, out_dt, stream)
+                                   : decode_by_out<128, __half>(p, out_dt, stream);
+    return q_dt == DType::BF16 ? decode_by_out<64, __nv_bfloat16>(p, out_dt, stream)
+                               : decode_by_out<64, __half>(p, out_dt, stream);
+}
+
+cudaError_t launch_combine(const AttnParams& p, int head_size, DType out_dt, cudaStream_t stream) {
+    return head_size == 128 ? combine_by_out<128>(p, out_dt, stream) : combine_by_out<64>(p, out_dt, stream);
+}
+
+
+}  // namespace kvi4

@@ -1,0 +1,251 @@
+// Device-side building blocks shared by the kernels of the INT4 per-(token, head) KV cache:
+// inline-PTX wrappers (mbarrier, bulk async copy, packed fp32x2 arithmetic, mma.sync, movmatrix)
+// and the nibble -> fp16 unpacking used by both attention kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace kvi4 {
+
+// Row geometry of one cached (token, head) vector.
+template <int D>
+struct Geo {
+    static constexpr int RB = D / 2 + 4;   // bytes: D/2 code bytes + fp32 scale word
+    static constexpr int RW = RB / 4;      // 32-bit words per row
+    static constexpr int KW = D / 8;       // code words per row (8 nibbles each)
+    static constexpr int KSTEPS = D / 16;  // k-steps of a 16-deep mma over the head dimension
+    static constexpr int KWPT = KW / 4;    // code words one thread of a quad reads per row
+    static constexpr int MT = D / 16;      // 16-row tiles covering the head dimension
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void count_status(uint32_t* status, int which) {
+    if (status != nullptr) atomicAdd(status + which, 1u);
+}
+
+// ------------------------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; give up after timeout_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns = kWaitTimeoutNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+// 1-D bulk copy global -> shared, completion signalled on an mbarrier (transaction bytes).
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// -------------------------------------------------------------------- packed fp32 (sm_100+)
+// Each lane of the pair is an independent IEEE round-to-nearest-even operation, so results are
+// bit-identical to two scalar operations.
+
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
+    uint64_t ua, ub, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ua), "l"(ub));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+__device__ __forceinline__ float2 sub_f32x2(float2 a, float2 b) {
+    uint64_t ua, ub, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ua), "l"(ub));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+    uint64_t ua, ub, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ua), "l"(ub));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+    uint64_t ua, ub, uc, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ua), "l"(ub), "l"(uc));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// ------------------------------------------------------------------------ tensor-core helpers
+
+// D = A(16x16, row) * B(16x8, col) + D, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 b16 matrix held in mma fragment layout (row = lane/4, cols 2*(lane%4), +1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ----------------------------------------------------------------------- nibble unpacking
+//
+// A 32-bit word holds 8 codes e0..e7 (e0 in bits 0-3, e1 in bits 4-7, ...).  OR-ing a nibble
+// into the mantissa of fp16 1024.0 (0x6400) gives exactly 1024 + n (the mantissa unit at that
+// exponent is 1); a nibble shifted up by 4 gives 1024 + 16 n.  Subtracting 1024 + zp, or
+// scaling by 1/16 and subtracting 64 + zp, leaves code - zp exactly as fp16.
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// fp16 (1024 + zp) and -(64 + zp) for a zero-point 0..15
+__device__ __forceinline__ uint32_t zp_lo_half(uint32_t zp) { return 0x6400u + zp; }
+__device__ __forceinline__ uint32_t zp_hi_half(uint32_t zp) { return 0xD400u + (zp << 4); }
+
+// Word w (8 codes) with per-half zero points -> 4 fp16x2 values holding code - zp:
+//   o[0] = (e0, e4), o[1] = (e1, e5), o[2] = (e2, e6), o[3] = (e3, e7)   (low half, high half)
+// zlo / zhi: the two halves' zp_lo_half / zp_hi_half packed into a 32-bit pair.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t zlo, uint32_t zhi, uint32_t (&o)[4]) {
+    constexpr uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kExp = 0x64006400u, kSixteenth = 0x2C002C00u;
+    const uint32_t w8 = w >> 8;
+    o[0] = hsub2(lop3_and_or(w, kLo, kExp), zlo);
+    o[1] = hfma2(lop3_and_or(w, kHi, kExp), kSixteenth, zhi);
+    o[2] = hsub2(lop3_and_or(w8, kLo, kExp), zlo);
+    o[3] = hfma2(lop3_and_or(w8, kHi, kExp), kSixteenth, zhi);
+}
+
+// Two rows' words (token a, token b) -> 8 fp16x2 values (a.e_i - zp_a, b.e_i - zp_b), i = 0..7.
+__device__ __forceinline__ void unpack_word_pair(uint32_t wa, uint32_t wb, uint32_t zlo, uint32_t zhi,
+                                                 uint32_t (&o)[8]) {
+    uint32_t lo[4], hi[4];
+    unpack_word(prmt(wa, wb, 0x5410u), zlo, zhi, lo);
+    unpack_word(prmt(wa, wb, 0x7632u), zlo, zhi, hi);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[i] = lo[i];
+        o[4 + i] = hi[i];
+    }
+}
+
+// Token order inside a 16-token block used by the attention kernels: mma row / key index r maps
+// to token tau(r) = ((r & 7) >> 1) + 4 * (r & 1) + 8 * (r >> 3).  It makes the four rows a thread
+// reads for P.V (tokens t, t+4, t+8, t+12 of lane quad t) fall in distinct shared-memory banks.
+__host__ __device__ __forceinline__ constexpr int block_token(int r) {
+    return ((r & 7) >> 1) + 4 * (r & 1) + 8 * (r >> 3);
+}
+
+}  // namespace kvi4

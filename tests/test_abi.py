@@ -1,0 +1,101 @@
+"""The C-ABI library loads without a GPU, exports every entry point include/kv_int4.h declares, and
+rejects invalid arguments on the host (these calls return before any CUDA work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kv_int4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int4_token_head_kv_gb300._build import build_library
+    return ctypes.CDLL(build_library())
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kv_int4_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in kv_int4.h but not exported"
+
+
+def test_host_side_validation(lib):
+    lib.kv_int4_write.restype = ctypes.c_int
+    lib.kv_int4_write.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                          ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]
+    fake = 1 << 20   # never dereferenced: every call below fails validation first
+    # head size 96 is not built
+    assert lib.kv_int4_write(fake, fake, 1, 4, 2, 96, fake, fake, fake, 8, 16, None) == 2
+    # block size must be 16
+    assert lib.kv_int4_write(fake, fake, 1, 4, 2, 128, fake, fake, fake, 8, 32, None) == 2
+    # fp32 inputs are not a cache-write dtype
+    assert lib.kv_int4_write(fake, fake, 2, 4, 2, 128, fake, fake, fake, 8, 16, None) == 2
+    # negative sizes / null pointers
+    assert lib.kv_int4_write(fake, fake, 1, -1, 2, 128, fake, fake, fake, 8, 16, None) == 1
+    assert lib.kv_int4_write(None, fake, 1, 4, 2, 128, fake, fake, fake, 8, 16, None) == 1
+    # misaligned input
+    assert lib.kv_int4_write(fake + 2, fake, 1, 4, 2, 128, fake, fake, fake, 8, 16, None) == 3
+    # nothing to do
+    assert lib.kv_int4_write(None, None, 1, 0, 2, 128, None, None, None, 8, 16, None) == 0
+
+
+def test_attention_validation_and_workspace_policy(lib):
+    f = lib.kv_int4_paged_attention
+    f.restype = ctypes.c_int
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float,
+                  vp, i32, vp, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    fake = 1 << 20
+    base = dict(q=fake, qd=1, nq=2, hq=32, cache=fake, nb=64, h=8, d=128, bs=16, bt=fake, mb=4, sl=fake, qsl=fake,
+                ns=2, mql=1, msl=64, scale=0.088, signs=fake, seg=0, out=fake, od=2, ws=None, wsb=0, st=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(*a.values())
+
+    assert call(h=3, hq=24) == 2           # kv heads must be a power of two <= 8
+    assert call(hq=48) == 2                # q heads per kv head must be a power of two <= 8
+    assert call(d=80) == 2
+    assert call(seg=24) == 2               # segment length must be a multiple of 16
+    assert call(q=None) == 1
+    assert call(out=fake + 4) == 3
+    lib.kv_int4_attention_workspace_bytes.restype = ctypes.c_size_t
+    lib.kv_int4_attention_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.kv_int4_attention_segment_len.restype = i32
+    lib.kv_int4_attention_segment_len.argtypes = [i32, i32, i32]
+    # one segment: no workspace
+    assert lib.kv_int4_attention_workspace_bytes(8, 64, 128, 8, 4096, 4096) == 0
+    # 8 seqs x 32 segments of 4096: partial outputs + (max, sum) pairs
+    units = 8 * 64 * 32
+    assert lib.kv_int4_attention_workspace_bytes(8, 64, 128, 8, 131072, 4096) == units * 128 * 4 + units * 8
+    assert call(msl=131072, seg=4096, mb=8192) == 4   # workspace required but missing
+    assert lib.kv_int4_attention_segment_len(8, 131072, 4096) == 4096
+    assert lib.kv_int4_attention_segment_len(8, 131072, 0) % 256 == 0
+
+
+def test_status_strings(lib):
+    lib.kv_int4_status_string.restype = ctypes.c_char_p
+    for s in range(6):
+        assert lib.kv_int4_status_string(s)
+    assert lib.kv_int4_status_string(99) == b"unknown status"
+
+
+def test_package_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "int4_token_head_kv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), fn
+                assert "kv_int4_oracle" not in src, fn
