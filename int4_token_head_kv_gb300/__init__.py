@@ -3,8 +3,8 @@
 The functions below have the C entry points' names.  They only marshal arguments: check that the
 torch tensors are CUDA, contiguous and of the right dtype and shape, then pass raw device pointers
 and the current CUDA stream to ``libkv_int4.so``.  Every step of the write and of the attention
-runs in that library's kernels; there is no fallback.  Importing this package fails loudly when the
-library has not been built (``python -m int4_token_head_kv_gb300._build``).
+runs in that library's kernels; there is no fallback: the first call (or ``load()``) raises
+ImportError when the library has not been built (``python int4_token_head_kv_gb300/_build.py``).
 """
 from __future__ import annotations
 
@@ -56,12 +56,20 @@ def _load():
     return lib
 
 
-_lib = _load()
+_lib = None
+
+
+def load():
+    """Load libkv_int4.so (once); raises ImportError when it has not been built."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
 
 
 def _check(fn: str, status: int):
     if status != 0:
-        raise KVInt4Error(fn, status, _lib.kv_int4_status_string(status).decode())
+        raise KVInt4Error(fn, status, load().kv_int4_status_string(status).decode())
 
 
 def _stream(stream) -> int:
@@ -81,7 +89,7 @@ def _cuda(t: torch.Tensor, name: str, dtypes=None) -> torch.Tensor:
 
 
 def kv_int4_row_bytes(head_size: int) -> int:
-    return int(_lib.kv_int4_row_bytes(head_size))
+    return int(load().kv_int4_row_bytes(head_size))
 
 
 def kv_int4_cache_shape(num_blocks: int, block_size: int, num_kv_heads: int, head_size: int):
@@ -105,19 +113,19 @@ def kv_int4_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Te
     if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.shape[3] != H or \
             kv_cache.shape[4] != kv_int4_row_bytes(d):
         raise ValueError(f"kv_cache must be {kv_int4_cache_shape('NB', 'bs', H, d)}")
-    st = _lib.kv_int4_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
+    st = load().kv_int4_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
                             rht_signs.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2],
                             _stream(stream))
     _check("kv_int4_write", st)
 
 
 def kv_int4_attention_segment_len(num_seqs: int, max_seq_len: int, segment_len: int = 0) -> int:
-    return int(_lib.kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len))
+    return int(load().kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len))
 
 
 def kv_int4_attention_workspace_bytes(num_q_tokens: int, num_q_heads: int, head_size: int, num_seqs: int,
                                       max_seq_len: int, segment_len: int = 0) -> int:
-    return int(_lib.kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
+    return int(load().kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
                                                       max_seq_len, segment_len))
 
 
@@ -149,7 +157,7 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = _lib.kv_int4_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H,
+    st = load().kv_int4_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H,
                                       d, bs, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
                                       query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
                                       float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(),
@@ -161,9 +169,9 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
 def kv_int4_read_device_status(stream=None) -> dict:
     """Synchronise the stream and return the device's status counters by name."""
     buf = (ctypes.c_uint32 * _STAT_COUNT)()
-    _check("kv_int4_read_device_status", _lib.kv_int4_read_device_status(buf, _stream(stream)))
+    _check("kv_int4_read_device_status", load().kv_int4_read_device_status(buf, _stream(stream)))
     return {name: int(buf[i]) for i, name in enumerate(STAT_NAMES)}
 
 
 def kv_int4_clear_device_status(stream=None) -> None:
-    _check("kv_int4_clear_device_status", _lib.kv_int4_clear_device_status(_stream(stream)))
+    _check("kv_int4_clear_device_status", load().kv_int4_clear_device_status(_stream(stream)))

@@ -83,10 +83,13 @@ __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t
 //   v = H_d (D q) (unnormalised), e = prescale exponent, qh = fp16(v * 2^e),
 //   alpha = c * 2^-e * softmax_scale * log2(e)  (raw score -> log2-domain logit, before the
 //   key's scale s' is applied).
-// The warp writes qh (D halves) to shared memory and returns alpha (all lanes).
+// The warp writes qh and ql (D halves each) to shared memory and returns alpha (all lanes).
+// The scaled vector is kept as two fp16 halves, qh = fp16(v 2^e) and ql = fp16(v 2^e - qh) (the
+// difference is exact in fp32), so that qh + ql carries about 22 significant bits: a plain fp16
+// copy (11 bits) turns large keys into logit errors that a heavy-tailed cache makes visible.
 template <int D, typename QT>
-__device__ __forceinline__ float rotate_query(const void* q, int64_t qoff, const float* sgn, __half* qh, float c,
-                                              float softmax_scale) {
+__device__ __forceinline__ float rotate_query(const void* q, int64_t qoff, const float* sgn, __half* qh, __half* ql,
+                                              float c, float softmax_scale) {
     const int lane = threadIdx.x & 31;
     float x[D / 32];
 #pragma unroll
@@ -98,8 +101,21 @@ __device__ __forceinline__ float rotate_query(const void* q, int64_t qoff, const
     const int e = prescale_exponent(warp_max(m));
     const float sc = exp2i(e);
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) qh[lane + 32 * k] = __float2half_rn(x[k] * sc);
+    for (int k = 0; k < D / 32; ++k) {
+        const float y = x[k] * sc;
+        const __half hi = __float2half_rn(y);
+        qh[lane + 32 * k] = hi;
+        ql[lane + 32 * k] = __float2half_rn(y - __half2float(hi));
+    }
     return c * exp2i(-e) * softmax_scale * kLog2e;
+}
+
+// fp32 pair -> (hi, lo) fp16x2 pairs with hi + lo ~ the pair to about 22 bits.
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_f16x2(a, b);
+    const __half2 h = *reinterpret_cast<const __half2*>(&hi);
+    const float2 hf = __half22float2(h);
+    lo = pack_f16x2(a - hf.x, b - hf.y);
 }
 
 // Un-rotate an accumulated output vector held by a warp (lane l: x[k] = o[l + 32 k]) and store it:

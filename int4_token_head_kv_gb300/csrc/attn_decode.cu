@@ -47,13 +47,13 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
                           + D * 4u                 // signs
                           + (uint32_t)Hq * 4u      // alpha
                           + 2u * kConsumerWarps * 8u * 4u  // per-warp (m, l)
-                          + (uint32_t)Hq * D * 2u;  // rotated fp16 queries
+                          + 2u * (uint32_t)Hq * D * 2u;  // rotated queries, fp16 hi and lo halves
     s.total = s.state_off + ((tail + 127u) & ~127u);
     return s;
 }
 
-template <int D, typename QT, typename OT>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ AttnParams p) {
+template <int D, bool WIDE, typename QT, typename OT>
+__global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParams p) {
     using Gm = Geo<D>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int seg = blockIdx.x, seq = blockIdx.y;
@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     float* st_m = alpha + Hq;
     float* st_l = st_m + kConsumerWarps * 8;
     __half* qh = reinterpret_cast<__half*>(st_l + kConsumerWarps * 8);
+    __half* ql = qh + Hq * D;
     float* st_o = reinterpret_cast<float*>(smem);   // epilogue overlay of the ring
 
     if (threadIdx.x == 0) {
@@ -136,7 +137,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     // Rotate this sequence's query (all Hq heads) into fp16 + per-head logit multiplier.
     if (warp < kConsumerWarps) {
         for (int v = warp; v < Hq; v += kConsumerWarps) {
-            const float a = rotate_query<D, QT>(p.q, ((int64_t)q0 * Hq + v) * D, sgn, qh + v * D, p.c, p.softmax_scale);
+            const float a = rotate_query<D, QT>(p.q, ((int64_t)q0 * Hq + v) * D, sgn, qh + v * D, ql + v * D, p.c,
+                                                p.softmax_scale);
             if (lane == 0) alpha[v] = a;
         }
     }
@@ -173,27 +175,40 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         const int sub = warp / H;
         const int tk0 = block_token(g), tk1 = block_token(g + 8);
 
-        // B fragments of Q' for the 16-deep k-steps (see the k-slot mapping in the header comment)
-        uint32_t qb[Gm::KSTEPS][2];
+        // Score columns (the mma N dimension, 8 wide).  WIDE (8 query heads per kv head): column n
+        // is head n, with a second 8-wide tile carrying the low halves.  Otherwise columns 0-3
+        // carry the high halves of heads 0-3 and columns 4-7 their low halves, so the split costs
+        // no extra mma: lane quad t then holds heads hb, hb+1 with hb = 2 (t & 1).
+        const int hb = WIDE ? 2 * t : 2 * (t & 1);
+        uint32_t qb[Gm::KSTEPS][WIDE ? 4 : 2];
         {
-            const bool live = g < G;
-            const __half* qv = qh + (h * G + (live ? g : 0)) * D;
+            const int head = WIDE ? g : (g & 3);
+            const bool live = head < G;
+            const __half* qv = (WIDE || g < 4 ? qh : ql) + (h * G + (live ? head : 0)) * D;
+            const __half* qv2 = ql + (h * G + (live ? head : 0)) * D;
+            const __half z = __float2half(0.0f);
 #pragma unroll
             for (int j = 0; j < Gm::KWPT; ++j) {
                 const int W = t + 4 * j;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int d0 = 8 * W + 2 * hh;
-                    const __half z = __float2half(0.0f);
                     __half2 b0 = live ? __halves2half2(qv[d0], qv[d0 + 4]) : __halves2half2(z, z);
                     __half2 b1 = live ? __halves2half2(qv[d0 + 1], qv[d0 + 5]) : __halves2half2(z, z);
                     qb[2 * j + hh][0] = *reinterpret_cast<uint32_t*>(&b0);
                     qb[2 * j + hh][1] = *reinterpret_cast<uint32_t*>(&b1);
+                    if constexpr (WIDE) {
+                        __half2 c0 = live ? __halves2half2(qv2[d0], qv2[d0 + 4]) : __halves2half2(z, z);
+                        __half2 c1 = live ? __halves2half2(qv2[d0 + 1], qv2[d0 + 5]) : __halves2half2(z, z);
+                        qb[2 * j + hh][2] = *reinterpret_cast<uint32_t*>(&c0);
+                        qb[2 * j + hh][3] = *reinterpret_cast<uint32_t*>(&c1);
+                    }
                 }
             }
         }
-        const float al0 = (2 * t < G) ? alpha[h * G + 2 * t] : 0.0f;
-        const float al1 = (2 * t + 1 < G) ? alpha[h * G + 2 * t + 1] : 0.0f;
+        const float al0 = (hb < G) ? alpha[h * G + hb] : 0.0f;
+        const float al1 = (hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
+        const bool lo_lane = !WIDE && t >= 2;   // this lane's P columns carry low halves
 
         for (int i = 0; i < nblk; ++i) {
             const int st = i % kStages;
@@ -211,8 +226,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp + (tk0 * H + h) * Gm::RB);
                 const uint32_t* kr1 = reinterpret_cast<const uint32_t*>(kp + (tk1 * H + h) * Gm::RB);
                 const uint32_t ks0 = kr0[Gm::KW], ks1 = kr1[Gm::KW];
-                // ---- S^T = (K - zp) Q'^T
+                // ---- S^T = (K - zp) Q'^T, high and low halves of Q'
                 float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float cl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 {
                     const uint32_t z0l = zp_lo_half(ks0 & 15u), z0h = zp_hi_half(ks0 & 15u);
                     const uint32_t z1l = zp_lo_half(ks1 & 15u), z1h = zp_hi_half(ks1 & 15u);
@@ -225,9 +241,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         unpack_word(kr1[t + 4 * j], zl1, zh1, a1);
                         mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * j][0], qb[2 * j][1]);
                         mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][0], qb[2 * j + 1][1]);
+                        if constexpr (WIDE) {
+                            mma_f16_16816(cl, a0[0], a1[0], a0[1], a1[1], qb[2 * j][2], qb[2 * j][3]);
+                            mma_f16_16816(cl, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][2], qb[2 * j + 1][3]);
+                        }
                     }
                 }
-                // ---- logits (log2 units), masking, online softmax for heads 2t, 2t+1
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if constexpr (WIDE) c[e] += cl[e];
+                    else c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);   // high + low columns
+                }
+                // ---- logits (log2 units), masking, online softmax for heads hb, hb+1
                 const bool v0 = tokbase + tk0 < tok_end, v1 = tokbase + tk1 < tok_end;
                 const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
                 const float x0 = v0 ? c[0] * sk0 * al0 : -INFINITY;
@@ -272,9 +297,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 }
                 const float wsc = __uint_as_float((254u - eref) << 23);   // 2^(127 - eref)
                 const float sv0 = __uint_as_float(vs0 & 0xFFFFFFF0u) * wsc, sv1 = __uint_as_float(vs1 & 0xFFFFFFF0u) * wsc;
-                const uint32_t xlo = pack_f16x2(v0 ? p0 * sv0 : 0.0f, v0 ? p1 * sv0 : 0.0f);
-                const uint32_t xhi = pack_f16x2(v1 ? p2 * sv1 : 0.0f, v1 ? p3 * sv1 : 0.0f);
-                const uint32_t b0 = movmatrix_trans(xlo), b1 = movmatrix_trans(xhi);
+                // weights w = p * s'_V * 2^-E as fp16 high + low halves
+                uint32_t xlo_h, xlo_l, xhi_h, xhi_l;
+                split_f16x2(v0 ? p0 * sv0 : 0.0f, v0 ? p1 * sv0 : 0.0f, xlo_h, xlo_l);
+                split_f16x2(v1 ? p2 * sv1 : 0.0f, v1 ? p3 * sv1 : 0.0f, xhi_h, xhi_l);
+                uint32_t b0, b1, b0l = 0, b1l = 0;
+                if constexpr (WIDE) {
+                    b0 = movmatrix_trans(xlo_h);
+                    b1 = movmatrix_trans(xhi_h);
+                    b0l = movmatrix_trans(xlo_l);
+                    b1l = movmatrix_trans(xhi_l);
+                } else {
+                    b0 = movmatrix_trans(lo_lane ? xlo_l : xlo_h);
+                    b1 = movmatrix_trans(lo_lane ? xhi_l : xhi_h);
+                }
                 // ---- O^T += (V - zp)^T P^T
                 const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp + ((t)*H + h) * Gm::RB);
                 const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp + ((t + 4) * H + h) * Gm::RB);
@@ -292,13 +328,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);           // tokens t+8, t+12
                     unpack_word_pair(vr2[g + 8], vr3[g + 8], zl23, zh23, ud);
 #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0, b1);
+                    for (int mt = 0; mt < 8; ++mt) {
+                        mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0, b1);
+                        if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0l, b1l);
+                    }
                 } else {
                     uint32_t ua[8], uc[8];
                     unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);   // d = 8g + i
                     unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);
 #pragma unroll
-                    for (int mt = 0; mt < 4; ++mt) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0, b1);
+                    for (int mt = 0; mt < 4; ++mt) {
+                        mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0, b1);
+                        if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0l, b1l);
+                    }
                 }
             }
             __syncwarp();
@@ -313,22 +355,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
+        if constexpr (!WIDE) {
+#pragma unroll
+            for (int mt = 0; mt < Gm::MT; ++mt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
+            }
+        }
+        const int hb = WIDE ? 2 * t : 2 * (t & 1);
         const float es = eref ? __uint_as_float(eref << 23) : 0.0f;   // 2^(eref - 127)
         float* so = st_o + warp * 8 * D;
+        if (WIDE || t < 2) {
 #pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) {
-            const int dlo = 8 * g + mt;
-            const int dhi = (D == 128) ? 64 + 8 * g + mt : 8 * g + 4 + mt;
-            so[(2 * t) * D + dlo] = o[mt][0] * es;
-            so[(2 * t + 1) * D + dlo] = o[mt][1] * es;
-            so[(2 * t) * D + dhi] = o[mt][2] * es;
-            so[(2 * t + 1) * D + dhi] = o[mt][3] * es;
-        }
-        if (g == 0) {
-            st_m[warp * 8 + 2 * t] = m0;
-            st_m[warp * 8 + 2 * t + 1] = m1;
-            st_l[warp * 8 + 2 * t] = l0;
-            st_l[warp * 8 + 2 * t + 1] = l1;
+            for (int mt = 0; mt < Gm::MT; ++mt) {
+                const int dlo = 8 * g + mt;
+                const int dhi = (D == 128) ? 64 + 8 * g + mt : 8 * g + 4 + mt;
+                so[hb * D + dlo] = o[mt][0] * es;
+                so[(hb + 1) * D + dlo] = o[mt][1] * es;
+                so[hb * D + dhi] = o[mt][2] * es;
+                so[(hb + 1) * D + dhi] = o[mt][3] * es;
+            }
+            if (g == 0) {
+                st_m[warp * 8 + hb] = m0;
+                st_m[warp * 8 + hb + 1] = m1;
+                st_l[warp * 8 + hb] = l0;
+                st_l[warp * 8 + hb + 1] = l1;
+            }
         }
     }
     __syncthreads();
@@ -399,8 +451,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
 template <int D, typename QT, typename OT>
 cudaError_t launch_decode_t(const AttnParams& p, cudaStream_t stream) {
     const DecodeSmem lay = decode_smem_layout<D>(p.H, p.Hq);
-    auto kern = decode_kernel<D, QT, OT>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total);
+    const bool wide = p.G == 8;
+    auto kern = wide ? decode_kernel<D, true, QT, OT> : decode_kernel<D, false, QT, OT>;
+    cudaError_t err = wide ? opt_in_smem<decode_kernel<D, true, QT, OT>>(lay.total)
+                           : opt_in_smem<decode_kernel<D, false, QT, OT>>(lay.total);
     if (err != cudaSuccess) return err;
     dim3 grid(p.nseg_max, p.num_seqs);
     kern<<<grid, kDecodeThreads, lay.total, stream>>>(p);

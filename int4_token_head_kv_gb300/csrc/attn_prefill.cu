@@ -7,9 +7,11 @@
 // of that kv head, 16 rows per warp.  Each warp walks the key blocks its rows can see (causal),
 // builds fp16 fragments of K - zp and V - zp directly from the packed bytes (read through L1, the
 // next block prefetched into registers), and runs
-//   S = Q' (K - zp)^T      mma.sync m16n8k16, Q' = rotated, power-of-two-prescaled fp16 queries
+//   S = Q' (K - zp)^T      mma.sync m16n8k16, Q' = rotated, power-of-two-prescaled queries as
+//                          fp16 high + low halves (two mma per step)
 //   online softmax with the per-key scale s'_K and the causal mask
-//   O += P_w (V - zp)      P_w = p * s'_V * 2^-E (fp16), straight from S's accumulator registers
+//   O += P_w (V - zp)      P_w = p * s'_V * 2^-E as fp16 high + low halves, straight from S's
+//                          accumulator registers
 // and un-rotates its rows at the end.  The fragment layouts are the decode kernel's with the
 // operand roles swapped (queries on the M side, keys on N).
 #include "attn_common.cuh"
@@ -86,7 +88,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 
     float* ostage = reinterpret_cast<float*>(smem);                         // [128][D] fp32 (epilogue)
     __half* qh = reinterpret_cast<__half*>(smem);                           // [128][D] fp16 (prologue)
-    float* alpha = reinterpret_cast<float*>(smem + (size_t)kRows * D * 4);  // [128]
+    __half* ql = qh + kRows * D;                                            // [128][D] fp16 (prologue)
+    uint4* qlf = reinterpret_cast<uint4*>(smem + (size_t)kRows * D * 4);    // [warps][KSTEPS][32] low-half A fragments
+    float* alpha = reinterpret_cast<float*>(qlf + kPrefillWarps * Gm::KSTEPS * 32);   // [128]
     float* sgn = alpha + kRows;                                             // [D]
     for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
     __syncthreads();
@@ -96,11 +100,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         const int R = warp * 16 + r;
         const int qt = qt0 + R / G, gg = R % G;
         if (qt < qlen) {
-            const float a = rotate_query<D, QT>(p.q, ((int64_t)(q0 + qt) * Hq + h * G + gg) * D, sgn, qh + R * D, p.c,
-                                                p.softmax_scale);
+            const float a = rotate_query<D, QT>(p.q, ((int64_t)(q0 + qt) * Hq + h * G + gg) * D, sgn, qh + R * D,
+                                                ql + R * D, p.c, p.softmax_scale);
             if (lane == 0) alpha[R] = a;
         } else {
-            for (int k = lane; k < D; k += 32) qh[R * D + k] = __float2half(0.0f);
+            for (int k = lane; k < D; k += 32) qh[R * D + k] = ql[R * D + k] = __float2half(0.0f);
             if (lane == 0) alpha[R] = 0.0f;
         }
     }
@@ -122,8 +126,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
             qa[2 * j + hh][1] = *reinterpret_cast<uint32_t*>(&a1);
             qa[2 * j + hh][2] = *reinterpret_cast<uint32_t*>(&a2);
             qa[2 * j + hh][3] = *reinterpret_cast<uint32_t*>(&a3);
+            // the low halves go to a fragment-ordered area read once per k-step in the main loop
+            __half2 l0 = __halves2half2(ql[Rg * D + d0], ql[Rg * D + d0 + 4]);
+            __half2 l1 = __halves2half2(ql[Rg8 * D + d0], ql[Rg8 * D + d0 + 4]);
+            __half2 l2 = __halves2half2(ql[Rg * D + d0 + 1], ql[Rg * D + d0 + 5]);
+            __half2 l3 = __halves2half2(ql[Rg8 * D + d0 + 1], ql[Rg8 * D + d0 + 5]);
+            qlf[(warp * Gm::KSTEPS + 2 * j + hh) * 32 + lane] =
+                make_uint4(*reinterpret_cast<uint32_t*>(&l0), *reinterpret_cast<uint32_t*>(&l1),
+                           *reinterpret_cast<uint32_t*>(&l2), *reinterpret_cast<uint32_t*>(&l3));
         }
     }
+    const uint4* my_qlf = qlf + warp * Gm::KSTEPS * 32 + lane;
     const float al_g = alpha[Rg], al_g8 = alpha[Rg8];
     const int qt_g = qt0 + Rg / G, qt_g8 = qt0 + Rg8 / G;
     const int lim_g = qt_g < qlen ? pos0 + qt_g : -1;     // last visible key of each row
@@ -168,8 +181,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint32_t* a = qa[2 * j + hh];
+                        const uint4 al = my_qlf[(2 * j + hh) * 32];
                         mma_f16_16816(s[0], a[0], a[1], a[2], a[3], b0[2 * hh], b0[2 * hh + 1]);
                         mma_f16_16816(s[1], a[0], a[1], a[2], a[3], b1[2 * hh], b1[2 * hh + 1]);
+                        mma_f16_16816(s[0], al.x, al.y, al.z, al.w, b0[2 * hh], b0[2 * hh + 1]);
+                        mma_f16_16816(s[1], al.x, al.y, al.z, al.w, b1[2 * hh], b1[2 * hh + 1]);
                     }
                 }
             }
@@ -241,10 +257,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
             for (int c = 0; c < 4; ++c)
                 sv[c] = (kbase + t + 4 * c <= max(lim_g, lim_g8)) ? __uint_as_float(cur.vs[c] & 0xFFFFFFF0u) * wsc : 0.0f;
             // P_w as the A operand (C layout of two 8-key tiles == A layout of one 16-key tile)
-            const uint32_t pa0 = pack_f16x2(pr[0][0] * sv[0], pr[0][1] * sv[1]);
-            const uint32_t pa1 = pack_f16x2(pr[0][2] * sv[0], pr[0][3] * sv[1]);
-            const uint32_t pa2 = pack_f16x2(pr[1][0] * sv[2], pr[1][1] * sv[3]);
-            const uint32_t pa3 = pack_f16x2(pr[1][2] * sv[2], pr[1][3] * sv[3]);
+            // (high and low fp16 halves, as for the queries)
+            uint32_t pa0, pa1, pa2, pa3, pl0, pl1, pl2, pl3;
+            split_f16x2(pr[0][0] * sv[0], pr[0][1] * sv[1], pa0, pl0);
+            split_f16x2(pr[0][2] * sv[0], pr[0][3] * sv[1], pa1, pl1);
+            split_f16x2(pr[1][0] * sv[2], pr[1][1] * sv[3], pa2, pl2);
+            split_f16x2(pr[1][2] * sv[2], pr[1][3] * sv[3], pa3, pl3);
             // ---- O += P_w (V - zp)
             const uint32_t zl01 = zp_lo_half(cur.vs[0] & 15u) | (zp_lo_half(cur.vs[1] & 15u) << 16);
             const uint32_t zh01 = zp_hi_half(cur.vs[0] & 15u) | (zp_hi_half(cur.vs[1] & 15u) << 16);
@@ -260,6 +278,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
                 for (int i = 0; i < 8; ++i) {
                     mma_f16_16816(o[i], pa0, pa1, pa2, pa3, ua[i], uc[i]);
                     mma_f16_16816(o[8 + i], pa0, pa1, pa2, pa3, ub[i], ud[i]);
+                    mma_f16_16816(o[i], pl0, pl1, pl2, pl3, ua[i], uc[i]);
+                    mma_f16_16816(o[8 + i], pl0, pl1, pl2, pl3, ub[i], ud[i]);
                 }
             } else {
                 uint32_t ua[8], uc[8];
@@ -269,6 +289,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
                 for (int i = 0; i < 4; ++i) {
                     mma_f16_16816(o[i], pa0, pa1, pa2, pa3, ua[i], uc[i]);
                     mma_f16_16816(o[4 + i], pa0, pa1, pa2, pa3, ua[4 + i], uc[4 + i]);
+                    mma_f16_16816(o[i], pl0, pl1, pl2, pl3, ua[i], uc[i]);
+                    mma_f16_16816(o[4 + i], pl0, pl1, pl2, pl3, ua[4 + i], uc[4 + i]);
                 }
             }
         }
@@ -308,9 +330,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 
 template <int D, typename QT, typename OT>
 cudaError_t launch_prefill_t(const AttnParams& p, int max_query_len, cudaStream_t stream) {
-    const size_t smem = (size_t)kRows * D * 4 + kRows * 4 + D * 4;
+    const size_t smem = (size_t)kRows * D * 4 + (size_t)kPrefillWarps * Geo<D>::KSTEPS * 32 * 16 + kRows * 4 + D * 4;
     auto kern = prefill_kernel<D, QT, OT>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = opt_in_smem<prefill_kernel<D, QT, OT>>(smem);
     if (err != cudaSuccess) return err;
     const int BQ = kRows / p.G;
     dim3 grid((max_query_len + BQ - 1) / BQ, p.H, p.num_seqs);

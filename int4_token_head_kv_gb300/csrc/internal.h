@@ -61,4 +61,18 @@ cudaError_t launch_prefill(const AttnParams& p, int head_size, int max_query_len
 
 int num_sms();
 
+// Opt a kernel in to `bytes` of dynamic shared memory, once per device (so that launches issued
+// under stream capture contain nothing but the launch itself).
+template <auto Kern>
+cudaError_t opt_in_smem(size_t bytes) {
+    static size_t done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (done[dev] >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done[dev] = bytes;
+    return e;
+}
+
 }  // namespace kvi4
