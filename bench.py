@@ -104,6 +104,22 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the slowest rank's time); identity on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank processes its own replica of the workload each step."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -215,12 +231,8 @@ def _gpu_arm(args):
     e1.record(stream)
     barrier()
     clocks = sampler.stop()
-    ms_step = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    value = attn_bytes * world / (ms_step * 1e-3) / 1e9
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    value = whole_job_gbs(attn_bytes, world, ms_step)
     # ---- the attention call alone, back to back (roofline of the dominant kernel call)
     barrier()
     e0.record(stream)

@@ -165,6 +165,13 @@ kv_int4_status kv_int4_read_device_status(uint32_t* counts, kv_int4_stream_t str
 /* Zero the current device's status counters (asynchronous on the stream). */
 kv_int4_status kv_int4_clear_device_status(kv_int4_stream_t stream);
 
+/*
+ * Diagnostic of the bounded-wait machinery: launches one CTA that waits on a shared-memory barrier
+ * nothing will ever complete and gives up after timeout_ns (clamped to 1 s), recording the give-up
+ * as KV_INT4_STAT_WAIT_TIMEOUT exactly as the pipelined kernels do.  The device stays usable.
+ */
+kv_int4_status kv_int4_selftest_wait_timeout(uint64_t timeout_ns, kv_int4_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char* kv_int4_status_string(kv_int4_status status);
 

@@ -53,6 +53,8 @@ def _load():
     lib.kv_int4_read_device_status.restype = ctypes.c_int
     lib.kv_int4_clear_device_status.argtypes = [vp]
     lib.kv_int4_clear_device_status.restype = ctypes.c_int
+    lib.kv_int4_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.kv_int4_selftest_wait_timeout.restype = ctypes.c_int
     return lib
 
 
@@ -175,3 +177,8 @@ def kv_int4_read_device_status(stream=None) -> dict:
 
 def kv_int4_clear_device_status(stream=None) -> None:
     _check("kv_int4_clear_device_status", load().kv_int4_clear_device_status(_stream(stream)))
+
+
+def kv_int4_selftest_wait_timeout(timeout_ns: int = 5_000_000, stream=None) -> None:
+    """Run the bounded-wait diagnostic (a wait nothing completes); it records one wait_timeout."""
+    _check("kv_int4_selftest_wait_timeout", load().kv_int4_selftest_wait_timeout(int(timeout_ns), _stream(stream)))

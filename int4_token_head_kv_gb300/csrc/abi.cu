@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "../../include/kv_int4.h"
+#include "device.cuh"
 #include "internal.h"
 
 namespace kvi4 {
@@ -60,6 +61,20 @@ int num_sms() {
     }
     return g_sms[dev];
 }
+
+namespace {
+
+// One thread waits on an mbarrier that expects an arrival nobody makes.
+__global__ void wait_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0, timeout_ns)) count_status(status, KV_INT4_STAT_WAIT_TIMEOUT);
+    }
+}
+
+}  // namespace
 
 }  // namespace kvi4
 
@@ -202,6 +217,14 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     if (e == cudaSuccess && nseg > 1) e = launch_combine(p, head_size, od, s);
     if (e == cudaSuccess && max_query_len > 1) e = launch_prefill(p, head_size, max_query_len, qd, od, s);
     return from_cuda(e);
+}
+
+kv_int4_status kv_int4_selftest_wait_timeout(uint64_t timeout_ns, kv_int4_stream_t stream) {
+    uint32_t* ptr = status_ptr();
+    if (!ptr) return KV_INT4_ECUDA;
+    if (timeout_ns > 1000000000ull) timeout_ns = 1000000000ull;
+    wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ptr, timeout_ns);
+    return from_cuda(cudaGetLastError());
 }
 
 kv_int4_status kv_int4_read_device_status(uint32_t* counts, kv_int4_stream_t stream) {
