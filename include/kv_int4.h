@@ -157,6 +157,41 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
                                        size_t workspace_bytes, kv_int4_stream_t stream);
 
 /*
+ * kv_int4_paged_attention_noalloc -- the same attention for callers that cannot allocate device
+ * memory.  (The pages have no counterpart: this entry point is an addition of this library.)
+ *
+ * Some callers cannot provide the workspace kv_int4_paged_attention asks for: a serving engine
+ * that hands all free device memory to its KV cache at start-up and keeps no allocator on the
+ * decode path, a plugin host that forbids device allocation after initialisation, or a decode loop
+ * that cannot afford cudaMalloc's implicit device-wide synchronisation.  This variant takes the
+ * same arguments minus the workspace and keeps the split-KV partials in a fixed scratch array of
+ * KV_INT4_NOALLOC_SCRATCH_BYTES bytes that lives in the library's own device memory (allocated
+ * when the library is loaded, held by every GPU that loads it until the process exits).  It calls
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Returns KV_INT4_EWORKSPACE, launching nothing, when kv_int4_attention_workspace_bytes() for
+ * these sizes exceeds KV_INT4_NOALLOC_SCRATCH_BYTES (use a larger segment_len, or the regular
+ * entry point).  The first call on a device looks up the scratch array's device address (a
+ * runtime call that does not touch any stream); make that first call before any stream capture.
+ * Every call shares the one array and it keeps the last call's contents; nothing in it needs to
+ * start at zero, because each call writes every partial it later reads.  Calls that overlap on the
+ * GPU (different streams, or different host threads on one device) race on the array: serialise
+ * them.
+ */
+#define KV_INT4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+kv_int4_status kv_int4_paged_attention_noalloc(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                               int32_t num_q_heads, const uint8_t* cache,
+                                               int64_t num_blocks, int32_t num_kv_heads,
+                                               int32_t head_size, int32_t block_size,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* seq_lens, const int32_t* query_start_loc,
+                                               int32_t num_seqs, int32_t max_query_len,
+                                               int32_t max_seq_len, float softmax_scale,
+                                               const float* rht_signs, int32_t segment_len, void* out,
+                                               kv_int4_dtype out_dtype, kv_int4_stream_t stream);
+
+/*
  * Copy the current device's status counters (KV_INT4_STAT_COUNT uint32 values) to the HOST array
  * counts.  Synchronises the stream first.  The counters keep counting until cleared.
  */

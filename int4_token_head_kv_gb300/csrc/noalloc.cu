@@ -1,0 +1,55 @@
+// kv_int4_paged_attention_noalloc: the paged attention with its split-KV scratch in a fixed
+// module-scope device array instead of a caller-provided workspace, for callers that cannot
+// allocate device memory.  The array is device memory of the library itself; in host code its
+// name only denotes a host-side stand-in, so the host looks up its device address once per device
+// and passes that address on, like any caller's workspace.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/kv_int4.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KV_INT4_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device with that
+// device current; nullptr when the lookup fails.
+void* scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_scratch[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_scratch[dev] = ptr;
+    }
+    return g_scratch[dev];
+}
+
+}  // namespace
+
+extern "C" kv_int4_status kv_int4_paged_attention_noalloc(
+    const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens, int32_t num_q_heads, const uint8_t* cache,
+    int64_t num_blocks, int32_t num_kv_heads, int32_t head_size, int32_t block_size, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+    int32_t max_query_len, int32_t max_seq_len, float softmax_scale, const float* rht_signs, int32_t segment_len,
+    void* out, kv_int4_dtype out_dtype, kv_int4_stream_t stream) {
+    const size_t need = kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
+                                                          max_seq_len, segment_len);
+    if (need > KV_INT4_NOALLOC_SCRATCH_BYTES) return KV_INT4_EWORKSPACE;
+    void* scratch = nullptr;
+    if (need > 0) {
+        scratch = scratch_address();
+        if (scratch == nullptr) return KV_INT4_ECUDA;
+    }
+    return kv_int4_paged_attention(q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads,
+                                   head_size, block_size, block_tables, max_blocks_per_seq, seq_lens,
+                                   query_start_loc, num_seqs, max_query_len, max_seq_len, softmax_scale, rht_signs,
+                                   segment_len, out, out_dtype, scratch,
+                                   need > 0 ? (size_t)KV_INT4_NOALLOC_SCRATCH_BYTES : 0, stream);
+}
