@@ -301,6 +301,8 @@ def _gpu_arm(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if args.extra:
+        result["extra"] = _extra(torch, kv, workloads, dev, args)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = _cpu_baseline("decode", args)
     if world > 1:
@@ -341,6 +343,75 @@ def _write_bench(torch, kv, workloads, dev, stream, args):
 
 
 # ------------------------------------------------------------------------------- CPU oracle
+
+def _attention_only(torch, kv, wl, dev, reps, rows=None):
+    """Write every token of ``wl`` (untimed), then time ``reps`` back-to-back attention calls
+    (captured in one CUDA graph) over the whole batch.  Returns ms per call."""
+    H, d = wl.num_kv_heads, wl.head_size
+    signs = torch.from_numpy(wl.signs).to(dev)
+    cache = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+    step = 1 << 18
+    for r0 in range(0, wl.key.shape[0], step):
+        r1 = min(wl.key.shape[0], r0 + step)
+        kv.kv_int4_write(wl.key[r0:r1].to(dev), wl.value[r0:r1].to(dev),
+                         torch.from_numpy(wl.slot_mapping[r0:r1]).to(dev), signs, cache)
+    q = wl.query.to(dev)
+    tables, lens = torch.from_numpy(wl.block_tables).to(dev), torch.from_numpy(wl.seq_lens).to(dev)
+    qsl = torch.from_numpy(wl.query_start_loc).to(dev)
+    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, wl.segment_len)
+    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(q.shape[0], wl.num_q_heads, d, len(wl.seq_lens),
+                                                                 wl.max_seq_len, seg)), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+
+    def call():
+        kv.kv_int4_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, signs,
+                                   max_query_len=wl.max_query_len, max_seq_len=wl.max_seq_len, out=out,
+                                   segment_len=seg, workspace=ws)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    del cache
+    return e0.elapsed_time(e1) / reps, seg
+
+
+def _extra(torch, kv, workloads, dev, args):
+    """The long-context and mixed workloads, attention call only (their caches exceed L2)."""
+    peak, _ = _peaks()
+    res = {}
+    wl = workloads.long_context_decode(seed=args.seed)
+    ms, seg = _attention_only(torch, kv, wl, dev, reps=20)
+    rb = kv.kv_int4_row_bytes(wl.head_size)
+    kvb = int(wl.seq_lens.sum()) * 2 * wl.num_kv_heads * rb + 2 * wl.query.numel() * 2
+    res["long_context_decode"] = {"ms": round(ms, 4), "GB/s": round(kvb / ms / 1e6, 1),
+                                  "frac": round(kvb / ms / 1e6 / peak, 4), "bytes": kvb, "segment_len": seg}
+    del wl
+    wl = workloads.mixed_prefill_decode(seed=args.seed)
+    ms, seg = _attention_only(torch, kv, wl, dev, reps=10)
+    kvb = int(wl.seq_lens.sum()) * 2 * wl.num_kv_heads * rb + 2 * wl.query.numel() * 2
+    # dense-equivalent attention FLOPs of the prefill chunks: 4 d per visible (query, key) pair per q head
+    pairs = sum(int(q) * (int(L) - int(q)) + int(q) * (int(q) + 1) // 2
+                for L, q in zip(wl.seq_lens, wl.query_lens) if q > 1)
+    flops = 4 * wl.head_size * pairs * wl.num_q_heads
+    res["mixed_prefill_decode"] = {"ms": round(ms, 4), "GB/s_packed_kv": round(kvb / ms / 1e6, 1),
+                                   "prefill_TFLOP": round(flops / 1e12, 4), "bytes": kvb, "segment_len": seg}
+    pre = workloads.make_attention_workload("prefill_only", wl.seq_lens[:4], wl.query_lens[:4], 32, 8, 128,
+                                            seed=args.seed)
+    ms_p, _ = _attention_only(torch, kv, pre, dev, reps=10)
+    res["mixed_prefill_decode"]["prefill_part_ms"] = round(ms_p, 4)
+    res["mixed_prefill_decode"]["prefill_part_TFLOP/s"] = round(flops / ms_p / 1e9, 1)
+    return res
+
 
 def _cpu_baseline(kind, args, nsample=None):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
@@ -423,6 +494,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", action="store_true",
+                    help="also time the long-context and mixed prefill+decode workloads (attention call only)")
     args = ap.parse_args()
     if args.impl == "reference":
         # the oracle runs single-threaded; fix BLAS threads before numpy loads

@@ -104,6 +104,7 @@ kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, 
     if (head_size != 64 && head_size != 128) return KV_INT4_EUNSUPPORTED;
     if (block_size != kBlockSize || num_kv_heads > 64 || !valid_dtype_16(dtype)) return KV_INT4_EUNSUPPORTED;
     if (num_tokens == 0) return KV_INT4_OK;
+    if (num_tokens * num_kv_heads * 2 >= (int64_t)1 << 31) return KV_INT4_EUNSUPPORTED;   // 32-bit vector index
     if (!k || !v || !slot_mapping || !rht_signs || !cache) return KV_INT4_EINVAL;
     if (!aligned16(k) || !aligned16(v) || !aligned16(cache)) return KV_INT4_EALIGN;
     WriteParams p;
@@ -124,8 +125,9 @@ kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, 
 int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
     if (num_seqs < 0 || max_seq_len < 0 || segment_len < 0) return 0;
     if (segment_len > 0) return (segment_len % kBlockSize == 0) ? segment_len : 0;
-    // Enough (sequence, segment) CTAs to keep two per SM busy, in multiples of 256 tokens.
-    const int64_t target = 2ll * num_sms();
+    // Enough (sequence, segment) CTAs for about four per SM of grid (two resident per SM, and
+    // sequences shorter than max_seq_len leave some of the grid idle), in multiples of 256 tokens.
+    const int64_t target = 4ll * num_sms();
     const int64_t work = (int64_t)num_seqs * (int64_t)max_seq_len;
     int64_t seg = (work + target - 1) / (target > 0 ? target : 1);
     seg = ((seg + 255) / 256) * 256;

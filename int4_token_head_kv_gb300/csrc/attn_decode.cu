@@ -26,7 +26,7 @@ namespace kvi4 {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kDecodeThreads = kConsumerWarps * 32;   // no producer warp: see the refill rule below
 constexpr int kStages = 4;
 
 struct DecodeSmem {
@@ -43,7 +43,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
     const uint32_t state = kConsumerWarps * 8u * D * 4u;
     s.state_off = ((ring > state ? ring : state) + 127u) & ~127u;
     const uint32_t tail = 2u * kStages * 8u      // full / empty barriers
-                          + kStages * 4u + 16u     // valid flags, abort flag
+                          + kStages * 4u + 16u     // valid flags, abort flag, refill counters
+                          + kStages * 4u + 16u
                           + D * 4u                 // signs
                           + (uint32_t)Hq * 4u      // alpha
                           + 2u * kConsumerWarps * 8u * 4u  // per-warp (m, l)
@@ -53,7 +54,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
 }
 
 template <int D, bool WIDE, typename QT, typename OT>
-__global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ AttnParams p) {
     using Gm = Geo<D>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int seg = blockIdx.x, seq = blockIdx.y;
@@ -88,10 +89,10 @@ __global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParam
     const DecodeSmem lay = decode_smem_layout<D>(H, Hq);
     uint8_t* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.state_off);
-    uint64_t* empty = full + kStages;
-    int* valid = reinterpret_cast<int*>(empty + kStages);
+    int* valid = reinterpret_cast<int*>(full + 2 * kStages);
     int* abort_flag = valid + kStages;
-    float* sgn = reinterpret_cast<float*>(abort_flag + 4);
+    int* released = abort_flag + 4;    // per stage: consumer warps done with its current block
+    float* sgn = reinterpret_cast<float*>(released + kStages + 4);
     float* alpha = sgn + D;
     float* st_m = alpha + Hq;
     float* st_l = st_m + kConsumerWarps * 8;
@@ -102,9 +103,10 @@ __global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParam
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            released[s] = 0;
         }
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;   // blocks issued so far
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
@@ -113,29 +115,30 @@ __global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParam
     const uint8_t* seq_cache = p.cache;
     const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + blk_first;
     const uint32_t stage_bytes = lay.stage_bytes;
-    uint64_t policy = 0;
-    int issued = 0;
+    // Ring refill rule: block i goes to stage i % kStages.  The first kStages blocks are issued up
+    // front; afterwards the LAST consumer warp to finish with block i (counted in released[])
+    // issues block i + kStages into the same stage, so no warp ever blocks waiting to refill.
     auto produce = [&](int i) {
         const int st = i % kStages;
         const int blk = __ldg(table + i);
         const bool ok = blk >= 0 && (int64_t)blk < p.num_blocks;
         valid[st] = ok ? 1 : 0;
+        atomicMax(&abort_flag[1], i + 1);
         if (ok) {
             mbar_arrive_expect_tx(&full[st], stage_bytes);
             bulk_copy_g2s(ring + (size_t)st * stage_bytes, seq_cache + (int64_t)blk * stage_bytes, stage_bytes, &full[st],
-                          policy);
+                          policy_evict_first());
         } else {
             count_status(p.status, 1);
             mbar_arrive(&full[st]);
         }
     };
-    if (warp == kConsumerWarps && lane == 0) {
-        policy = policy_evict_first();
-        for (; issued < min(kStages, nblk); ++issued) produce(issued);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < min(kStages, nblk); ++i) produce(i);
     }
 
     // Rotate this sequence's query (all Hq heads) into fp16 + per-head logit multiplier.
-    if (warp < kConsumerWarps) {
+    {
         for (int v = warp; v < Hq; v += kConsumerWarps) {
             const float a = rotate_query<D, QT>(p.q, ((int64_t)q0 * Hq + v) * D, sgn, qh + v * D, ql + v * D, p.c,
                                                 p.softmax_scale);
@@ -152,23 +155,7 @@ __global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParam
     uint32_t eref = 0;   // running max biased exponent of V scales seen so far
     const int g = lane >> 2, t = lane & 3;
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------------ producer
-        if (lane == 0) {
-            for (; issued < nblk; ++issued) {
-                const int st = issued % kStages;
-                if (!mbar_wait(&empty[st], ((issued / kStages) - 1) & 1)) {
-                    count_status(p.status, 3);
-                    atomicExch(abort_flag, 1);
-                    break;
-                }
-                if (*(volatile int*)abort_flag) break;
-                produce(issued);
-            }
-            // make sure no copy is still landing in the ring before it is reused / the CTA exits
-            for (int i = max(0, issued - kStages); i < issued; ++i) mbar_wait(&full[i % kStages], (i / kStages) & 1);
-        }
-    } else {
+    {
         // ------------------------------------------------------------------ consumers
         const int h = warp % H;
         const int wph = kConsumerWarps / H;
@@ -344,12 +331,26 @@ __global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParam
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (lane == 0) {
+                __threadfence_block();   // this warp's reads of the stage come before the count
+                if (atomicAdd(&released[st], 1) == kConsumerWarps - 1) {
+                    released[st] = 0;
+                    __threadfence_block();
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    if (i + kStages < nblk && !*(volatile int*)abort_flag) produce(i + kStages);
+                }
+            }
         }
     }
     // ---- per-warp state to shared memory, once the ring is drained
     __syncthreads();
-    if (warp < kConsumerWarps) {
+    if (threadIdx.x == 0 && abort_flag[0]) {
+        // a wait gave up: let every copy still in flight land before the ring is reused
+        const int issued = abort_flag[1];
+        for (int i = max(0, issued - kStages); i < issued; ++i) mbar_wait(&full[i % kStages], (i / kStages) & 1);
+    }
+    __syncthreads();
+    {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -387,7 +388,7 @@ __global__ void __maxnreg__(112) decode_kernel(const __grid_constant__ AttnParam
 
     // ---- merge the warps of each kv head, then finish (single segment) or store the partial
     const int wph = kConsumerWarps / H;
-    for (int v = warp; v < Hq; v += kConsumerWarps + 1) {
+    for (int v = warp; v < Hq; v += kConsumerWarps) {
         const int h = v / G, col = v % G;
         float M = kNegBig;
         for (int s = 0; s < wph; ++s) M = fmaxf(M, st_m[(h + s * H) * 8 + col]);

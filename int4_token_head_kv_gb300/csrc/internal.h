@@ -70,7 +70,10 @@ cudaError_t opt_in_smem(size_t bytes) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (done[dev] >= bytes) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    // prefer the largest shared-memory carve-out, so that several CTAs fit on an SM
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(Kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) done[dev] = bytes;
     return e;
 }

@@ -39,134 +39,261 @@ __device__ __forceinline__ float2 upcast_pair<__half>(uint32_t w) {
     return __half22float2(h);
 }
 
+// load_vector: D 16-bit inputs (D/2 little-endian pairs) -> fp32 after the sign flips (XOR masks on
+// the pairs: bit 15 of each half is the sign in fp16 and bf16) and the stride-1 butterflies.
+// encode_vector: the remaining butterflies, normalisation, scale / zero-point and codes; output
+// the D/8 code words and the scale word of the cache row.
 template <int D, typename T>
-__global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_constant__ WriteParams p) {
+__device__ __forceinline__ void load_vector(const uint4* src, const uint32_t* sign_mask, float (&u)[D]) {
+#pragma unroll
+    for (int cc = 0; cc < D / 8; ++cc) {
+        const uint4 q = src[cc];
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int j = cc * 4 + e;
+            const float2 x = upcast_pair<T>(w4[e] ^ sign_mask[j]);
+            // stride-1 butterfly straight from the pair
+            u[2 * j] = __fadd_rn(x.x, x.y);
+            u[2 * j + 1] = __fsub_rn(x.x, x.y);
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void encode_vector(float (&u)[D], float c, uint32_t (&words)[Geo<D>::KW + 1]) {
     using Gm = Geo<D>;
-    // Sign flips as XOR masks on pairs of 16-bit inputs (the sign bit is bit 15 of each half in
-    // both fp16 and bf16).
-    __shared__ uint32_t sign_mask[D / 2];
-    for (int j = threadIdx.x; j < D / 2; j += blockDim.x) {
+    // strides 2 .. D/2, two lanes at a time
+#pragma unroll
+    for (int hs = 2; hs < D; hs <<= 1) {
+#pragma unroll
+        for (int i = 0; i < D; i += 2) {
+            if (i & hs) continue;
+            const float2 a = make_float2(u[i], u[i + 1]);
+            const float2 b = make_float2(u[i + hs], u[i + hs + 1]);
+            const float2 s = add_f32x2(a, b);
+            const float2 d = sub_f32x2(a, b);
+            u[i] = s.x;
+            u[i + 1] = s.y;
+            u[i + hs] = d.x;
+            u[i + hs + 1] = d.y;
+        }
+    }
+    const float2 c2 = make_float2(c, c);
+#pragma unroll
+    for (int i = 0; i < D; i += 2) {
+        const float2 y = mul_f32x2(make_float2(u[i], u[i + 1]), c2);
+        u[i] = y.x;
+        u[i + 1] = y.y;
+    }
+    // min / max over the rotated vector (exact)
+    float mx0 = u[0], mx1 = u[1], mn0 = u[0], mn1 = u[1];
+#pragma unroll
+    for (int i = 2; i < D; i += 4) {
+        mx0 = max3(mx0, u[i], u[i + 1]);
+        mn0 = min3(mn0, u[i], u[i + 1]);
+        if (i + 3 < D) {
+            mx1 = max3(mx1, u[i + 2], u[i + 3]);
+            mn1 = min3(mn1, u[i + 2], u[i + 3]);
+        }
+    }
+    const float mx = fmaxf(mx0, mx1), mn = fminf(mn0, mn1);
+    float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+    if (!(s >= 1e-6f)) s = 1e-6f;
+    const uint32_t sb = __float_as_uint(s) & 0xFFFFFFF0u;
+    const float sp = __uint_as_float(sb);
+    const float zr = rintf(__fdiv_rn(-mn, sp));
+    const uint32_t zp = zr < 0.0f ? 0u : (zr > 15.0f ? 15u : (uint32_t)zr);
+    const float r = __frcp_rn(sp);
+    const float zpm = kRoundMagic + (float)zp;   // exact
+    // The map y -> RN(y * r + zpm) is monotone, so the codes of min and max bound all codes:
+    // clamping is needed only when one of them falls outside [0, 15].
+    const float lo = __fmaf_rn(mn, r, zpm), hi = __fmaf_rn(mx, r, zpm);
+    const bool clamp = !(lo >= kRoundMagic && hi <= kRoundMagic + 15.0f);
+    const float2 r2 = make_float2(r, r), z2 = make_float2(zpm, zpm);
+#pragma unroll
+    for (int wi = 0; wi < Gm::KW; ++wi) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            float2 f = fma_f32x2(make_float2(u[wi * 8 + k], u[wi * 8 + k + 1]), r2, z2);
+            if (clamp) {
+                f.x = fminf(fmaxf(f.x, kRoundMagic), kRoundMagic + 15.0f);
+                f.y = fminf(fmaxf(f.y, kRoundMagic), kRoundMagic + 15.0f);
+            }
+            acc += (__float_as_uint(f.x) << (4 * k)) + (__float_as_uint(f.y) << (4 * k + 4));
+        }
+        // each term carried kRoundMagicBits << 4k; their sum modulo 2^32 is 0x3F400000
+        words[wi] = acc - 0x3F400000u;
+    }
+    words[Gm::KW] = sb | zp;
+}
+
+// Work split: vectors are numbered v = (t * 2 + plane) * H + h, so H consecutive vectors are one
+// (token, plane) row group, contiguous in the cache.  Each warp owns tiles of 32 consecutive
+// vectors and works through them on its own (no CTA-wide barriers): it prefetches the next tile's
+// inputs with coalesced 16-byte cp.async copies into one of two padded shared-memory buffers
+// (row stride 2D + 16 bytes, so the 16-byte reads of 8 neighbouring rows hit distinct banks),
+// encodes the current tile with one vector per lane, stages the encoded rows in the buffer it just
+// read, and writes each row group with one bulk async store (when H divides 32 and a group is a
+// multiple of 16 bytes; otherwise each lane stores its own row).
+constexpr int kWarpVecs = 32;
+constexpr int kWriteWarps = kWriteThreads / 32;
+
+template <int D>
+struct WriteSmem {
+    static constexpr int kRowPad = 2 * D + 16;
+    static constexpr int kBuf = kWarpVecs * kRowPad;            // one tile of inputs
+    static constexpr int kPerWarp = 2 * kBuf;
+    static constexpr int kBytes = kWriteWarps * kPerWarp + (D / 2) * 4;
+};
+
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_store_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Vector index -> (row of K/V, plane) with 32-bit arithmetic; shifts when H is a power of two.
+struct VecIndex {
+    uint32_t H, hmask;
+    int hshift;   // -1: H is not a power of two
+    __device__ __forceinline__ void split(uint32_t v, uint32_t& token, uint32_t& h, uint32_t& plane) const {
+        uint32_t tp;
+        if (hshift >= 0) {
+            h = v & hmask;
+            tp = v >> hshift;
+        } else {
+            tp = v / H;
+            h = v - tp * H;
+        }
+        plane = tp & 1u;
+        token = tp >> 1;
+    }
+};
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_constant__ WriteParams p) {
+    using Gm = Geo<D>;
+    using Sm = WriteSmem<D>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint8_t* wbuf = smem + warp * Sm::kPerWarp;
+    uint32_t* sign_mask = reinterpret_cast<uint32_t*>(smem + kWriteWarps * Sm::kPerWarp);
+    for (int j = tid; j < D / 2; j += kWriteThreads) {
         const float s0 = p.signs[2 * j], s1 = p.signs[2 * j + 1];
         sign_mask[j] = ((__float_as_uint(s0) >> 31) << 15) | ((__float_as_uint(s1) >> 31) << 31);
         if (blockIdx.x == 0 && ((fabsf(s0) != 1.0f) || (fabsf(s1) != 1.0f))) count_status(p.status, 4);
     }
     __syncthreads();
 
-    const int H = p.H;
-    const int64_t nvec = p.num_tokens * H * 2;
-    for (int64_t vi = (int64_t)blockIdx.x * kWriteThreads + threadIdx.x; vi < nvec;
-         vi += (int64_t)gridDim.x * kWriteThreads) {
-        // vi = (t * 2 + plane) * H + h: a warp writes whole contiguous (token, plane) rows
-        const int h = (int)(vi % H);
-        const int64_t tp = vi / H;
-        const int plane = (int)(tp & 1);
-        const int64_t t = tp >> 1;
-        const int64_t slot = __ldg(p.slots + t);
-        if (slot < 0) continue;
-        if (slot >= p.num_slots) {
-            if (plane == 0 && h == 0) count_status(p.status, 0);
-            continue;
-        }
+    const uint32_t H = (uint32_t)p.H;
+    VecIndex vx;
+    vx.H = H;
+    vx.hmask = H - 1;
+    vx.hshift = (H & (H - 1)) == 0 ? __ffs(H) - 1 : -1;
+    const uint32_t nvec = (uint32_t)(p.num_tokens * H * 2);
+    const uint32_t ntiles = (nvec + kWarpVecs - 1) / kWarpVecs;
+    const uint32_t gwarp = blockIdx.x * kWriteWarps + warp, nwarps = gridDim.x * kWriteWarps;
+    constexpr int kChunks = D * 2 / 16;                 // 16-byte chunks per input vector
+    const uint32_t group_bytes = H * Gm::RB;
+    const bool grouped = vx.hshift >= 0 && H <= (uint32_t)kWarpVecs && (group_bytes % 16) == 0;
+    const uint8_t* kin = static_cast<const uint8_t*>(p.k);
+    const uint8_t* vin = static_cast<const uint8_t*>(p.v);
 
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(plane ? p.v : p.k) +
-                                                          (t * H + h) * D);
+    // lane copies chunks lane + 32 k of the tile: vector (lane + 32 k) / kChunks, chunk (lane % kChunks)
+    auto prefetch = [&](uint32_t tile, uint8_t* buf) {
+        const uint32_t v0 = tile * kWarpVecs;
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+            const uint32_t ci = lane + 32 * k;
+            const uint32_t vl = ci / kChunks, c = ci % kChunks;
+            if (v0 + vl < nvec) {
+                uint32_t tok, h, pl;
+                vx.split(v0 + vl, tok, h, pl);
+                const uint8_t* src = (pl ? vin : kin) + ((uint64_t)(tok * H + h) * (D * 2) + c * 16);
+                cp_async_16(buf + vl * Sm::kRowPad + c * 16, src);
+            }
+        }
+        cp_async_commit();
+    };
+
+    uint32_t tile = gwarp;
+    int it = 0;
+    if (tile < ntiles) prefetch(tile, wbuf);
+    for (; tile < ntiles; tile += nwarps, ++it) {
+        uint8_t* cur = wbuf + (it & 1) * Sm::kBuf;
+        uint8_t* nxt = wbuf + ((it + 1) & 1) * Sm::kBuf;
+        // the other buffer was last an output stage: its bulk stores must have read it
+        if (grouped) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        if (tile + nwarps < ntiles) prefetch(tile + nwarps, nxt);
+        else cp_async_commit();   // keep one group per iteration
+        cp_async_wait_1();
+        __syncwarp();
+        const uint32_t v = tile * kWarpVecs + lane;
+        const bool live = v < nvec;
         float u[D];
+        if (live) load_vector<D, T>(reinterpret_cast<const uint4*>(cur + lane * Sm::kRowPad), sign_mask, u);
+        __syncwarp();   // the tile's inputs are in registers; its buffer becomes the output stage
+        uint32_t words[Gm::KW + 1];
+        if (live) encode_vector<D>(u, p.c, words);
+        uint32_t tok = 0, h = 0, pl = 0;
+        if (live) vx.split(v, tok, h, pl);
+        if (grouped) {
+            uint32_t* orow = reinterpret_cast<uint32_t*>(cur + lane * Gm::RB);
+            if (live) {
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 q = __ldg(src + c);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = c * 4 + e;
-                const float2 x = upcast_pair<T>(w4[e] ^ sign_mask[j]);
-                // stride-1 butterfly straight from the pair
-                u[2 * j] = __fadd_rn(x.x, x.y);
-                u[2 * j + 1] = __fsub_rn(x.x, x.y);
+                for (int wi = 0; wi <= Gm::KW; ++wi) orow[wi] = words[wi];
             }
-        }
-        // strides 2 .. D/2, two lanes at a time
-#pragma unroll
-        for (int hs = 2; hs < D; hs <<= 1) {
-#pragma unroll
-            for (int i = 0; i < D; i += 2) {
-                if (i & hs) continue;
-                const float2 a = make_float2(u[i], u[i + 1]);
-                const float2 b = make_float2(u[i + hs], u[i + hs + 1]);
-                const float2 s = add_f32x2(a, b);
-                const float2 d = sub_f32x2(a, b);
-                u[i] = s.x;
-                u[i + 1] = s.y;
-                u[i + hs] = d.x;
-                u[i + hs + 1] = d.y;
-            }
-        }
-        const float2 c2 = make_float2(p.c, p.c);
-#pragma unroll
-        for (int i = 0; i < D; i += 2) {
-            const float2 y = mul_f32x2(make_float2(u[i], u[i + 1]), c2);
-            u[i] = y.x;
-            u[i + 1] = y.y;
-        }
-        // min / max over the rotated vector (exact)
-        float mx0 = u[0], mx1 = u[1], mn0 = u[0], mn1 = u[1];
-#pragma unroll
-        for (int i = 2; i < D; i += 4) {
-            mx0 = max3(mx0, u[i], u[i + 1]);
-            mn0 = min3(mn0, u[i], u[i + 1]);
-            if (i + 3 < D) {
-                mx1 = max3(mx1, u[i + 2], u[i + 3]);
-                mn1 = min3(mn1, u[i + 2], u[i + 3]);
-            }
-        }
-        const float mx = fmaxf(mx0, mx1), mn = fminf(mn0, mn1);
-        float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
-        if (!(s >= 1e-6f)) s = 1e-6f;
-        const uint32_t sb = __float_as_uint(s) & 0xFFFFFFF0u;
-        const float sp = __uint_as_float(sb);
-        const float zr = rintf(__fdiv_rn(-mn, sp));
-        const uint32_t zp = zr < 0.0f ? 0u : (zr > 15.0f ? 15u : (uint32_t)zr);
-        const float r = __frcp_rn(sp);
-        const float zpm = kRoundMagic + (float)zp;   // exact
-        // The map y -> RN(y * r + zpm) is monotone, so the codes of min and max bound all codes:
-        // clamping is needed only when one of them falls outside [0, 15].
-        const float lo = __fmaf_rn(mn, r, zpm), hi = __fmaf_rn(mx, r, zpm);
-        const bool clamp = !(lo >= kRoundMagic && hi <= kRoundMagic + 15.0f);
-        const float2 r2 = make_float2(r, r), z2 = make_float2(zpm, zpm);
-
-        uint32_t words[Gm::KW];
-#pragma unroll
-        for (int wi = 0; wi < Gm::KW; ++wi) {
-            uint32_t acc = 0;
-#pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-                float2 f = fma_f32x2(make_float2(u[wi * 8 + k], u[wi * 8 + k + 1]), r2, z2);
-                if (clamp) {
-                    f.x = fminf(fmaxf(f.x, kRoundMagic), kRoundMagic + 15.0f);
-                    f.y = fminf(fmaxf(f.y, kRoundMagic), kRoundMagic + 15.0f);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staged rows -> bulk store
+            __syncwarp();
+            // the first lane of each row group stores the whole group
+            if (live && h == 0) {
+                const int64_t slot = __ldg(p.slots + tok);
+                if (slot >= p.num_slots) {
+                    if (pl == 0) count_status(p.status, 0);
+                } else if (slot >= 0) {
+                    const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+                    bulk_store_s2g(p.cache + ((blk * 2 + pl) * kBlockSize + off) * (int64_t)group_bytes,
+                                   cur + lane * Gm::RB, group_bytes);
                 }
-                acc += (__float_as_uint(f.x) << (4 * k)) + (__float_as_uint(f.y) << (4 * k + 4));
             }
-            // each term carried kRoundMagicBits << 4k; their sum modulo 2^32 is 0x3F400000
-            words[wi] = acc - 0x3F400000u;
-        }
-
-        const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-        uint32_t* row = reinterpret_cast<uint32_t*>(p.cache + (((blk * 2 + plane) * kBlockSize + off) * H + h) * Gm::RB);
+        } else if (live) {
+            const int64_t slot = __ldg(p.slots + tok);
+            if (slot >= p.num_slots) {
+                if (pl == 0 && h == 0) count_status(p.status, 0);
+            } else if (slot >= 0) {
+                const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+                uint32_t* row = reinterpret_cast<uint32_t*>(p.cache + (((blk * 2 + pl) * kBlockSize + off) * H + h) * Gm::RB);
 #pragma unroll
-        for (int wi = 0; wi < Gm::KW; ++wi) row[wi] = words[wi];
-        row[Gm::KW] = sb | zp;
+                for (int wi = 0; wi <= Gm::KW; ++wi) row[wi] = words[wi];
+            }
+        }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (grouped) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     (void)kRoundMagicBits;
 }
 
 template <int D, typename T>
 cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
-    const int64_t nvec = p.num_tokens * p.H * 2;
-    int64_t blocks = (nvec + kWriteThreads - 1) / kWriteThreads;
-    const int64_t cap = (int64_t)num_sms() * 64;
+    using Sm = WriteSmem<D>;
+    const int64_t ntiles = (p.num_tokens * p.H * 2 + kWarpVecs - 1) / kWarpVecs;
+    int64_t blocks = (ntiles + kWriteWarps - 1) / kWriteWarps;
+    const int64_t cap = (int64_t)num_sms() * 3;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    write_kernel<D, T><<<(unsigned)blocks, kWriteThreads, 0, stream>>>(p);
+    cudaError_t err = opt_in_smem<write_kernel<D, T>>(Sm::kBytes);
+    if (err != cudaSuccess) return err;
+    write_kernel<D, T><<<(unsigned)blocks, kWriteThreads, Sm::kBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
