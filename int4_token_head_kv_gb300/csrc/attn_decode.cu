@@ -10,9 +10,11 @@
 //
 // GB300 design:
 //  * One CTA per (sequence, segment) covers ALL kv heads, so each 16-token block is one
-//    contiguous 16-byte-aligned region (K plane then V plane, 2 * 16 * H * (D/2+4) bytes) that a
-//    producer warp streams into a 4-stage shared-memory ring with 1-D bulk async copies
-//    (cp.async.bulk + mbarrier transaction counts, L2 evict-first).
+//    contiguous 16-byte-aligned region (K plane then V plane, 2 * 16 * H * (D/2+4) bytes) that is
+//    streamed into a 4-stage shared-memory ring with 1-D bulk async copies (cp.async.bulk +
+//    mbarrier transaction counts, L2 evict-first).  There is no producer warp: the segment's block
+//    ids are staged in shared memory up front, four lanes issue the first four copies, and the
+//    last consumer warp to finish with a stage issues its next block.
 //  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block when H < 8).
 //    Scores S^T[16 tokens x 8 heads] = (K - zp)[16 x D] . Q'^T come from mma.sync m16n8k16 on
 //    fp16 operands built straight from the packed bytes (codes and code - zp are exact in fp16);
@@ -28,6 +30,7 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = kConsumerWarps * 32;   // no producer warp: see the refill rule below
 constexpr int kStages = 4;
+constexpr int kTableWin = 512;   // block-table entries of a CTA's segment staged in shared memory
 
 struct DecodeSmem {
     uint32_t stage_bytes;   // one block (K + V planes)
@@ -43,8 +46,9 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
     const uint32_t state = kConsumerWarps * 8u * D * 4u;
     s.state_off = ((ring > state ? ring : state) + 127u) & ~127u;
     const uint32_t tail = 2u * kStages * 8u      // full / empty barriers
-                          + kStages * 4u + 16u     // valid flags, abort flag, refill counters
-                          + kStages * 4u + 16u
+                          + kStages * 4u + 16u     // valid flags, abort flag
+                          + kStages * 4u + 16u     // refill counters
+                          + kTableWin * 4u         // block-table window
                           + D * 4u                 // signs
                           + (uint32_t)Hq * 4u      // alpha
                           + 2u * kConsumerWarps * 8u * 4u  // per-warp (m, l)
@@ -92,7 +96,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     int* valid = reinterpret_cast<int*>(full + 2 * kStages);
     int* abort_flag = valid + kStages;
     int* released = abort_flag + 4;    // per stage: consumer warps done with its current block
-    float* sgn = reinterpret_cast<float*>(released + kStages + 4);
+    int* tbl = released + kStages + 4;    // block ids of this segment's first kTableWin blocks
+    float* sgn = reinterpret_cast<float*>(tbl + kTableWin);
     float* alpha = sgn + D;
     float* st_m = alpha + Hq;
     float* st_l = st_m + kConsumerWarps * 8;
@@ -109,18 +114,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         abort_flag[1] = 0;   // blocks issued so far
         fence_mbar_init();
     }
+    const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + blk_first;
+    // one coalesced load of the segment's block ids, so that no ring refill waits on global memory
+    for (int i = threadIdx.x; i < min(nblk, kTableWin); i += blockDim.x) tbl[i] = __ldg(table + i);
     for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
     __syncthreads();
 
     const uint8_t* seq_cache = p.cache;
-    const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + blk_first;
     const uint32_t stage_bytes = lay.stage_bytes;
     // Ring refill rule: block i goes to stage i % kStages.  The first kStages blocks are issued up
     // front; afterwards the LAST consumer warp to finish with block i (counted in released[])
     // issues block i + kStages into the same stage, so no warp ever blocks waiting to refill.
     auto produce = [&](int i) {
         const int st = i % kStages;
-        const int blk = __ldg(table + i);
+        const int blk = i < kTableWin ? tbl[i] : __ldg(table + i);
         const bool ok = blk >= 0 && (int64_t)blk < p.num_blocks;
         valid[st] = ok ? 1 : 0;
         atomicMax(&abort_flag[1], i + 1);
@@ -133,17 +140,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             mbar_arrive(&full[st]);
         }
     };
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < min(kStages, nblk); ++i) produce(i);
-    }
+    if (threadIdx.x < min(kStages, nblk)) produce(threadIdx.x);   // the first copies, one lane each
 
-    // Rotate this sequence's query (all Hq heads) into fp16 + per-head logit multiplier.
-    {
-        for (int v = warp; v < Hq; v += kConsumerWarps) {
-            const float a = rotate_query<D, QT>(p.q, ((int64_t)q0 * Hq + v) * D, sgn, qh + v * D, ql + v * D, p.c,
-                                                p.softmax_scale);
-            if (lane == 0) alpha[v] = a;
+    // Rotate this sequence's query (all Hq heads) into fp16 halves + per-head logit multiplier,
+    // four vectors per warp at a time.
+    for (int v0 = warp; v0 < Hq; v0 += 4 * kConsumerWarps) {
+        int64_t rows[4];
+        int slot[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int v = v0 + k * kConsumerWarps;
+            rows[k] = v < Hq ? (int64_t)q0 * Hq + v : -1;
+            slot[k] = v < Hq ? v : 0;
         }
+        rotate_queries<D, QT, 4>(p.q, rows, slot, sgn, qh, ql, alpha, p.c, p.softmax_scale);
     }
     __syncthreads();
 
@@ -197,56 +207,84 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         const float al1 = (hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
         const bool lo_lane = !WIDE && t >= 2;   // this lane's P columns carry low halves
 
-        for (int i = 0; i < nblk; ++i) {
-            const int st = i % kStages;
-            if (!mbar_wait(&full[st], (i / kStages) & 1)) {
+        // Two blocks (32 tokens) per iteration: their score chains, one softmax update and their
+        // P.V products interleave, which gives each warp independent work to overlap latencies.
+        for (int i = 0; i < nblk; i += 2) {
+            const int npair = min(2, nblk - i);
+            int st[2];
+            bool ok[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) st[b] = (i + b) % kStages;
+            bool timed_out = false;
+            for (int b = 0; b < npair; ++b) {
+                if (!mbar_wait(&full[st[b]], ((i + b) / kStages) & 1)) timed_out = true;
+            }
+            if (timed_out) {
                 if (lane == 0) {
                     count_status(p.status, 3);
                     atomicExch(abort_flag, 1);
                 }
                 break;
             }
-            if ((i % wph) == sub && valid[st]) {
-                const uint8_t* kp = ring + (size_t)st * stage_bytes;
-                const uint8_t* vp = kp + (size_t)kBlockSize * H * Gm::RB;
-                const int tokbase = (blk_first + i) * kBlockSize;
-                const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp + (tk0 * H + h) * Gm::RB);
-                const uint32_t* kr1 = reinterpret_cast<const uint32_t*>(kp + (tk1 * H + h) * Gm::RB);
-                const uint32_t ks0 = kr0[Gm::KW], ks1 = kr1[Gm::KW];
-                // ---- S^T = (K - zp) Q'^T, high and low halves of Q'
-                float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                float cl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                {
-                    const uint32_t z0l = zp_lo_half(ks0 & 15u), z0h = zp_hi_half(ks0 & 15u);
-                    const uint32_t z1l = zp_lo_half(ks1 & 15u), z1h = zp_hi_half(ks1 & 15u);
-                    const uint32_t zl0 = z0l | (z0l << 16), zh0 = z0h | (z0h << 16);
-                    const uint32_t zl1 = z1l | (z1l << 16), zh1 = z1h | (z1h << 16);
 #pragma unroll
-                    for (int j = 0; j < Gm::KWPT; ++j) {
-                        uint32_t a0[4], a1[4];
-                        unpack_word(kr0[t + 4 * j], zl0, zh0, a0);
-                        unpack_word(kr1[t + 4 * j], zl1, zh1, a1);
-                        mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * j][0], qb[2 * j][1]);
-                        mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][0], qb[2 * j + 1][1]);
-                        if constexpr (WIDE) {
-                            mma_f16_16816(cl, a0[0], a1[0], a0[1], a1[1], qb[2 * j][2], qb[2 * j][3]);
-                            mma_f16_16816(cl, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][2], qb[2 * j + 1][3]);
+            for (int b = 0; b < 2; ++b) ok[b] = b < npair && valid[st[b]];
+            if (((i >> 1) % wph) == sub && (ok[0] || ok[1])) {
+                const uint8_t* kp[2];
+                const uint8_t* vp[2];
+                int tokbase[2];
+                float x[2][4];
+                uint32_t vs0[2], vs1[2];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    kp[b] = ring + (size_t)st[b] * stage_bytes;
+                    vp[b] = kp[b] + (size_t)kBlockSize * H * Gm::RB;
+                    tokbase[b] = (blk_first + i + b) * kBlockSize;
+                }
+                // ---- S^T = (K - zp) Q'^T for both blocks, high and low halves of Q'
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp[b] + (tk0 * H + h) * Gm::RB);
+                    const uint32_t* kr1 = reinterpret_cast<const uint32_t*>(kp[b] + (tk1 * H + h) * Gm::RB);
+                    const uint32_t ks0 = kr0[Gm::KW], ks1 = kr1[Gm::KW];
+                    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    float cl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    if (ok[b]) {
+                        const uint32_t z0l = zp_lo_half(ks0 & 15u), z0h = zp_hi_half(ks0 & 15u);
+                        const uint32_t z1l = zp_lo_half(ks1 & 15u), z1h = zp_hi_half(ks1 & 15u);
+                        const uint32_t zl0 = z0l | (z0l << 16), zh0 = z0h | (z0h << 16);
+                        const uint32_t zl1 = z1l | (z1l << 16), zh1 = z1h | (z1h << 16);
+#pragma unroll
+                        for (int j = 0; j < Gm::KWPT; ++j) {
+                            uint32_t a0[4], a1[4];
+                            unpack_word(kr0[t + 4 * j], zl0, zh0, a0);
+                            unpack_word(kr1[t + 4 * j], zl1, zh1, a1);
+                            mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * j][0], qb[2 * j][1]);
+                            mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][0], qb[2 * j + 1][1]);
+                            if constexpr (WIDE) {
+                                mma_f16_16816(cl, a0[0], a1[0], a0[1], a1[1], qb[2 * j][2], qb[2 * j][3]);
+                                mma_f16_16816(cl, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][2], qb[2 * j + 1][3]);
+                            }
                         }
                     }
-                }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if constexpr (WIDE) c[e] += cl[e];
-                    else c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);   // high + low columns
+                    for (int e = 0; e < 4; ++e) {
+                        if constexpr (WIDE) c[e] += cl[e];
+                        else c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);   // high + low columns
+                    }
+                    const bool v0 = ok[b] && tokbase[b] + tk0 < tok_end, v1 = ok[b] && tokbase[b] + tk1 < tok_end;
+                    const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
+                    x[b][0] = v0 ? c[0] * sk0 * al0 : -INFINITY;
+                    x[b][1] = v0 ? c[1] * sk0 * al1 : -INFINITY;
+                    x[b][2] = v1 ? c[2] * sk1 * al0 : -INFINITY;
+                    x[b][3] = v1 ? c[3] * sk1 * al1 : -INFINITY;
+                    const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp[b] + (tk0 * H + h) * Gm::RB);
+                    const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp[b] + (tk1 * H + h) * Gm::RB);
+                    vs0[b] = v0 ? vg0[Gm::KW] : 0u;   // invisible tokens: scale word 0 (exponent 0, weight 0)
+                    vs1[b] = v1 ? vg1[Gm::KW] : 0u;
                 }
-                // ---- logits (log2 units), masking, online softmax for heads hb, hb+1
-                const bool v0 = tokbase + tk0 < tok_end, v1 = tokbase + tk1 < tok_end;
-                const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
-                const float x0 = v0 ? c[0] * sk0 * al0 : -INFINITY;
-                const float x1 = v0 ? c[1] * sk0 * al1 : -INFINITY;
-                const float x2 = v1 ? c[2] * sk1 * al0 : -INFINITY;
-                const float x3 = v1 ? c[3] * sk1 * al1 : -INFINITY;
-                float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+                // ---- one online-softmax update for heads hb, hb+1 over the 32 tokens
+                float bm0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+                float bm1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
@@ -254,18 +292,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 }
                 const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
                 const float r0 = fast_exp2(m0 - mn0), r1 = fast_exp2(m1 - mn1);
-                const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
-                const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+                float pr[2][4];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    pr[b][0] = fast_exp2(x[b][0] - mn0);
+                    pr[b][1] = fast_exp2(x[b][1] - mn1);
+                    pr[b][2] = fast_exp2(x[b][2] - mn0);
+                    pr[b][3] = fast_exp2(x[b][3] - mn1);
+                }
                 m0 = mn0;
                 m1 = mn1;
-                l0 = l0 * r0 + (p0 + p2);
-                l1 = l1 * r1 + (p1 + p3);
+                l0 = l0 * r0 + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
+                l1 = l1 * r1 + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
                 // ---- V scales: exponent reference so the fp16 weights stay in range
-                const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp + (tk0 * H + h) * Gm::RB);
-                const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp + (tk1 * H + h) * Gm::RB);
-                const uint32_t vs0 = vg0[Gm::KW], vs1 = vg1[Gm::KW];
-                const uint32_t e0 = v0 ? (vs0 >> 23) & 0xFFu : 0u, e1 = v1 ? (vs1 >> 23) & 0xFFu : 0u;
-                const uint32_t eblk = __reduce_max_sync(0xffffffffu, max(e0, e1));
+                const uint32_t emax = max(max((vs0[0] >> 23) & 0xFFu, (vs1[0] >> 23) & 0xFFu),
+                                          max((vs0[1] >> 23) & 0xFFu, (vs1[1] >> 23) & 0xFFu));
+                const uint32_t eblk = __reduce_max_sync(0xffffffffu, emax);
                 float escale = 1.0f;
                 if (eblk > eref) {
                     // 2^(eref - eblk); 0 when nothing was accumulated yet or the jump underflows
@@ -283,61 +325,68 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     }
                 }
                 const float wsc = __uint_as_float((254u - eref) << 23);   // 2^(127 - eref)
-                const float sv0 = __uint_as_float(vs0 & 0xFFFFFFF0u) * wsc, sv1 = __uint_as_float(vs1 & 0xFFFFFFF0u) * wsc;
-                // weights w = p * s'_V * 2^-E as fp16 high + low halves
-                uint32_t xlo_h, xlo_l, xhi_h, xhi_l;
-                split_f16x2(v0 ? p0 * sv0 : 0.0f, v0 ? p1 * sv0 : 0.0f, xlo_h, xlo_l);
-                split_f16x2(v1 ? p2 * sv1 : 0.0f, v1 ? p3 * sv1 : 0.0f, xhi_h, xhi_l);
-                uint32_t b0, b1, b0l = 0, b1l = 0;
-                if constexpr (WIDE) {
-                    b0 = movmatrix_trans(xlo_h);
-                    b1 = movmatrix_trans(xhi_h);
-                    b0l = movmatrix_trans(xlo_l);
-                    b1l = movmatrix_trans(xhi_l);
-                } else {
-                    b0 = movmatrix_trans(lo_lane ? xlo_l : xlo_h);
-                    b1 = movmatrix_trans(lo_lane ? xhi_l : xhi_h);
-                }
-                // ---- O^T += (V - zp)^T P^T
-                const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp + ((t)*H + h) * Gm::RB);
-                const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp + ((t + 4) * H + h) * Gm::RB);
-                const uint32_t* vr2 = reinterpret_cast<const uint32_t*>(vp + ((t + 8) * H + h) * Gm::RB);
-                const uint32_t* vr3 = reinterpret_cast<const uint32_t*>(vp + ((t + 12) * H + h) * Gm::RB);
-                const uint32_t w0 = vr0[Gm::KW], w1 = vr1[Gm::KW], w2 = vr2[Gm::KW], w3 = vr3[Gm::KW];
-                const uint32_t zl01 = zp_lo_half(w0 & 15u) | (zp_lo_half(w1 & 15u) << 16);
-                const uint32_t zh01 = zp_hi_half(w0 & 15u) | (zp_hi_half(w1 & 15u) << 16);
-                const uint32_t zl23 = zp_lo_half(w2 & 15u) | (zp_lo_half(w3 & 15u) << 16);
-                const uint32_t zh23 = zp_hi_half(w2 & 15u) | (zp_hi_half(w3 & 15u) << 16);
-                if constexpr (D == 128) {
-                    uint32_t ua[8], ub[8], uc[8], ud[8];
-                    unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);           // d = 8g + i, tokens t, t+4
-                    unpack_word_pair(vr0[g + 8], vr1[g + 8], zl01, zh01, ub);   // d = 64 + 8g + i
-                    unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);           // tokens t+8, t+12
-                    unpack_word_pair(vr2[g + 8], vr3[g + 8], zl23, zh23, ud);
+                // ---- O^T += (V - zp)^T P^T for both blocks
 #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0, b1);
-                        if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0l, b1l);
+                for (int b = 0; b < 2; ++b) {
+                    if (!ok[b]) continue;
+                    const float sv0 = __uint_as_float(vs0[b] & 0xFFFFFFF0u) * wsc;
+                    const float sv1 = __uint_as_float(vs1[b] & 0xFFFFFFF0u) * wsc;
+                    // weights w = p * s'_V * 2^-E as fp16 high + low halves (invisible tokens: 0)
+                    uint32_t xlo_h, xlo_l, xhi_h, xhi_l;
+                    split_f16x2(pr[b][0] * sv0, pr[b][1] * sv0, xlo_h, xlo_l);
+                    split_f16x2(pr[b][2] * sv1, pr[b][3] * sv1, xhi_h, xhi_l);
+                    uint32_t b0, b1, b0l = 0, b1l = 0;
+                    if constexpr (WIDE) {
+                        b0 = movmatrix_trans(xlo_h);
+                        b1 = movmatrix_trans(xhi_h);
+                        b0l = movmatrix_trans(xlo_l);
+                        b1l = movmatrix_trans(xhi_l);
+                    } else {
+                        b0 = movmatrix_trans(lo_lane ? xlo_l : xlo_h);
+                        b1 = movmatrix_trans(lo_lane ? xhi_l : xhi_h);
                     }
-                } else {
-                    uint32_t ua[8], uc[8];
-                    unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);   // d = 8g + i
-                    unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);
+                    const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp[b] + ((t)*H + h) * Gm::RB);
+                    const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 4) * H + h) * Gm::RB);
+                    const uint32_t* vr2 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 8) * H + h) * Gm::RB);
+                    const uint32_t* vr3 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 12) * H + h) * Gm::RB);
+                    const uint32_t w0 = vr0[Gm::KW], w1 = vr1[Gm::KW], w2 = vr2[Gm::KW], w3 = vr3[Gm::KW];
+                    const uint32_t zl01 = zp_lo_half(w0 & 15u) | (zp_lo_half(w1 & 15u) << 16);
+                    const uint32_t zh01 = zp_hi_half(w0 & 15u) | (zp_hi_half(w1 & 15u) << 16);
+                    const uint32_t zl23 = zp_lo_half(w2 & 15u) | (zp_lo_half(w3 & 15u) << 16);
+                    const uint32_t zh23 = zp_hi_half(w2 & 15u) | (zp_hi_half(w3 & 15u) << 16);
+                    if constexpr (D == 128) {
+                        uint32_t ua[8], ub[8], uc[8], ud[8];
+                        unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);           // d = 8g + i, tokens t, t+4
+                        unpack_word_pair(vr0[g + 8], vr1[g + 8], zl01, zh01, ub);   // d = 64 + 8g + i
+                        unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);           // tokens t+8, t+12
+                        unpack_word_pair(vr2[g + 8], vr3[g + 8], zl23, zh23, ud);
 #pragma unroll
-                    for (int mt = 0; mt < 4; ++mt) {
-                        mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0, b1);
-                        if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0l, b1l);
+                        for (int mt = 0; mt < 8; ++mt) {
+                            mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0, b1);
+                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0l, b1l);
+                        }
+                    } else {
+                        uint32_t ua[8], uc[8];
+                        unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);   // d = 8g + i
+                        unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);
+#pragma unroll
+                        for (int mt = 0; mt < 4; ++mt) {
+                            mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0, b1);
+                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0l, b1l);
+                        }
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) {
-                __threadfence_block();   // this warp's reads of the stage come before the count
-                if (atomicAdd(&released[st], 1) == kConsumerWarps - 1) {
-                    released[st] = 0;
-                    __threadfence_block();
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    if (i + kStages < nblk && !*(volatile int*)abort_flag) produce(i + kStages);
+                __threadfence_block();   // this warp's reads of the stages come before the counts
+                for (int b = 0; b < npair; ++b) {
+                    if (atomicAdd(&released[st[b]], 1) == kConsumerWarps - 1) {
+                        released[st[b]] = 0;
+                        __threadfence_block();
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        if (i + b + kStages < nblk && !*(volatile int*)abort_flag) produce(i + b + kStages);
+                    }
                 }
             }
         }
@@ -386,34 +435,45 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     }
     __syncthreads();
 
-    // ---- merge the warps of each kv head, then finish (single segment) or store the partial
+    // ---- merge the warps of each kv head, then finish (single segment) or store the partial;
+    // four vectors per warp at a time
     const int wph = kConsumerWarps / H;
-    for (int v = warp; v < Hq; v += kConsumerWarps) {
-        const int h = v / G, col = v % G;
-        float M = kNegBig;
-        for (int s = 0; s < wph; ++s) M = fmaxf(M, st_m[(h + s * H) * 8 + col]);
-        float Lsum = 0.0f;
-        float acc[D / 32];
+    for (int v0 = warp; v0 < Hq; v0 += 4 * kConsumerWarps) {
+        float acc[4][D / 32], inv_l[4];
+        int64_t ooff[4];
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
-        for (int s = 0; s < wph; ++s) {
-            const int w = h + s * H;
-            const float wt = fast_exp2(st_m[w * 8 + col] - M);
-            Lsum += wt * st_l[w * 8 + col];
+        for (int k = 0; k < 4; ++k) {
+            const int v = v0 + k * kConsumerWarps;
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) acc[k] += wt * st_o[(w * 8 + col) * D + lane + 32 * k];
-        }
-        if (nseg == 1) {
-            unrotate_store<D, OT>(acc, Lsum > 0.0f ? 1.0f / Lsum : 0.0f, sgn, p.c, p.out, ((int64_t)q0 * Hq + v) * D);
-        } else {
-            const int64_t pi = ((int64_t)seq * Hq + v) * p.nseg_max + seg;
+            for (int j = 0; j < D / 32; ++j) acc[k][j] = 0.0f;
+            inv_l[k] = 0.0f;
+            ooff[k] = -1;
+            if (v >= Hq) continue;
+            const int h = v / G, col = v % G;
+            float M = kNegBig;
+            for (int s = 0; s < wph; ++s) M = fmaxf(M, st_m[(h + s * H) * 8 + col]);
+            float Lsum = 0.0f;
+            for (int s = 0; s < wph; ++s) {
+                const int w = h + s * H;
+                const float wt = fast_exp2(st_m[w * 8 + col] - M);
+                Lsum += wt * st_l[w * 8 + col];
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) p.ws_o[pi * D + lane + 32 * k] = acc[k];
-            if (lane == 0) {
-                p.ws_ml[pi * 2] = M;
-                p.ws_ml[pi * 2 + 1] = Lsum;
+                for (int j = 0; j < D / 32; ++j) acc[k][j] += wt * st_o[(w * 8 + col) * D + lane + 32 * j];
+            }
+            if (nseg == 1) {
+                inv_l[k] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+                ooff[k] = ((int64_t)q0 * Hq + v) * D;
+            } else {
+                const int64_t pi = ((int64_t)seq * Hq + v) * p.nseg_max + seg;
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) p.ws_o[pi * D + lane + 32 * j] = acc[k][j];
+                if (lane == 0) {
+                    p.ws_ml[pi * 2] = M;
+                    p.ws_ml[pi * 2 + 1] = Lsum;
+                }
             }
         }
+        if (nseg == 1) unrotate_store_batch<D, OT, 4>(acc, inv_l, sgn, p.c, p.out, ooff);
     }
 }
 
@@ -434,18 +494,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
     const int nseg = (L + p.seg_len - 1) / p.seg_len;
     if (nseg <= 1) return;
     const int64_t base = ((int64_t)seq * p.Hq + v) * p.nseg_max;
+    // lanes run over segments: global max, per-segment weights and the weighted sum of l
     float M = kNegBig;
-    for (int s = 0; s < nseg; ++s) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
-    float Lsum = 0.0f;
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+        const int s = s0 + lane;
+        if (s < nseg) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
+    }
+    M = warp_max(M);
+    float Lpart = 0.0f;
     float acc[D / 32];
 #pragma unroll
     for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
-    for (int s = 0; s < nseg; ++s) {
-        const float wt = fast_exp2(p.ws_ml[(base + s) * 2] - M);
-        Lsum += wt * p.ws_ml[(base + s) * 2 + 1];
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+        const int s = s0 + lane;
+        const float wt = s < nseg ? fast_exp2(p.ws_ml[(base + s) * 2] - M) : 0.0f;
+        if (s < nseg) Lpart += wt * p.ws_ml[(base + s) * 2 + 1];
+        const int n = min(32, nseg - s0);
+        // partial outputs of this group of segments: independent loads, four segments at a time
+        for (int j0 = 0; j0 < n; j0 += 4) {
+            float o4[4][D / 32], w4[4];
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) acc[k] += wt * p.ws_o[(base + s) * D + lane + 32 * k];
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u;
+                w4[u] = __shfl_sync(0xffffffffu, wt, j & 31);
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k)
+                    o4[u][k] = j < n ? p.ws_o[(base + s0 + j) * D + lane + 32 * k] : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) acc[k] += w4[u] * o4[u][k];
+            }
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lpart += __shfl_xor_sync(0xffffffffu, Lpart, o);
+    const float Lsum = Lpart;
     unrotate_store<D, OT>(acc, Lsum > 0.0f ? 1.0f / Lsum : 0.0f, sgn, p.c, p.out, ((int64_t)q0 * p.Hq + v) * D);
 }
 
