@@ -175,15 +175,15 @@ def _gpu_arm(args):
     cache_bytes = wl.num_blocks * 2 * 16 * H * rb
     replicas = max(2, -(-2 * L2_BYTES // cache_bytes))
     caches, host, t = _decode_setup(torch, kv, wl, dev, replicas)
-    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, wl.segment_len)
+    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, args.segment_len)
     nseg = -(-wl.max_seq_len // seg)
-    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(wl.query.shape[0], Hq, d, len(wl.seq_lens),
-                                                                 wl.max_seq_len, seg)), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(Hq, H, d, len(wl.seq_lens), wl.max_seq_len, seg)),
+                     dtype=torch.uint8, device=dev)
     out = torch.empty((wl.query.shape[0], Hq, d), dtype=wl.query.dtype, device=dev)
     kv_bytes = int(wl.seq_lens.sum()) * 2 * H * rb
     qo_bytes = 2 * wl.query.numel() * wl.query.element_size()
     attn_bytes = kv_bytes + qo_bytes
-    launches_per_step = 1 + 1 + (1 if nseg > 1 else 0)
+    launches_per_step = 1 + 3   # write; query rotation, segment walker, combine
 
     def write(i):
         kv.kv_int4_write(t["k"], t["v"], t["slots"], t["signs"], caches[i % replicas])
@@ -344,7 +344,7 @@ def _write_bench(torch, kv, workloads, dev, stream, args):
 
 # ------------------------------------------------------------------------------- CPU oracle
 
-def _attention_only(torch, kv, wl, dev, reps, rows=None):
+def _attention_only(torch, kv, wl, dev, reps, rows=None, segment_len=0):
     """Write every token of ``wl`` (untimed), then time ``reps`` back-to-back attention calls
     (captured in one CUDA graph) over the whole batch.  Returns ms per call."""
     H, d = wl.num_kv_heads, wl.head_size
@@ -358,8 +358,8 @@ def _attention_only(torch, kv, wl, dev, reps, rows=None):
     q = wl.query.to(dev)
     tables, lens = torch.from_numpy(wl.block_tables).to(dev), torch.from_numpy(wl.seq_lens).to(dev)
     qsl = torch.from_numpy(wl.query_start_loc).to(dev)
-    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, wl.segment_len)
-    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(q.shape[0], wl.num_q_heads, d, len(wl.seq_lens),
+    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, segment_len)
+    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(wl.num_q_heads, H, d, len(wl.seq_lens),
                                                                  wl.max_seq_len, seg)), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
 
@@ -493,6 +493,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--segment-len", type=int, default=0,
+                    help="split-KV segment length in tokens (multiple of 16); 0 = the library's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra", action="store_true",
                     help="also time the long-context and mixed prefill+decode workloads (attention call only)")

@@ -101,16 +101,20 @@ kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, 
 
 /*
  * Bytes of workspace kv_int4_paged_attention needs for these sizes (same arguments as the
- * attention call; segment_len 0 = the library's choice).  Returns 0 when the arguments are invalid
- * or no workspace is needed.
+ * attention call; segment_len 0 = the library's choice).  It holds each sequence's first
+ * segment index and, per split-KV segment (at most num_seqs * ceil(max_seq_len / segment_len) of
+ * them), eight warps' partial outputs (head_size * 32 bytes each, twice that when
+ * num_q_heads = 8 * num_kv_heads) and (max, sum) pairs.  Returns 0 when the arguments are invalid
+ * or num_seqs is 0.
  */
-size_t kv_int4_attention_workspace_bytes(int64_t num_q_tokens, int32_t num_q_heads,
-                                         int32_t head_size, int32_t num_seqs, int32_t max_seq_len,
-                                         int32_t segment_len);
+size_t kv_int4_attention_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                         int32_t num_seqs, int32_t max_seq_len, int32_t segment_len);
 
 /*
  * The KV-token length of one split-KV segment that kv_int4_paged_attention uses for these sizes
- * (segment_len 0 = the library's choice; otherwise segment_len itself).  0 if invalid.
+ * (segment_len 0 = the library's choice, about eight segments per resident CTA over
+ * num_seqs * max_seq_len tokens, a multiple of 32 in 32..4096; otherwise segment_len itself).
+ * 0 if invalid.
  */
 int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len);
 
@@ -126,21 +130,27 @@ int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int
  * Computation: Q is rotated once (q' = R q); scores are dot products of q' with the raw codes
  * in the rotated domain, the zero-point is subtracted from the codes and the scale s' applied per
  * key; an online softmax accumulates P V in the rotated domain and the result is un-rotated
- * (out = R^T o).  Sequences with one query token take the decode kernel, which splits long
- * contexts into segments of segment_len tokens and combines the per-segment partials; sequences
- * with more than one query token take the chunked-prefill kernel.
+ * (out = R^T o).  Sequences with one query token take the decode path: their contexts are cut
+ * into segments of segment_len tokens (segment k of a sequence holds its tokens
+ * [k segment_len, (k+1) segment_len)), a grid of about two CTAs per SM walks the batch's segments
+ * in runs balanced by cache blocks, each segment writes a (max, sum, output) partial, and a
+ * combine step merges each sequence's partials in segment order.  A segment's arithmetic does not
+ * depend on the rest of the batch, so for a fixed segment_len a sequence's output is the same
+ * alone or in any batch.  Sequences with more than one query token take the chunked-prefill
+ * kernel.
  *
  * q                [num_q_tokens, num_q_heads, head_size], q_dtype F16 or BF16, 16-B aligned.
  * cache            as written by kv_int4_write.
  * block_tables     [num_seqs, max_blocks_per_seq] int32.
  * seq_lens         [num_seqs] int32; query_start_loc [num_seqs + 1] int32 (cumulative).
  * max_query_len    host int: max over b of q_len_b (1 for a pure decode batch).
- * max_seq_len      host int: >= max over b of seq_lens[b]; sizes the segment grid.
+ * max_seq_len      host int: >= max over b of seq_lens[b]; sizes the workspace.  Longer decode
+ *                  contexts are clamped to it (and counted as bad metadata).
  * rht_signs        the vector passed to kv_int4_write.
  * segment_len      KV tokens per split-KV segment, a multiple of 16; 0 = library's choice.
  * out              [num_q_tokens, num_q_heads, head_size], out_dtype F16, BF16 or F32.
- * workspace        >= kv_int4_attention_workspace_bytes(...) bytes, 16-B aligned; may be NULL
- *                  when that size is 0.  Overlapping calls must not share a workspace.
+ * workspace        >= kv_int4_attention_workspace_bytes(...) bytes, 16-B aligned.  Overlapping
+ *                  calls must not share a workspace.
  * Supported: head_size in {64, 128}; block_size 16; num_kv_heads in {1, 2, 4, 8};
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}.  An empty context (seq_len 0) yields zeros.
  */
@@ -164,7 +174,7 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
  * that hands all free device memory to its KV cache at start-up and keeps no allocator on the
  * decode path, a plugin host that forbids device allocation after initialisation, or a decode loop
  * that cannot afford cudaMalloc's implicit device-wide synchronisation.  This variant takes the
- * same arguments minus the workspace and keeps the split-KV partials in a fixed scratch array of
+ * same arguments minus the workspace and keeps its workspace in a fixed scratch array of
  * KV_INT4_NOALLOC_SCRATCH_BYTES bytes that lives in the library's own device memory (allocated
  * when the library is loaded, held by every GPU that loads it until the process exits).  It calls
  * no cudaMalloc, cudaFree or allocating library routine.

@@ -42,7 +42,7 @@ def _load():
     lib.kv_int4_status_string.restype = ctypes.c_char_p
     lib.kv_int4_write.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, vp, vp, i64, i32, vp]
     lib.kv_int4_write.restype = ctypes.c_int
-    lib.kv_int4_attention_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.kv_int4_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.kv_int4_attention_workspace_bytes.restype = szt
     lib.kv_int4_attention_segment_len.argtypes = [i32, i32, i32]
     lib.kv_int4_attention_segment_len.restype = i32
@@ -125,9 +125,9 @@ def kv_int4_attention_segment_len(num_seqs: int, max_seq_len: int, segment_len: 
     return int(load().kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len))
 
 
-def kv_int4_attention_workspace_bytes(num_q_tokens: int, num_q_heads: int, head_size: int, num_seqs: int,
+def kv_int4_attention_workspace_bytes(num_q_heads: int, num_kv_heads: int, head_size: int, num_seqs: int,
                                       max_seq_len: int, segment_len: int = 0) -> int:
-    return int(load().kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
+    return int(load().kv_int4_attention_workspace_bytes(num_q_heads, num_kv_heads, head_size, num_seqs,
                                                       max_seq_len, segment_len))
 
 
@@ -154,7 +154,7 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
     _cuda(out, "out", tuple(_DTYPES))
     if out.shape != query.shape:
         raise ValueError("out must have the query's shape")
-    need = kv_int4_attention_workspace_bytes(Nq, Hq, d, S, max_seq_len, segment_len)
+    need = kv_int4_attention_workspace_bytes(Hq, H, d, S, max_seq_len, segment_len)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None

@@ -2,6 +2,7 @@
 // counters, the split-KV segment policy, and kernel launches on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -125,28 +126,68 @@ kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, 
 int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
     if (num_seqs < 0 || max_seq_len < 0 || segment_len < 0) return 0;
     if (segment_len > 0) return (segment_len % kBlockSize == 0) ? segment_len : 0;
-    // Enough (sequence, segment) CTAs for about four per SM of grid (two resident per SM, and
-    // sequences shorter than max_seq_len leave some of the grid idle), in multiples of 256 tokens.
-    const int64_t target = 4ll * num_sms();
+    // About eight segments per walker CTA (two per SM) over the largest batch these sizes allow, so
+    // that the block-balanced split stays even when contexts are shorter than max_seq_len; a
+    // multiple of 32 tokens (whole block pairs), 32..4096.
+    const int64_t ctas = 2ll * num_sms();
     const int64_t work = (int64_t)num_seqs * (int64_t)max_seq_len;
-    int64_t seg = (work + target - 1) / (target > 0 ? target : 1);
-    seg = ((seg + 255) / 256) * 256;
-    if (seg < 256) seg = 256;
-    if (seg > (1 << 20)) seg = 1 << 20;
+    int64_t seg = (work + 8 * ctas - 1) / (8 * ctas);
+    seg = ((seg + 31) / 32) * 32;
+    if (seg < 32) seg = 32;
+    if (seg > 4096) seg = 4096;
     return (int32_t)seg;
 }
 
-size_t kv_int4_attention_workspace_bytes(int64_t num_q_tokens, int32_t num_q_heads, int32_t head_size,
+}  // extern "C"
+
+namespace {
+
+// Workspace of the decode path, in 256-byte-aligned regions:
+//   meta  [num_seqs + 1] int32             first unit of each sequence
+//   cnt   [num_seqs, H] int32              combine chunks finished
+//   po    [units, 8, po_floats]            unnormalised partial outputs
+//   pml   [units, 8, 16] fp32              partial (max, sum) per column
+//   cp    [num_seqs, H, chunks, cp_floats] combine chunk partials
+// units <= num_seqs * ceil(max_seq_len / segment_len); a (sequence, kv head) has at most
+// chunks = ceil(ceil(max_seq_len / segment_len) * (8 / H) / 8) combine chunks.
+struct WsLayout {
+    size_t meta, cnt, po, pml, cp, total;
+    int64_t chunks;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool ws_layout(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int32_t num_seqs, int32_t max_seq_len,
+               int32_t seg, WsLayout* w) {
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_size <= 0 || seg <= 0)
+        return false;
+    const int G = num_q_heads / num_kv_heads;
+    const int64_t seg_per_seq = ((int64_t)max_seq_len + seg - 1) / seg;
+    const int64_t max_units = (int64_t)num_seqs * seg_per_seq;
+    const int64_t recs = seg_per_seq * (8 / num_kv_heads);
+    w->chunks = recs > 0 ? (recs + kDecodeChunkRecords - 1) / kDecodeChunkRecords : 1;
+    w->meta = 0;
+    w->cnt = align256((size_t)(num_seqs + 1) * 4);
+    w->po = w->cnt + align256((size_t)num_seqs * num_kv_heads * 4);
+    w->pml = w->po + align256((size_t)max_units * 8 * decode_po_floats(head_size, G) * 4);
+    w->cp = w->pml + align256((size_t)max_units * 8 * 16 * 4);
+    const size_t cp_bytes =
+        w->chunks > 1 ? (size_t)num_seqs * num_kv_heads * w->chunks * decode_cp_floats(head_size, G) * 4 : 0;
+    w->total = w->cp + cp_bytes;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kv_int4_attention_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
                                          int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
-    if (num_q_tokens < 0 || num_q_heads <= 0 || head_size <= 0 || num_seqs < 0 || max_seq_len < 0) return 0;
+    if (num_seqs <= 0 || max_seq_len < 0) return 0;
     const int32_t seg = kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len);
-    if (seg <= 0) return 0;
-    const int64_t nseg = ((int64_t)max_seq_len + seg - 1) / seg;
-    if (nseg <= 1) return 0;
-    // partial outputs [num_seqs, Hq, nseg, D] then (max, sum) pairs [num_seqs, Hq, nseg, 2]
-    const int64_t units = (int64_t)num_seqs * num_q_heads * nseg;
-    const size_t o_bytes = (size_t)units * head_size * 4;
-    return ((o_bytes + 255) & ~(size_t)255) + (size_t)units * 2 * 4;
+    WsLayout w;
+    if (!ws_layout(num_q_heads, num_kv_heads, head_size, num_seqs, max_seq_len, seg, &w)) return 0;
+    return w.total;
 }
 
 kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
@@ -178,12 +219,13 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
 
     const int32_t seg = kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len);
     if (seg <= 0) return KV_INT4_EINVAL;
-    const int64_t nseg = max_seq_len > 0 ? ((int64_t)max_seq_len + seg - 1) / seg : 1;
-    if (nseg > 65535ll * 1024) return KV_INT4_EUNSUPPORTED;
-    const size_t need = kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
-                                                          max_seq_len, segment_len);
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KV_INT4_EWORKSPACE;
-    if (need > 0 && !aligned16(workspace)) return KV_INT4_EALIGN;
+    const int64_t len_cap = std::min<int64_t>(max_seq_len, (int64_t)max_blocks_per_seq * kBlockSize);
+    const int64_t max_blocks_total = (int64_t)num_seqs * ((len_cap + kBlockSize - 1) / kBlockSize);
+    if (max_blocks_total >= ((int64_t)1 << 31)) return KV_INT4_EUNSUPPORTED;   // 32-bit block positions
+    WsLayout w;
+    if (!ws_layout(num_q_heads, num_kv_heads, head_size, num_seqs, max_seq_len, seg, &w)) return KV_INT4_EINVAL;
+    if (workspace == nullptr || workspace_bytes < w.total) return KV_INT4_EWORKSPACE;
+    if (!aligned16(workspace)) return KV_INT4_EALIGN;
 
     AttnParams p;
     p.q = q;
@@ -193,11 +235,17 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     p.qsl = query_start_loc;
     p.signs = rht_signs;
     p.out = out;
-    const int64_t units = (int64_t)num_seqs * num_q_heads * nseg;
-    p.ws_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
-    p.ws_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                  (((size_t)units * head_size * 4 + 255) & ~(size_t)255))
-                       : nullptr;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.ws_meta = reinterpret_cast<int32_t*>(ws + w.meta);
+    p.ws_cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
+    p.ws_po = reinterpret_cast<float*>(ws + w.po);
+    p.ws_pml = reinterpret_cast<float*>(ws + w.pml);
+    p.ws_cp = reinterpret_cast<float*>(ws + w.cp);
+    p.combine_chunks = (int)w.chunks;
+    p.seg_rcp = div_rcp((uint32_t)seg);
+    p.segb_rcp = div_rcp((uint32_t)(seg / kBlockSize));
+    p.wph_shift = num_kv_heads == 8 ? 0 : num_kv_heads == 4 ? 1 : num_kv_heads == 2 ? 2 : 3;
+    if ((int64_t)num_seqs * num_kv_heads * w.chunks >= ((int64_t)1 << 31)) return KV_INT4_EUNSUPPORTED;
     p.status = status_ptr();
     p.num_blocks = num_blocks;
     p.num_q_tokens = num_q_tokens;
@@ -208,15 +256,16 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     p.Hq = num_q_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.seg_len = seg;
-    p.nseg_max = (int)nseg;
+    p.len_cap = (int)len_cap;
     p.softmax_scale = softmax_scale;
     p.c = (float)(1.0 / std::sqrt((double)head_size));
 
+    const int64_t max_units = (int64_t)num_seqs * (((int64_t)max_seq_len + seg - 1) / seg);
+    const int ctas = decode_grid_size(max_blocks_total, max_units);
     const DType qd = q_dtype == KV_INT4_BF16 ? DType::BF16 : DType::F16;
     const DType od = out_dtype == KV_INT4_BF16 ? DType::BF16 : (out_dtype == KV_INT4_F16 ? DType::F16 : DType::F32);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode(p, head_size, qd, od, s);
-    if (e == cudaSuccess && nseg > 1) e = launch_combine(p, head_size, od, s);
+    cudaError_t e = launch_decode(p, head_size, ctas, qd, od, s);
     if (e == cudaSuccess && max_query_len > 1) e = launch_prefill(p, head_size, max_query_len, qd, od, s);
     return from_cuda(e);
 }

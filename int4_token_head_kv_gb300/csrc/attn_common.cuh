@@ -110,22 +110,12 @@ __device__ __forceinline__ float rotate_query(const void* q, int64_t qoff, const
     return c * exp2i(-e) * softmax_scale * kLog2e;
 }
 
-// The same rotation for up to NB vectors of one warp at a time (vector k is query row rows[k]; a
-// negative row means no vector).  All loads are issued first and the butterfly stages of the NB
-// vectors interleave, so the warp pays one chain of shuffle latencies instead of NB.
-// Row r of q is at element offset r * D; its results go to qh/ql + slot[k] * D and alpha[slot[k]].
-template <int D, typename QT, int NB>
-__device__ __forceinline__ void rotate_queries(const void* q, const int64_t (&rows)[NB], const int (&slot)[NB],
-                                               const float* sgn, __half* qh, __half* ql, float* alpha, float c,
-                                               float softmax_scale) {
+// Walsh-Hadamard transform of NB vectors of one warp at once (vector k: lane l holds
+// x[k][j] = v_k[l + 32 j]).  The butterfly stages of the NB vectors interleave, so the warp pays
+// one chain of shuffle latencies instead of NB.
+template <int D, int NB>
+__device__ __forceinline__ void warp_fwht_batch(float (&x)[NB][D / 32]) {
     const int lane = threadIdx.x & 31;
-    float x[NB][D / 32];
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j)
-            x[k][j] = rows[k] >= 0 ? load_elem<QT>(q, rows[k] * D + lane + 32 * j) * sgn[lane + 32 * j] : 0.0f;
-    }
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -149,73 +139,6 @@ __device__ __forceinline__ void rotate_queries(const void* q, const int64_t (&ro
                 x[k][j + h] = a - b;
             }
         }
-    }
-    float m[NB];
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-        m[k] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) m[k] = fmaxf(m[k], fabsf(x[k][j]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int k = 0; k < NB; ++k) m[k] = fmaxf(m[k], __shfl_xor_sync(0xffffffffu, m[k], o));
-    }
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-        if (rows[k] < 0) continue;
-        const int e = prescale_exponent(m[k]);
-        const float sc = exp2i(e);
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
-            const float y = x[k][j] * sc;
-            const __half hi = __float2half_rn(y);
-            qh[slot[k] * D + lane + 32 * j] = hi;
-            ql[slot[k] * D + lane + 32 * j] = __float2half_rn(y - __half2float(hi));
-        }
-        if (lane == 0) alpha[slot[k]] = c * exp2i(-e) * softmax_scale * kLog2e;
-    }
-}
-
-// Un-rotate and store up to NB output vectors of one warp at a time (vector k: lane holds
-// x[k][j] = o[lane + 32 j]; stored at out + ooff[k] when ooff[k] >= 0), butterflies interleaved.
-template <int D, typename OT, int NB>
-__device__ __forceinline__ void unrotate_store_batch(float (&x)[NB][D / 32], const float (&inv_l)[NB], const float* sgn,
-                                                     float c, void* out, const int64_t (&ooff)[NB]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) x[k][j] *= inv_l[k];
-    }
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int k = 0; k < NB; ++k) {
-#pragma unroll
-            for (int j = 0; j < D / 32; ++j) {
-                const float o = __shfl_xor_sync(0xffffffffu, x[k][j], h);
-                x[k][j] = (lane & h) ? (o - x[k][j]) : (x[k][j] + o);
-            }
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-#pragma unroll
-        for (int h = 1; h < D / 32; h <<= 1) {
-#pragma unroll
-            for (int j = 0; j < D / 32; ++j) {
-                if (j & h) continue;
-                const float a = x[k][j], b = x[k][j + h];
-                x[k][j] = a + b;
-                x[k][j + h] = a - b;
-            }
-        }
-        if (ooff[k] < 0) continue;
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j)
-            store_elem<OT>(out, ooff[k] + lane + 32 * j, x[k][j] * c * sgn[lane + 32 * j]);
     }
 }
 

@@ -1,4 +1,4 @@
-// Decode attention over the INT4 cache (one query token per sequence), with split-KV segments.
+// Decode attention over the INT4 cache (one query token per sequence), as split-KV segments.
 //
 // Method ("[Feature] Triton INT4 / INT2 per-token-head KV cache quantization", description of the
 // packed read path): Q is rotated with the same random Hadamard transform as K and V, scores are
@@ -8,20 +8,32 @@
 // (max, sum, accumulator) partials are combined afterwards ("3D" segment reduction of the
 // unified-attention interface, test_triton_unified_attention_per_token_head_scale).
 //
-// GB300 design:
-//  * One CTA per (sequence, segment) covers ALL kv heads, so each 16-token block is one
-//    contiguous 16-byte-aligned region (K plane then V plane, 2 * 16 * H * (D/2+4) bytes) that is
-//    streamed into a 4-stage shared-memory ring with 1-D bulk async copies (cp.async.bulk +
-//    mbarrier transaction counts, L2 evict-first).  There is no producer warp: the segment's block
-//    ids are staged in shared memory up front, four lanes issue the first four copies, and the
-//    last consumer warp to finish with a stage issues its next block.
-//  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block when H < 8).
-//    Scores S^T[16 tokens x 8 heads] = (K - zp)[16 x D] . Q'^T come from mma.sync m16n8k16 on
+// GB300 design, two launches per call:
+//  1. decode_kernel walks split-KV units.  Unit sigma of sequence b is its KV tokens
+//     [sigma S, (sigma + 1) S), S = seg_len.  A fixed grid of about two CTAs per SM takes
+//     contiguous runs of units, balanced by cache blocks (CTA c owns the units whose first block
+//     falls in [c T / n, (c + 1) T / n) of the batch's T decode blocks), and every unit writes
+//     its own (max, sum, unnormalised output) partial.  A unit's arithmetic does not depend on
+//     the CTA that runs it, so a sequence's output does not depend on the rest of the batch.
+//  2. combine_kernel merges the units of each sequence in a fixed order and un-rotates.
+//
+// Walker CTA:
+//  * All kv heads of a 16-token block are one contiguous, 16-byte-aligned region (K plane then V
+//    plane, 2 * 16 * H * (D/2+4) bytes) streamed through a 4-stage shared-memory ring by 1-D bulk
+//    async copies (cp.async.bulk + mbarrier transaction counts, L2 evict-first).  The ring runs
+//    across unit boundaries.  There is no producer warp: the CTA's block ids are staged in shared
+//    memory up front, four lanes issue the first four copies, and the last consumer warp to
+//    finish with a stage issues its next block.  The raw query rows of each run of units of one
+//    sequence arrive the same way (double-buffered), and each warp rotates the query vectors of
+//    its kv head itself (H_d D q in fp32, then fp16 high + low halves laid out as mma fragments
+//    through a small per-warp shared-memory scratch).
+//  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block pair when H < 8).
+//    Scores S^T[16 tokens x 8 columns] = (K - zp)[16 x D] . Q'^T come from mma.sync m16n8k16 on
 //    fp16 operands built straight from the packed bytes (codes and code - zp are exact in fp16);
-//    the zero-point is subtracted while unpacking, which is the sum(Q) * zp correction folded in.
+//    subtracting the zero-point while unpacking is the sum(Q) * zp correction folded in.
 //  * P^T is transposed in registers (movmatrix) into the B operand of O^T[D x 8] += (V - zp)^T P^T.
-//    V's per-key scale is folded into P (w = p * s'_V * 2^-E, E a running max exponent, so the fp16
-//    weights never overflow).
+//    V's per-key scale is folded into P (w = p * s'_V * 2^-E, E a running max exponent, so the
+//    fp16 weights never overflow); w and Q' are carried as fp16 high + low halves.
 #include "attn_common.cuh"
 
 namespace kvi4 {
@@ -29,216 +41,514 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = kConsumerWarps * 32;   // no producer warp: see the refill rule below
-constexpr int kStages = 4;
-constexpr int kTableWin = 512;   // block-table entries of a CTA's segment staged in shared memory
+constexpr int kMaxStages = 8;                         // ring slots the state area has room for
+constexpr int kMaxUnits = kDecodeMaxUnits;            // units per CTA (the host sizes the grid so)
+constexpr int kTableWin = 256;                        // block ids of a CTA staged in shared memory
+constexpr uint32_t kSmemPerSm = 233472;               // 228 KB of shared memory per SM
+constexpr uint32_t kSmemPerCtaReserved = 1024;
+
+constexpr int kMaxHead = 128;
+
+// Ring depth and rows of a warp's query scratch.  With up to 4 query heads per kv head the
+// high and low halves pass through 4 rows one after the other, which leaves room for a fifth
+// ring stage at two CTAs per SM; 8 heads per kv head need 8 rows and keep 4 stages.
+template <bool WIDE>
+struct WalkerShape {
+    static constexpr int kStages = WIDE ? 4 : 5;
+    static constexpr int kScrRows = WIDE ? 8 : 4;
+};
 
 struct DecodeSmem {
     uint32_t stage_bytes;   // one block (K + V planes)
-    uint32_t state_off;     // start of barriers etc. (after the ring / epilogue state overlay)
+    uint32_t qraw_bytes;    // one sequence's query rows (Hq x D, 16-bit)
+    uint32_t nq;            // query buffers (2 when two CTAs still fit an SM, else 1)
+    uint32_t q_off;
+    uint32_t scr_off;       // per-warp scratch: scratch rows x (D + 8) halves
+    uint32_t state_off;     // barriers, counters, unit list, block-table window
     uint32_t total;
 };
 
-template <int D>
+constexpr uint32_t kStateBytes = kMaxStages * 8u + 2u * 8u    // ring and query barriers
+                                 + kConsumerWarps * 8u        // scan scratch
+                                 + (kMaxStages + 4u + kMaxStages + 4u + 8u) * 4u   // valid, flags, refill counters, info
+                                 + kMaxUnits * 16u            // units
+                                 + 3u * kMaxUnits * 4u        // unit start blocks, run starts, run query rows
+                                 + kTableWin * 4u             // block-table window
+                                 + kMaxHead * 4u;             // signs
+
+template <int D, bool WIDE>
 __host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
+    using Sh = WalkerShape<WIDE>;
     DecodeSmem s;
     s.stage_bytes = 2u * kBlockSize * (uint32_t)H * Geo<D>::RB;
-    const uint32_t ring = kStages * s.stage_bytes;
-    const uint32_t state = kConsumerWarps * 8u * D * 4u;
-    s.state_off = ((ring > state ? ring : state) + 127u) & ~127u;
-    const uint32_t tail = 2u * kStages * 8u      // full / empty barriers
-                          + kStages * 4u + 16u     // valid flags, abort flag
-                          + kStages * 4u + 16u     // refill counters
-                          + kTableWin * 4u         // block-table window
-                          + D * 4u                 // signs
-                          + (uint32_t)Hq * 4u      // alpha
-                          + 2u * kConsumerWarps * 8u * 4u  // per-warp (m, l)
-                          + 2u * (uint32_t)Hq * D * 2u;  // rotated queries, fp16 hi and lo halves
-    s.total = s.state_off + ((tail + 127u) & ~127u);
+    s.qraw_bytes = (uint32_t)Hq * D * 2u;
+    s.q_off = (Sh::kStages * s.stage_bytes + 127u) & ~127u;
+    s.nq = 2;
+    for (;;) {
+        s.scr_off = (s.q_off + s.nq * s.qraw_bytes + 127u) & ~127u;
+        s.state_off = (s.scr_off + kConsumerWarps * Sh::kScrRows * (D + 8) * 2u + 127u) & ~127u;
+        s.total = s.state_off + ((kStateBytes + 127u) & ~127u);
+        if (s.nq == 1 || 2u * (s.total + kSmemPerCtaReserved) <= kSmemPerSm) break;
+        s.nq = 1;
+    }
     return s;
 }
 
-template <int D, bool WIDE, typename QT, typename OT>
+// Exclusive prefix sum over the CTA's 256 threads (all threads must call it); *total gets the sum.
+__device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long long v, unsigned long long* wsum,
+                                                                   unsigned long long* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    unsigned long long before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+        const unsigned long long s = wsum[w];
+        before += (w < warp) ? s : 0ull;
+        all += s;
+    }
+    __syncthreads();
+    *total = all;
+    return before + x - v;
+}
+
+__device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// ------------------------------------------------------------------ 1. split-KV unit walker
+
+template <int D, bool WIDE, typename QT>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ AttnParams p) {
     using Gm = Geo<D>;
+    constexpr int NB = WIDE ? 8 : 4;      // query vectors a warp rotates (its kv head's group)
+    constexpr int NLS = WIDE ? 32 : 16;
+    constexpr int SR = D + 8;             // scratch row stride (halves), staggers banks
+    constexpr int kStages = WalkerShape<WIDE>::kStages;
+    constexpr int kScrRows = WalkerShape<WIDE>::kScrRows;
+    constexpr uint32_t PO = decode_po_floats(D, WIDE ? 8 : 1);
     extern __shared__ __align__(128) uint8_t smem[];
-    const int seg = blockIdx.x, seq = blockIdx.y;
-    const int q0 = __ldg(p.qsl + seq);
-    if (__ldg(p.qsl + seq + 1) - q0 != 1) return;   // not a decode sequence
-    if (q0 < 0 || (int64_t)q0 >= p.num_q_tokens) {
-        if (seg == 0 && threadIdx.x == 0) count_status(p.status, 2);
-        return;
-    }
-    const int H = p.H, G = p.G, Hq = p.Hq;
+    const int H = p.H, G = p.G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int L = __ldg(p.seq_lens + seq);
-    const int Lmax = min(p.max_blocks_per_seq * kBlockSize, p.nseg_max * p.seg_len);
-    if (L > Lmax) {   // longer than its block table or than the max_seq_len the grid was sized for
-        if (seg == 0 && threadIdx.x == 0) count_status(p.status, 2);
-        L = Lmax;
-    }
-    if (L <= 0) {   // empty context: zero output
-        if (seg == 0) {
-            for (int i = threadIdx.x; i < Hq * D; i += blockDim.x) store_elem<OT>(p.out, (int64_t)q0 * Hq * D + i, 0.0f);
-        }
-        return;
-    }
-    const int S = p.seg_len;
-    const int tok_begin = seg * S;
-    if (tok_begin >= L) return;
-    const int tok_end = min(L, tok_begin + S);
-    const int nseg = (L + S - 1) / S;
-    const int blk_first = tok_begin / kBlockSize;
-    const int nblk = (tok_end + kBlockSize - 1) / kBlockSize - blk_first;
 
-    const DecodeSmem lay = decode_smem_layout<D>(H, Hq);
+    const DecodeSmem lay = decode_smem_layout<D, WIDE>(H, p.Hq);
+    const int nq = (int)lay.nq;
     uint8_t* ring = smem;
+    uint8_t* qbuf = smem + lay.q_off;
+    __half* qscr = reinterpret_cast<__half*>(smem + lay.scr_off) + warp * kScrRows * SR;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.state_off);
-    int* valid = reinterpret_cast<int*>(full + 2 * kStages);
-    int* abort_flag = valid + kStages;
-    int* released = abort_flag + 4;    // per stage: consumer warps done with its current block
-    int* tbl = released + kStages + 4;    // block ids of this segment's first kTableWin blocks
+    uint64_t* qfull = full + kMaxStages;
+    unsigned long long* wsum = reinterpret_cast<unsigned long long*>(qfull + 2);
+    int* valid = reinterpret_cast<int*>(wsum + kConsumerWarps);
+    int* flags = valid + kMaxStages;   // [0] a wait gave up, [1] blocks issued, [2] query rows issued
+    int* released = flags + 4;         // per stage: consumer warps done with its current block
+    int* qreleased = released + kMaxStages;   // per query buffer: consumer warps done reading it
+    int* info = qreleased + 4;
+    int4* units = reinterpret_cast<int4*>(info + 8);     // (seq, first block in seq, global unit, tokens)
+    int* ustart = reinterpret_cast<int*>(units + kMaxUnits);   // first block, in the batch's block order
+    int* run_first = ustart + kMaxUnits;                 // first unit of each run of one sequence
+    int* run_q0 = run_first + kMaxUnits;                 // that sequence's query row
+    int* tbl = run_q0 + kMaxUnits;                       // block ids of the CTA's first kTableWin blocks
     float* sgn = reinterpret_cast<float*>(tbl + kTableWin);
-    float* alpha = sgn + D;
-    float* st_m = alpha + Hq;
-    float* st_l = st_m + kConsumerWarps * 8;
-    __half* qh = reinterpret_cast<__half*>(st_l + kConsumerWarps * 8);
-    __half* ql = qh + Hq * D;
-    float* st_o = reinterpret_cast<float*>(smem);   // epilogue overlay of the ring
 
+    // Launched as a programmatic dependent (of the cache write, typically): everything up to
+    // griddep_wait() below reads only the host-provided metadata (query_start_loc, seq_lens, block
+    // tables, signs) and writes only shared memory.  The combine may be scheduled right away: it
+    // waits for this grid before reading anything, and its CTAs become resident as walker CTAs
+    // retire.
+    griddep_launch_dependents();
+    const float sg_in = threadIdx.x < D ? __ldg(p.signs + threadIdx.x) : 0.0f;   // consumed below
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             released[s] = 0;
         }
-        abort_flag[0] = 0;
-        abort_flag[1] = 0;   // blocks issued so far
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qfull[s], 1);
+            qreleased[s] = 0;
+        }
+        for (int s = 0; s < 4; ++s) flags[s] = 0;
         fence_mbar_init();
     }
-    const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + blk_first;
-    // one coalesced load of the segment's block ids, so that no ring refill waits on global memory
-    for (int i = threadIdx.x; i < min(nblk, kTableWin); i += blockDim.x) tbl[i] = __ldg(table + i);
-    for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
+
+    // ---- the batch's decode units: each thread scans a contiguous slice of the sequences
+    const int N = p.num_seqs, S = p.seg_len, SB = S / kBlockSize;
+    const int per = (N + kDecodeThreads - 1) / kDecodeThreads;
+    const int b0 = min(N, (int)threadIdx.x * per), b1 = min(N, b0 + per);
+    // (decode context length or 0, query row) of sequence b from its metadata
+    auto decode_of = [&](int q0, int q1, int L, bool count) -> int2 {
+        if (q1 - q0 != 1) return make_int2(0, 0);
+        if (q0 < 0 || (int64_t)q0 >= p.num_q_tokens) {
+            if (count) count_status(p.status, 2);
+            return make_int2(0, 0);
+        }
+        if (L > p.len_cap) {   // longer than max_seq_len or than its block table
+            if (count) count_status(p.status, 2);
+            L = p.len_cap;
+        }
+        return make_int2(max(L, 0), q0);
+    };
+    // Stage (L, q0) of every sequence in shared memory (the ring is idle until the first copy).
+    // Thread t's i-th sequence t * per + i sits at entry i * 256 + t, so the passes below read
+    // consecutive words across a warp; a batch too large for it reads global memory per pass.
+    int2* meta = reinterpret_cast<int2*>(smem);
+    const bool staged = (uint32_t)per * kDecodeThreads * 8u <= lay.state_off;
+    if (staged) {
+        for (int i0 = 0; i0 < per; i0 += 4) {
+            int q0[4], q1[4], L[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int b = min(b0 + i0 + k, N - 1);
+                q0[k] = __ldg(p.qsl + b);
+                q1[k] = __ldg(p.qsl + b + 1);
+                L[k] = __ldg(p.seq_lens + b);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (b0 + i0 + k < b1)
+                    meta[(i0 + k) * kDecodeThreads + threadIdx.x] = decode_of(q0[k], q1[k], L[k], blockIdx.x == 0);
+            }
+        }
+    }
+    if (threadIdx.x < D) sgn[threadIdx.x] = sg_in < 0.0f ? -1.0f : 1.0f;
+    __syncthreads();
+    // (L, q0) of this thread's i-th sequence, and of any sequence b
+    auto own_info = [&](int i, bool count) -> int2 {
+        if (staged) return meta[i * kDecodeThreads + threadIdx.x];
+        const int b = b0 + i;
+        return decode_of(__ldg(p.qsl + b), __ldg(p.qsl + b + 1), __ldg(p.seq_lens + b), count);
+    };
+    auto seq_info = [&](int b) -> int2 {
+        if (staged) return meta[(b % per) * kDecodeThreads + b / per];
+        return decode_of(__ldg(p.qsl + b), __ldg(p.qsl + b + 1), __ldg(p.seq_lens + b), false);
+    };
+    uint32_t my_units = 0, my_blocks = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int L = own_info(b - b0, blockIdx.x == 0).x;
+        my_units += fast_div((uint32_t)(L + S - 1), (uint32_t)S, p.seg_rcp);
+        my_blocks += (uint32_t)((L + kBlockSize - 1) / kBlockSize);
+    }
+    unsigned long long tot;
+    const unsigned long long pre =
+        block_exclusive_scan(((unsigned long long)my_blocks << 32) | my_units, wsum, &tot);
+    const uint32_t U = (uint32_t)tot, T = (uint32_t)(tot >> 32);
+    const uint32_t ub_t = (uint32_t)pre, bb_t = (uint32_t)(pre >> 32);
+
+    // This CTA's share of the batch's blocks, [f(c), f(c+1)) with f(c) = c T / n in fp32: any
+    // monotone f with f(0) = 0 and f(n) = T splits the blocks exactly, and every CTA evaluates
+    // the shared boundary the same way.  Then the units that start inside it.
+    const float per_cta = (float)T / (float)gridDim.x;
+    auto boundary = [&](uint32_t c) -> uint32_t {
+        if (c >= gridDim.x) return T;
+        const uint32_t f = (uint32_t)((float)c * per_cta);
+        return f < T ? f : T;
+    };
+    const uint32_t A = boundary(blockIdx.x), E = boundary(blockIdx.x + 1);
+    auto units_before = [&](uint32_t X, uint32_t bb, uint32_t nseg) -> uint32_t {
+        if (X <= bb) return 0u;
+        const uint32_t k = fast_div(X - bb + SB - 1, (uint32_t)SB, p.segb_rcp);
+        return k < nseg ? k : nseg;
+    };
+    uint32_t below_a = 0, below_e = 0;
+    {
+        uint32_t bb = bb_t, ub = ub_t;
+        for (int b = b0; b < b1; ++b) {
+            const int L = own_info(b - b0, false).x;
+            const uint32_t nseg = fast_div((uint32_t)(L + S - 1), (uint32_t)S, p.seg_rcp);
+            const uint32_t nblk = (uint32_t)((L + kBlockSize - 1) / kBlockSize);
+            below_a += units_before(A, bb, nseg);
+            below_e += units_before(E, bb, nseg);
+            bb += nblk;
+            ub += nseg;
+        }
+    }
+    unsigned long long lohi;
+    block_exclusive_scan(((unsigned long long)below_e << 32) | below_a, wsum, &lohi);
+    const uint32_t u_lo = (uint32_t)lohi;
+    int nunits = (int)((uint32_t)(lohi >> 32) - u_lo);
+    if (nunits > kMaxUnits) {   // cannot happen for a grid the host sized; never overrun the list
+        if (threadIdx.x == 0) count_status(p.status, 2);
+        nunits = kMaxUnits;
+    }
+    {
+        uint32_t bb = bb_t, ub = ub_t;
+        for (int b = b0; b < b1 && ub < u_lo + (uint32_t)nunits; ++b) {
+            const int L = own_info(b - b0, false).x;
+            const int nseg = (int)fast_div((uint32_t)(L + S - 1), (uint32_t)S, p.seg_rcp);
+            const int nblk = (L + kBlockSize - 1) / kBlockSize;
+            const int64_t lo_rel = (int64_t)u_lo - ub, hi_rel = (int64_t)u_lo + nunits - ub;
+            const int64_t s_lo = lo_rel > 0 ? lo_rel : 0;
+            const int64_t s_hi = hi_rel < nseg ? hi_rel : nseg;
+            for (int64_t sg = s_lo; sg < s_hi; ++sg) {
+                const int j = (int)(ub + sg - u_lo);
+                units[j] = make_int4(b, (int)sg * SB, (int)(ub + sg), min(S, L - (int)sg * S));
+                ustart[j] = (int)(bb + sg * SB);
+            }
+            bb += (uint32_t)nblk;
+            ub += (uint32_t)nseg;
+        }
+    }
+    __syncthreads();
+    // runs of consecutive units of one sequence share a rotated-query record
+    unsigned long long nruns_ll;
+    {
+        const int j = threadIdx.x;
+        const bool first = j < nunits && (j == 0 || units[j].x != units[j - 1].x);
+        const int r = (int)block_exclusive_scan(first ? 1ull : 0ull, wsum, &nruns_ll);
+        if (first) {
+            run_first[r] = j;
+            run_q0[r] = seq_info(units[j].x).y;
+        }
+    }
+    const int nruns = (int)nruns_ll;
+    const int Bs = nunits > 0 ? ustart[0] : 0;
+    const int nb_cta = nunits > 0 ? ustart[nunits - 1] - Bs + (units[nunits - 1].w + kBlockSize - 1) / kBlockSize : 0;
+
+    // block id of the CTA's i-th block (the unit holding it, then its block table entry)
+    auto block_id = [&](int i) -> int {
+        int lo = 0, hi = nunits - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ustart[mid] - Bs <= i) lo = mid;
+            else hi = mid - 1;
+        }
+        const int4 u = units[lo];
+        return __ldg(p.block_tables + (int64_t)u.x * p.max_blocks_per_seq + u.y + (i - (ustart[lo] - Bs)));
+    };
+    for (int i = threadIdx.x; i < min(nb_cta, kTableWin); i += kDecodeThreads) tbl[i] = block_id(i);
     __syncthreads();
 
-    const uint8_t* seq_cache = p.cache;
-    const uint32_t stage_bytes = lay.stage_bytes;
+    const uint32_t stage_bytes = lay.stage_bytes, qraw_bytes = lay.qraw_bytes;
     // Ring refill rule: block i goes to stage i % kStages.  The first kStages blocks are issued up
     // front; afterwards the LAST consumer warp to finish with block i (counted in released[])
     // issues block i + kStages into the same stage, so no warp ever blocks waiting to refill.
     auto produce = [&](int i) {
         const int st = i % kStages;
-        const int blk = i < kTableWin ? tbl[i] : __ldg(table + i);
+        const int blk = i < kTableWin ? tbl[i] : block_id(i);
         const bool ok = blk >= 0 && (int64_t)blk < p.num_blocks;
         valid[st] = ok ? 1 : 0;
-        atomicMax(&abort_flag[1], i + 1);
+        atomicMax(&flags[1], i + 1);
         if (ok) {
             mbar_arrive_expect_tx(&full[st], stage_bytes);
-            bulk_copy_g2s(ring + (size_t)st * stage_bytes, seq_cache + (int64_t)blk * stage_bytes, stage_bytes, &full[st],
-                          policy_evict_first());
+            bulk_copy_g2s(ring + (size_t)st * stage_bytes, p.cache + (int64_t)blk * stage_bytes, stage_bytes,
+                          &full[st], policy_evict_first());
         } else {
             count_status(p.status, 1);
             mbar_arrive(&full[st]);
         }
     };
-    if (threadIdx.x < min(kStages, nblk)) produce(threadIdx.x);   // the first copies, one lane each
-
-    // Rotate this sequence's query (all Hq heads) into fp16 halves + per-head logit multiplier,
-    // four vectors per warp at a time.
-    for (int v0 = warp; v0 < Hq; v0 += 4 * kConsumerWarps) {
-        int64_t rows[4];
-        int slot[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int v = v0 + k * kConsumerWarps;
-            rows[k] = v < Hq ? (int64_t)q0 * Hq + v : -1;
-            slot[k] = v < Hq ? v : 0;
+    // Query rows of run r go to buffer r % nq, refilled the same way once every warp has read them.
+    auto produce_q = [&](int r) {
+        const int qs = r & (nq - 1);
+        atomicMax(&flags[2], r + 1);
+        mbar_arrive_expect_tx(&qfull[qs], qraw_bytes);
+        bulk_copy_g2s(qbuf + (size_t)qs * qraw_bytes, static_cast<const uint8_t*>(p.q) + (size_t)run_q0[r] * qraw_bytes,
+                      qraw_bytes, &qfull[qs], policy_evict_first());
+    };
+    griddep_wait();   // the cache (and the query) are produced by earlier kernels of the stream
+    if (blockIdx.x == 0) {   // the combine's sequence index and chunk counters
+        uint32_t ub = ub_t;
+        for (int b = b0; b < b1; ++b) {
+            p.ws_meta[b] = (int)ub;
+            ub += fast_div((uint32_t)(own_info(b - b0, false).x + S - 1), (uint32_t)S, p.seg_rcp);
         }
-        rotate_queries<D, QT, 4>(p.q, rows, slot, sgn, qh, ql, alpha, p.c, p.softmax_scale);
+        if (threadIdx.x == 0) p.ws_meta[N] = (int)U;
+        for (int i = threadIdx.x; i < N * H; i += kDecodeThreads) p.ws_cnt[i] = 0;
     }
-    __syncthreads();
+    if (threadIdx.x == 0) {   // the first query rows, then the first blocks
+        for (int r = 0; r < min(nq, nruns); ++r) produce_q(r);
+        for (int i = 0; i < min(kStages, nb_cta); ++i) produce(i);
+    }
 
-    // consumer state (lives across the role split so that the barriers below are uniform)
     float o[Gm::MT][4];
-#pragma unroll
-    for (int i = 0; i < Gm::MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float m0 = kNegBig, m1 = kNegBig, l0 = 0.0f, l1 = 0.0f;
-    uint32_t eref = 0;   // running max biased exponent of V scales seen so far
+    uint32_t eref = 0;   // running max biased exponent of V scales seen in the unit
     const int g = lane >> 2, t = lane & 3;
+    const int h = warp & (H - 1);
+    const int wph = 1 << p.wph_shift;
+    const int sub = warp >> (3 - p.wph_shift);
+    const int tk0 = block_token(g), tk1 = block_token(g + 8);
+    // Score columns (the mma N dimension, 8 wide).  WIDE (8 query heads per kv head): column n is
+    // head n, with a second 8-wide tile carrying the low halves.  Otherwise columns 0-3 carry the
+    // high halves of heads 0-3 and columns 4-7 their low halves, so the split costs no extra mma:
+    // lane quad t then holds heads hb, hb+1 with hb = 2 (t & 1).
+    const int hb = WIDE ? 2 * t : 2 * (t & 1);
+    const bool lo_lane = !WIDE && t >= 2;   // this lane's P columns carry low halves
+    uint32_t qb[Gm::KSTEPS][WIDE ? 4 : 2];
+    const float lsc = p.c * p.softmax_scale * kLog2e;
+    float al0 = 0.0f, al1 = 0.0f;
+    int run = -1, prev_seq = -1;
+    bool stop = false;
 
-    {
-        // ------------------------------------------------------------------ consumers
-        const int h = warp % H;
-        const int wph = kConsumerWarps / H;
-        const int sub = warp / H;
-        const int tk0 = block_token(g), tk1 = block_token(g + 8);
-
-        // Score columns (the mma N dimension, 8 wide).  WIDE (8 query heads per kv head): column n
-        // is head n, with a second 8-wide tile carrying the low halves.  Otherwise columns 0-3
-        // carry the high halves of heads 0-3 and columns 4-7 their low halves, so the split costs
-        // no extra mma: lane quad t then holds heads hb, hb+1 with hb = 2 (t & 1).
-        const int hb = WIDE ? 2 * t : 2 * (t & 1);
-        uint32_t qb[Gm::KSTEPS][WIDE ? 4 : 2];
-        {
-            const int head = WIDE ? g : (g & 3);
-            const bool live = head < G;
-            const __half* qv = (WIDE || g < 4 ? qh : ql) + (h * G + (live ? head : 0)) * D;
-            const __half* qv2 = ql + (h * G + (live ? head : 0)) * D;
-            const __half z = __float2half(0.0f);
+    for (int j = 0; j < nunits && !stop; ++j) {
+        const int4 u = units[j];
+        if (u.x != prev_seq) {   // a new sequence: rotate its query vectors of kv head h
+            prev_seq = u.x;
+            ++run;
+            const int qs = run & (nq - 1);
+            if (!mbar_wait(&qfull[qs], (uint32_t)(run >> (nq - 1)) & 1u)) {
+                if (lane == 0) {
+                    count_status(p.status, 3);
+                    atomicExch(flags, 1);
+                }
+                break;
+            }
+            const uint8_t* raw = qbuf + (size_t)qs * qraw_bytes;
+            float x[NB][D / 32];
 #pragma unroll
-            for (int j = 0; j < Gm::KWPT; ++j) {
-                const int W = t + 4 * j;
+            for (int k = 0; k < NB; ++k) {
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int d0 = 8 * W + 2 * hh;
-                    __half2 b0 = live ? __halves2half2(qv[d0], qv[d0 + 4]) : __halves2half2(z, z);
-                    __half2 b1 = live ? __halves2half2(qv[d0 + 1], qv[d0 + 5]) : __halves2half2(z, z);
-                    qb[2 * j + hh][0] = *reinterpret_cast<uint32_t*>(&b0);
-                    qb[2 * j + hh][1] = *reinterpret_cast<uint32_t*>(&b1);
-                    if constexpr (WIDE) {
-                        __half2 c0 = live ? __halves2half2(qv2[d0], qv2[d0 + 4]) : __halves2half2(z, z);
-                        __half2 c1 = live ? __halves2half2(qv2[d0 + 1], qv2[d0 + 5]) : __halves2half2(z, z);
-                        qb[2 * j + hh][2] = *reinterpret_cast<uint32_t*>(&c0);
-                        qb[2 * j + hh][3] = *reinterpret_cast<uint32_t*>(&c1);
-                    }
+                for (int q = 0; q < D / 32; ++q)
+                    x[k][q] = k < G ? load_elem<QT>(raw, (int64_t)(h * G + k) * D + lane + 32 * q) * sgn[lane + 32 * q]
+                                    : 0.0f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();   // this warp's reads of the buffer come before the count
+                if (atomicAdd(&qreleased[qs], 1) == kConsumerWarps - 1) {
+                    qreleased[qs] = 0;
+                    __threadfence_block();
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    if (run + nq < nruns && !*(volatile int*)flags) produce_q(run + nq);
                 }
             }
+            // v = H_d D q; a power-of-two prescale brings max|v| into [2^14, 2^15) for the fp16 halves
+            warp_fwht_batch<D, NB>(x);
+            float mx[NB];
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                mx[k] = 0.0f;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) mx[k] = fmaxf(mx[k], fabsf(x[k][q]));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                for (int k = 0; k < NB; ++k) mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], off));
+            }
+            al0 = 0.0f;
+            al1 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                const int e = prescale_exponent(mx[k]);
+                mx[k] = exp2i(e);                        // now the scale
+                const float a = lsc * exp2i(-e);         // raw score -> log2-domain logit (before s'_K)
+                if (k == hb && k < G) al0 = a;
+                if (k == hb + 1 && k < G) al1 = a;
+            }
+            // Score-mma B fragments through the scratch: lane (g, t) feeds, for code word
+            // W = t + 4 q of a key row (dims 8W .. 8W+7), the pairs (8W+2hh, 8W+2hh+4) and
+            // (8W+2hh+1, 8W+2hh+5) of its column's vector, hh = 0, 1.
+            auto build = [&](int slot, int row) {
+                const int head = WIDE ? g : (g & 3);
+                const bool live = head < G;
+                const __half* qv = qscr + row * SR;
+#pragma unroll
+                for (int q = 0; q < Gm::KWPT; ++q) {
+                    const int W = t + 4 * q;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int d0 = 8 * W + 2 * hh;
+                        qb[2 * q + hh][slot] = live ? pack_halves(qv[d0], qv[d0 + 4]) : 0u;
+                        qb[2 * q + hh][slot + 1] = live ? pack_halves(qv[d0 + 1], qv[d0 + 5]) : 0u;
+                    }
+                }
+            };
+            if constexpr (!WIDE) {
+                // rows 0-3 hold the high halves of heads 0-3 for lanes g < 4, then the low
+                // halves for lanes g >= 4
+#pragma unroll
+                for (int k = 0; k < NB; ++k) {
+                    if (k >= G) continue;
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) qscr[k * SR + lane + 32 * q] = __float2half_rn(x[k][q] * mx[k]);
+                }
+                __syncwarp();
+                if (g < 4) build(0, g & 3);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < NB; ++k) {
+                    if (k >= G) continue;
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        const float y = x[k][q] * mx[k];
+                        qscr[k * SR + lane + 32 * q] = __float2half_rn(y - __half2float(__float2half_rn(y)));
+                    }
+                }
+                __syncwarp();
+                if (g >= 4) build(0, g & 3);
+            } else {
+                // high halves of heads 0-7, then (rows reused) their low halves
+#pragma unroll
+                for (int k = 0; k < NB; ++k) {
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) qscr[k * SR + lane + 32 * q] = __float2half_rn(x[k][q] * mx[k]);
+                }
+                __syncwarp();
+                build(0, g);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < NB; ++k) {
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        const float y = x[k][q] * mx[k];
+                        qscr[k * SR + lane + 32 * q] = __float2half_rn(y - __half2float(__float2half_rn(y)));
+                    }
+                }
+                __syncwarp();
+                build(2, g);
+            }
+            __syncwarp();   // the scratch is free for the next run
         }
-        const float al0 = (hb < G) ? alpha[h * G + hb] : 0.0f;
-        const float al1 = (hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
-        const bool lo_lane = !WIDE && t >= 2;   // this lane's P columns carry low halves
+
+#pragma unroll
+        for (int i = 0; i < Gm::MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+        m0 = kNegBig;
+        m1 = kNegBig;
+        l0 = 0.0f;
+        l1 = 0.0f;
+        eref = 0;
+        const int li0 = ustart[j] - Bs;
+        const int nbu = (u.w + kBlockSize - 1) / kBlockSize;
 
         // Two blocks (32 tokens) per iteration: their score chains, one softmax update and their
         // P.V products interleave, which gives each warp independent work to overlap latencies.
-        for (int i = 0; i < nblk; i += 2) {
-            const int npair = min(2, nblk - i);
+        for (int k = 0; k < nbu; k += 2) {
+            const int i = li0 + k;
+            const int npair = min(2, nbu - k);
             int st[2];
             bool ok[2];
 #pragma unroll
             for (int b = 0; b < 2; ++b) st[b] = (i + b) % kStages;
             bool timed_out = false;
             for (int b = 0; b < npair; ++b) {
-                if (!mbar_wait(&full[st[b]], ((i + b) / kStages) & 1)) timed_out = true;
+                if (!mbar_wait(&full[st[b]], (uint32_t)((i + b) / kStages) & 1u)) timed_out = true;
             }
             if (timed_out) {
                 if (lane == 0) {
                     count_status(p.status, 3);
-                    atomicExch(abort_flag, 1);
+                    atomicExch(flags, 1);
                 }
+                stop = true;
                 break;
             }
 #pragma unroll
             for (int b = 0; b < 2; ++b) ok[b] = b < npair && valid[st[b]];
-            if (((i >> 1) % wph) == sub && (ok[0] || ok[1])) {
+            if (((k >> 1) & (wph - 1)) == sub && (ok[0] || ok[1])) {
                 const uint8_t* kp[2];
                 const uint8_t* vp[2];
-                int tokbase[2];
                 float x[2][4];
                 uint32_t vs0[2], vs1[2];
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     kp[b] = ring + (size_t)st[b] * stage_bytes;
                     vp[b] = kp[b] + (size_t)kBlockSize * H * Gm::RB;
-                    tokbase[b] = (blk_first + i + b) * kBlockSize;
                 }
                 // ---- S^T = (K - zp) Q'^T for both blocks, high and low halves of Q'
 #pragma unroll
@@ -254,15 +564,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         const uint32_t zl0 = z0l | (z0l << 16), zh0 = z0h | (z0h << 16);
                         const uint32_t zl1 = z1l | (z1l << 16), zh1 = z1h | (z1h << 16);
 #pragma unroll
-                        for (int j = 0; j < Gm::KWPT; ++j) {
+                        for (int q = 0; q < Gm::KWPT; ++q) {
                             uint32_t a0[4], a1[4];
-                            unpack_word(kr0[t + 4 * j], zl0, zh0, a0);
-                            unpack_word(kr1[t + 4 * j], zl1, zh1, a1);
-                            mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * j][0], qb[2 * j][1]);
-                            mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][0], qb[2 * j + 1][1]);
+                            unpack_word(kr0[t + 4 * q], zl0, zh0, a0);
+                            unpack_word(kr1[t + 4 * q], zl1, zh1, a1);
+                            mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * q][0], qb[2 * q][1]);
+                            mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][0], qb[2 * q + 1][1]);
                             if constexpr (WIDE) {
-                                mma_f16_16816(cl, a0[0], a1[0], a0[1], a1[1], qb[2 * j][2], qb[2 * j][3]);
-                                mma_f16_16816(cl, a0[2], a1[2], a0[3], a1[3], qb[2 * j + 1][2], qb[2 * j + 1][3]);
+                                mma_f16_16816(cl, a0[0], a1[0], a0[1], a1[1], qb[2 * q][2], qb[2 * q][3]);
+                                mma_f16_16816(cl, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][2], qb[2 * q + 1][3]);
                             }
                         }
                     }
@@ -271,7 +581,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         if constexpr (WIDE) c[e] += cl[e];
                         else c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);   // high + low columns
                     }
-                    const bool v0 = ok[b] && tokbase[b] + tk0 < tok_end, v1 = ok[b] && tokbase[b] + tk1 < tok_end;
+                    const int tb = (k + b) * kBlockSize;   // token offset of this block in the unit
+                    const bool v0 = ok[b] && tb + tk0 < u.w, v1 = ok[b] && tb + tk1 < u.w;
                     const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
                     x[b][0] = v0 ? c[0] * sk0 * al0 : -INFINITY;
                     x[b][1] = v0 ? c[1] * sk0 * al1 : -INFINITY;
@@ -335,15 +646,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     uint32_t xlo_h, xlo_l, xhi_h, xhi_l;
                     split_f16x2(pr[b][0] * sv0, pr[b][1] * sv0, xlo_h, xlo_l);
                     split_f16x2(pr[b][2] * sv1, pr[b][3] * sv1, xhi_h, xhi_l);
-                    uint32_t b0, b1, b0l = 0, b1l = 0;
+                    uint32_t bb0, bb1, bb0l = 0, bb1l = 0;
                     if constexpr (WIDE) {
-                        b0 = movmatrix_trans(xlo_h);
-                        b1 = movmatrix_trans(xhi_h);
-                        b0l = movmatrix_trans(xlo_l);
-                        b1l = movmatrix_trans(xhi_l);
+                        bb0 = movmatrix_trans(xlo_h);
+                        bb1 = movmatrix_trans(xhi_h);
+                        bb0l = movmatrix_trans(xlo_l);
+                        bb1l = movmatrix_trans(xhi_l);
                     } else {
-                        b0 = movmatrix_trans(lo_lane ? xlo_l : xlo_h);
-                        b1 = movmatrix_trans(lo_lane ? xhi_l : xhi_h);
+                        bb0 = movmatrix_trans(lo_lane ? xlo_l : xlo_h);
+                        bb1 = movmatrix_trans(lo_lane ? xhi_l : xhi_h);
                     }
                     const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp[b] + ((t)*H + h) * Gm::RB);
                     const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 4) * H + h) * Gm::RB);
@@ -355,15 +666,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     const uint32_t zl23 = zp_lo_half(w2 & 15u) | (zp_lo_half(w3 & 15u) << 16);
                     const uint32_t zh23 = zp_hi_half(w2 & 15u) | (zp_hi_half(w3 & 15u) << 16);
                     if constexpr (D == 128) {
-                        uint32_t ua[8], ub[8], uc[8], ud[8];
-                        unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);           // d = 8g + i, tokens t, t+4
-                        unpack_word_pair(vr0[g + 8], vr1[g + 8], zl01, zh01, ub);   // d = 64 + 8g + i
-                        unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);           // tokens t+8, t+12
+                        uint32_t ua[8], ubv[8], uc[8], ud[8];
+                        unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);            // d = 8g + i, tokens t, t+4
+                        unpack_word_pair(vr0[g + 8], vr1[g + 8], zl01, zh01, ubv);   // d = 64 + 8g + i
+                        unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);            // tokens t+8, t+12
                         unpack_word_pair(vr2[g + 8], vr3[g + 8], zl23, zh23, ud);
 #pragma unroll
                         for (int mt = 0; mt < 8; ++mt) {
-                            mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0, b1);
-                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ub[mt], uc[mt], ud[mt], b0l, b1l);
+                            mma_f16_16816(o[mt], ua[mt], ubv[mt], uc[mt], ud[mt], bb0, bb1);
+                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ubv[mt], uc[mt], ud[mt], bb0l, bb1l);
                         }
                     } else {
                         uint32_t ua[8], uc[8];
@@ -371,8 +682,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);
 #pragma unroll
                         for (int mt = 0; mt < 4; ++mt) {
-                            mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0, b1);
-                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], b0l, b1l);
+                            mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], bb0, bb1);
+                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], bb0l, bb1l);
                         }
                     }
                 }
@@ -385,21 +696,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         released[st[b]] = 0;
                         __threadfence_block();
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        if (i + b + kStages < nblk && !*(volatile int*)abort_flag) produce(i + b + kStages);
+                        if (i + b + kStages < nb_cta && !*(volatile int*)flags) produce(i + b + kStages);
                     }
                 }
             }
         }
-    }
-    // ---- per-warp state to shared memory, once the ring is drained
-    __syncthreads();
-    if (threadIdx.x == 0 && abort_flag[0]) {
-        // a wait gave up: let every copy still in flight land before the ring is reused
-        const int issued = abort_flag[1];
-        for (int i = max(0, issued - kStages); i < issued; ++i) mbar_wait(&full[i % kStages], (i / kStages) & 1);
-    }
-    __syncthreads();
-    {
+        if (stop) break;
+
+        // ---- this warp's partial of unit j: (m, l) per column and O in fragment order, O scaled
+        // back by 2^(E - 127).  Lanes t < 2 hold the finished columns when the low halves ride in
+        // columns 4-7 (their sums are added in first).
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -412,179 +718,251 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
             }
         }
-        const int hb = WIDE ? 2 * t : 2 * (t & 1);
         const float es = eref ? __uint_as_float(eref << 23) : 0.0f;   // 2^(eref - 127)
-        float* so = st_o + warp * 8 * D;
+        const size_t recn = (size_t)u.z * kConsumerWarps + warp;
         if (WIDE || t < 2) {
+            const int ls = WIDE ? lane : (g * 2 + t);
+            float4* po = reinterpret_cast<float4*>(p.ws_po + recn * PO) + ls;
 #pragma unroll
-            for (int mt = 0; mt < Gm::MT; ++mt) {
-                const int dlo = 8 * g + mt;
-                const int dhi = (D == 128) ? 64 + 8 * g + mt : 8 * g + 4 + mt;
-                so[hb * D + dlo] = o[mt][0] * es;
-                so[(hb + 1) * D + dlo] = o[mt][1] * es;
-                so[hb * D + dhi] = o[mt][2] * es;
-                so[(hb + 1) * D + dhi] = o[mt][3] * es;
-            }
+            for (int mt = 0; mt < Gm::MT; ++mt)
+                po[mt * NLS] = make_float4(o[mt][0] * es, o[mt][1] * es, o[mt][2] * es, o[mt][3] * es);
             if (g == 0) {
-                st_m[warp * 8 + hb] = m0;
-                st_m[warp * 8 + hb + 1] = m1;
-                st_l[warp * 8 + hb] = l0;
-                st_l[warp * 8 + hb + 1] = l1;
+                float* ml = p.ws_pml + recn * 16 + 2 * (2 * t);
+                ml[0] = m0;
+                ml[1] = l0;
+                ml[2] = m1;
+                ml[3] = l1;
             }
         }
     }
-    __syncthreads();
 
-    // ---- merge the warps of each kv head, then finish (single segment) or store the partial;
-    // four vectors per warp at a time
-    const int wph = kConsumerWarps / H;
-    for (int v0 = warp; v0 < Hq; v0 += 4 * kConsumerWarps) {
-        float acc[4][D / 32], inv_l[4];
-        int64_t ooff[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int v = v0 + k * kConsumerWarps;
-#pragma unroll
-            for (int j = 0; j < D / 32; ++j) acc[k][j] = 0.0f;
-            inv_l[k] = 0.0f;
-            ooff[k] = -1;
-            if (v >= Hq) continue;
-            const int h = v / G, col = v % G;
-            float M = kNegBig;
-            for (int s = 0; s < wph; ++s) M = fmaxf(M, st_m[(h + s * H) * 8 + col]);
-            float Lsum = 0.0f;
-            for (int s = 0; s < wph; ++s) {
-                const int w = h + s * H;
-                const float wt = fast_exp2(st_m[w * 8 + col] - M);
-                Lsum += wt * st_l[w * 8 + col];
-#pragma unroll
-                for (int j = 0; j < D / 32; ++j) acc[k][j] += wt * st_o[(w * 8 + col) * D + lane + 32 * j];
-            }
-            if (nseg == 1) {
-                inv_l[k] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-                ooff[k] = ((int64_t)q0 * Hq + v) * D;
-            } else {
-                const int64_t pi = ((int64_t)seq * Hq + v) * p.nseg_max + seg;
-#pragma unroll
-                for (int j = 0; j < D / 32; ++j) p.ws_o[pi * D + lane + 32 * j] = acc[k][j];
-                if (lane == 0) {
-                    p.ws_ml[pi * 2] = M;
-                    p.ws_ml[pi * 2 + 1] = Lsum;
-                }
-            }
-        }
-        if (nseg == 1) unrotate_store_batch<D, OT, 4>(acc, inv_l, sgn, p.c, p.out, ooff);
+    // ---- a wait gave up: let every copy still in flight land before the CTA exits
+    __syncthreads();
+    if (threadIdx.x == 0 && flags[0]) {
+        const int issued = flags[1];
+        for (int i = max(0, issued - kStages); i < issued; ++i) mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u);
+        const int qissued = flags[2];
+        for (int r = max(0, qissued - nq); r < qissued; ++r) mbar_wait(&qfull[r & (nq - 1)], (uint32_t)(r >> (nq - 1)) & 1u);
     }
 }
 
-// Combine the per-segment partials of every decode sequence that spans more than one segment.
-template <int D, typename OT>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p) {
+// ------------------------------------------------------------------ 2. combine
+
+constexpr int kCombineWarps = 8;
+
+// One warp per (decode sequence, kv head h, chunk of kDecodeChunkRecords records), a record
+// being (unit, warp of kv head h); grid (chunk groups, kv heads, sequences), min(8, chunks)
+// warps per CTA.  Lane l owns the accumulator slots l + 32 k of the partial
+// outputs (whole 512-byte rows per k, so every load is coalesced) and merges its chunk's records
+// in order with an online rescaling.  A sequence with one chunk is finished by that warp; with
+// several, each chunk is published to the workspace and the last chunk to arrive (counted
+// atomically, nothing waits) merges all chunks in chunk order.  Every sum's order depends only on
+// the sequence, never on the batch or on which warp finished last.
+template <int D, bool WIDE, typename OT>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttnParams p) {
+    constexpr int NLS = WIDE ? 32 : 16;
+    constexpr int NT = Geo<D>::MT * NLS;   // float4 slots of one record
+    constexpr int SPL = NT / 32;           // slots per lane
+    constexpr int UNR = WIDE ? 2 : 4;      // records in flight per lane
+    constexpr int CPF = NT * 4 + 16;       // floats of a chunk partial: slots, then (m, l) per column
+    constexpr int SO = D + 4;
     __shared__ float sgn[D];
+    extern __shared__ __align__(16) float sout_all[];   // [warps][8 * SO]
+    griddep_wait();
+    griddep_launch_dependents();   // the next call's walker may start its set-up
     for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
     __syncthreads();
-    const int seq = blockIdx.x;
-    const int v = blockIdx.y * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (v >= p.Hq) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, G = p.G, Hq = p.Hq, C = p.combine_chunks;
+    const int c = blockIdx.x * (blockDim.x >> 5) + warp, h = blockIdx.y, seq = blockIdx.z;
+    if (c >= C) return;
     const int q0 = __ldg(p.qsl + seq);
-    if (__ldg(p.qsl + seq + 1) - q0 != 1) return;
-    if (q0 < 0 || (int64_t)q0 >= p.num_q_tokens) return;
-    const int L = min(__ldg(p.seq_lens + seq), min(p.max_blocks_per_seq * kBlockSize, p.nseg_max * p.seg_len));
-    const int nseg = (L + p.seg_len - 1) / p.seg_len;
-    if (nseg <= 1) return;
-    const int64_t base = ((int64_t)seq * p.Hq + v) * p.nseg_max;
-    // lanes run over segments: global max, per-segment weights and the weighted sum of l
-    float M = kNegBig;
-    for (int s0 = 0; s0 < nseg; s0 += 32) {
-        const int s = s0 + lane;
-        if (s < nseg) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
+    if (__ldg(p.qsl + seq + 1) - q0 != 1 || q0 < 0 || (int64_t)q0 >= p.num_q_tokens) return;
+    const int L = min(max(__ldg(p.seq_lens + seq), 0), p.len_cap);
+    const int nseg = (int)fast_div((uint32_t)(L + p.seg_len - 1), (uint32_t)p.seg_len, p.seg_rcp);
+    const int64_t obase = ((int64_t)q0 * Hq + (int64_t)h * G) * D;
+    if (nseg == 0) {   // empty context: zero output
+        if (c == 0)
+            for (int i = lane; i < G * D; i += 32) store_elem<OT>(p.out, obase + i, 0.0f);
+        return;
     }
-    M = warp_max(M);
-    float Lpart = 0.0f;
-    float acc[D / 32];
+    const int ws = p.wph_shift;
+    const int R = nseg << ws;
+    const int nch = (R + kDecodeChunkRecords - 1) / kDecodeChunkRecords;
+    if (c >= nch) return;
+    const int ub = p.ws_meta[seq];
+    auto rec_of = [&](int r) -> size_t {
+        return (size_t)(ub + (r >> ws)) * kConsumerWarps + h + (r & ((1 << ws) - 1)) * H;
+    };
+    const int tq = WIDE ? (lane & 3) : (lane & 1);   // this lane's columns: 2 tq, 2 tq + 1
+
+    float m0 = kNegBig, m1 = kNegBig, l0 = 0.0f, l1 = 0.0f;
+    float4 acc[SPL];
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
-    for (int s0 = 0; s0 < nseg; s0 += 32) {
-        const int s = s0 + lane;
-        const float wt = s < nseg ? fast_exp2(p.ws_ml[(base + s) * 2] - M) : 0.0f;
-        if (s < nseg) Lpart += wt * p.ws_ml[(base + s) * 2 + 1];
-        const int n = min(32, nseg - s0);
-        // partial outputs of this group of segments: independent loads, four segments at a time
-        for (int j0 = 0; j0 < n; j0 += 4) {
-            float o4[4][D / 32], w4[4];
+    for (int k = 0; k < SPL; ++k) acc[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    auto merge = [&](const float4& ml, const float4 (&ov)[SPL]) {
+        const float n0 = fmaxf(m0, ml.x), n1 = fmaxf(m1, ml.z);
+        const float a0 = fast_exp2(m0 - n0), b0 = fast_exp2(ml.x - n0);
+        const float a1 = fast_exp2(m1 - n1), b1 = fast_exp2(ml.z - n1);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u;
-                w4[u] = __shfl_sync(0xffffffffu, wt, j & 31);
+        for (int k = 0; k < SPL; ++k) {
+            acc[k].x = acc[k].x * a0 + ov[k].x * b0;
+            acc[k].z = acc[k].z * a0 + ov[k].z * b0;
+            acc[k].y = acc[k].y * a1 + ov[k].y * b1;
+            acc[k].w = acc[k].w * a1 + ov[k].w * b1;
+        }
+        l0 = l0 * a0 + ml.y * b0;
+        l1 = l1 * a1 + ml.w * b1;
+        m0 = n0;
+        m1 = n1;
+    };
+    const float4* po = reinterpret_cast<const float4*>(p.ws_po);
+    const float4* pml = reinterpret_cast<const float4*>(p.ws_pml);
+    const int r_end = min(R, (c + 1) * kDecodeChunkRecords);
+    for (int r0 = c * kDecodeChunkRecords; r0 < r_end; r0 += UNR) {
+        float4 ml[UNR], ov[UNR][SPL];
 #pragma unroll
-                for (int k = 0; k < D / 32; ++k)
-                    o4[u][k] = j < n ? p.ws_o[(base + s0 + j) * D + lane + 32 * k] : 0.0f;
+        for (int u = 0; u < UNR; ++u) {
+            const bool live = r0 + u < r_end;
+            const size_t rc = rec_of(live ? r0 + u : r0);
+            ml[u] = live ? pml[rc * 4 + tq] : make_float4(kNegBig, 0.0f, kNegBig, 0.0f);
+#pragma unroll
+            for (int k = 0; k < SPL; ++k) ov[u][k] = live ? po[rc * NT + lane + 32 * k] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) merge(ml[u], ov[u]);
+    }
+
+    if (nch > 1) {
+        const int64_t pair = (int64_t)seq * H + h;
+        float4* cp = reinterpret_cast<float4*>(p.ws_cp + (pair * C + c) * CPF);
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) cp[lane + 32 * k] = acc[k];
+        if (lane < (WIDE ? 4 : 2)) cp[NT + tq] = make_float4(m0, l0, m1, l1);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(p.ws_cnt + pair, 1) == nch - 1;
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence();
+        m0 = kNegBig;
+        m1 = kNegBig;
+        l0 = 0.0f;
+        l1 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) acc[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const float4* cps = reinterpret_cast<const float4*>(p.ws_cp + pair * C * CPF);
+        for (int c0 = 0; c0 < nch; c0 += UNR) {
+            float4 ml[UNR], ov[UNR][SPL];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const bool live = c0 + u < nch;
+                const float4* q = cps + (size_t)(live ? c0 + u : c0) * (CPF / 4);
+                ml[u] = live ? __ldcg(q + NT + tq) : make_float4(kNegBig, 0.0f, kNegBig, 0.0f);
+#pragma unroll
+                for (int k = 0; k < SPL; ++k) ov[u][k] = live ? __ldcg(q + lane + 32 * k) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-#pragma unroll
-                for (int k = 0; k < D / 32; ++k) acc[k] += w4[u] * o4[u][k];
-            }
+            for (int u = 0; u < UNR; ++u) merge(ml[u], ov[u]);
         }
     }
+
+    // normalise, transpose through shared memory, un-rotate each of the G outputs
+    float* so = sout_all + warp * 8 * SO;
+    const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
+    const int c0 = 2 * tq, c1 = c0 + 1;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lpart += __shfl_xor_sync(0xffffffffu, Lpart, o);
-    const float Lsum = Lpart;
-    unrotate_store<D, OT>(acc, Lsum > 0.0f ? 1.0f / Lsum : 0.0f, sgn, p.c, p.out, ((int64_t)q0 * p.Hq + v) * D);
+    for (int k = 0; k < SPL; ++k) {
+        const int slot = lane + 32 * k;
+        const int mt = slot / NLS, ls = slot % NLS;
+        const int gq = WIDE ? (ls >> 2) : (ls >> 1);
+        const int dlo = 8 * gq + mt;
+        const int dhi = (D == 128) ? 64 + 8 * gq + mt : 8 * gq + 4 + mt;
+        if (c0 < G) {
+            so[c0 * SO + dlo] = acc[k].x * inv0;
+            so[c0 * SO + dhi] = acc[k].z * inv0;
+        }
+        if (c1 < G) {
+            so[c1 * SO + dlo] = acc[k].y * inv1;
+            so[c1 * SO + dhi] = acc[k].w * inv1;
+        }
+    }
+    __syncwarp();
+    for (int col = 0; col < G; ++col) {
+        float x[D / 32];
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) x[k] = so[col * SO + lane + 32 * k];
+        unrotate_store<D, OT>(x, 1.0f, sgn, p.c, p.out, obase + (int64_t)col * D);
+    }
 }
 
-template <int D, typename QT, typename OT>
-cudaError_t launch_decode_t(const AttnParams& p, cudaStream_t stream) {
-    const DecodeSmem lay = decode_smem_layout<D>(p.H, p.Hq);
-    const bool wide = p.G == 8;
-    auto kern = wide ? decode_kernel<D, true, QT, OT> : decode_kernel<D, false, QT, OT>;
-    cudaError_t err = wide ? opt_in_smem<decode_kernel<D, true, QT, OT>>(lay.total)
-                           : opt_in_smem<decode_kernel<D, false, QT, OT>>(lay.total);
+// ------------------------------------------------------------------ launchers
+
+template <int D, bool WIDE, typename QT, typename OT>
+cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stream) {
+    const DecodeSmem lay = decode_smem_layout<D, WIDE>(p.H, p.Hq);
+    cudaError_t err = opt_in_smem<decode_kernel<D, WIDE, QT>>(lay.total);
     if (err != cudaSuccess) return err;
-    dim3 grid(p.nseg_max, p.num_seqs);
-    kern<<<grid, kDecodeThreads, lay.total, stream>>>(p);
-    return cudaGetLastError();
+    // Both kernels are programmatic dependents of their predecessor: each starts its set-up while
+    // the previous kernel finishes and waits for it (griddep_wait) before touching its results.
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t wcfg = {};
+    wcfg.gridDim = dim3((unsigned)num_ctas);
+    wcfg.blockDim = dim3(kDecodeThreads);
+    wcfg.dynamicSmemBytes = lay.total;
+    wcfg.stream = stream;
+    wcfg.attrs = &attr;
+    wcfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&wcfg, decode_kernel<D, WIDE, QT>, p);
+    if (err != cudaSuccess) return err;
+
+    const int warps = p.combine_chunks < kCombineWarps ? p.combine_chunks : kCombineWarps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.combine_chunks + warps - 1) / warps), (unsigned)p.H, (unsigned)p.num_seqs);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = (size_t)warps * 8 * (D + 4) * 4;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, WIDE, OT>, p);
 }
 
-template <int D, typename OT>
-cudaError_t launch_combine_t(const AttnParams& p, cudaStream_t stream) {
-    dim3 grid(p.num_seqs, (p.Hq + 7) / 8);
-    combine_kernel<D, OT><<<grid, 256, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-template <int D, typename QT>
-cudaError_t decode_by_out(const AttnParams& p, DType out_dt, cudaStream_t s) {
+template <int D, bool WIDE, typename QT>
+cudaError_t decode_by_out(const AttnParams& p, int num_ctas, DType out_dt, cudaStream_t s) {
     switch (out_dt) {
-        case DType::F16: return launch_decode_t<D, QT, __half>(p, s);
-        case DType::BF16: return launch_decode_t<D, QT, __nv_bfloat16>(p, s);
-        default: return launch_decode_t<D, QT, float>(p, s);
+        case DType::F16: return launch_decode_t<D, WIDE, QT, __half>(p, num_ctas, s);
+        case DType::BF16: return launch_decode_t<D, WIDE, QT, __nv_bfloat16>(p, num_ctas, s);
+        default: return launch_decode_t<D, WIDE, QT, float>(p, num_ctas, s);
     }
 }
 
-template <int D>
-cudaError_t combine_by_out(const AttnParams& p, DType out_dt, cudaStream_t s) {
-    switch (out_dt) {
-        case DType::F16: return launch_combine_t<D, __half>(p, s);
-        case DType::BF16: return launch_combine_t<D, __nv_bfloat16>(p, s);
-        default: return launch_combine_t<D, float>(p, s);
-    }
+template <int D, bool WIDE>
+cudaError_t decode_by_q(const AttnParams& p, int num_ctas, DType q_dt, DType out_dt, cudaStream_t s) {
+    return q_dt == DType::BF16 ? decode_by_out<D, WIDE, __nv_bfloat16>(p, num_ctas, out_dt, s)
+                               : decode_by_out<D, WIDE, __half>(p, num_ctas, out_dt, s);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const AttnParams& p, int head_size, DType q_dt, DType out_dt, cudaStream_t stream) {
+int decode_grid_size(int64_t max_blocks_total, int64_t max_units) {
+    int64_t n = 2ll * num_sms();
+    if (n > max_units) n = max_units;
+    const int64_t need = (max_blocks_total + kMaxUnits - 1) / kMaxUnits;   // at most kMaxUnits unit starts per CTA
+    if (n < need) n = need;
+    if (n < 1) n = 1;
+    return n > 0x7FFFFFFF ? 0x7FFFFFFF : (int)n;
+}
+
+cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
+                          cudaStream_t stream) {
+    const bool wide = p.G == 8;
     if (head_size == 128)
-        return q_dt == DType::BF16 ? decode_by_out<128, __nv_bfloat16>(p, out_dt, stream)
-                                   : decode_by_out<128, __half>(p, out_dt, stream);
-    return q_dt == DType::BF16 ? decode_by_out<64, __nv_bfloat16>(p, out_dt, stream)
-                               : decode_by_out<64, __half>(p, out_dt, stream);
+        return wide ? decode_by_q<128, true>(p, num_ctas, q_dt, out_dt, stream)
+                    : decode_by_q<128, false>(p, num_ctas, q_dt, out_dt, stream);
+    return wide ? decode_by_q<64, true>(p, num_ctas, q_dt, out_dt, stream)
+                : decode_by_q<64, false>(p, num_ctas, q_dt, out_dt, stream);
 }
-
-cudaError_t launch_combine(const AttnParams& p, int head_size, DType out_dt, cudaStream_t stream) {
-    return head_size == 128 ? combine_by_out<128>(p, out_dt, stream) : combine_by_out<64>(p, out_dt, stream);
-}
-
 
 }  // namespace kvi4

@@ -31,6 +31,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// n / d for n < 2^31 with rcp = floor(2^32 / d) (all ones for d = 1): the high product is n / d
+// or one less, and one comparison fixes it.
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, uint32_t d, uint32_t rcp) {
+    uint32_t q = __umulhi(n, rcp);
+    if (n - q * d >= d) ++q;
+    return q;
+}
+
 __device__ __forceinline__ void count_status(uint32_t* status, int which) {
     if (status != nullptr) atomicAdd(status + which, 1u);
 }
@@ -91,6 +99,23 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with the programmatic-serialization attribute may start while the previous
+// kernel of the stream is still running; griddep_wait() blocks until that kernel has completed and
+// its memory is visible.  Without the attribute both are no-ops.
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // -------------------------------------------------------------------- packed fp32 (sm_100+)

@@ -35,8 +35,11 @@ struct AttnParams {
     const int32_t* qsl;       // query_start_loc
     const float* signs;
     void* out;
-    float* ws_o;              // [num_q_tokens, Hq, nseg_max, D] partial outputs (not normalised)
-    float* ws_ml;             // [num_q_tokens, Hq, nseg_max, 2] partial (max in log2 units, sum)
+    int32_t* ws_meta;         // [num_seqs + 1] first split-KV unit of each sequence (exclusive prefix)
+    int32_t* ws_cnt;          // [num_seqs, H] combine chunks finished (zeroed by the walker)
+    float* ws_cp;             // [num_seqs, H, combine_chunks, ...] combine chunk partials
+    float* ws_po;             // [units, 8 warps, po_floats] unnormalised partial outputs (fragment order)
+    float* ws_pml;            // [units, 8 warps, 8 columns, 2] partial (max in log2 units, sum)
     uint32_t* status;
     int64_t num_blocks;
     int64_t num_q_tokens;
@@ -46,20 +49,39 @@ struct AttnParams {
     int G;                    // q heads per kv head
     int Hq;
     int max_blocks_per_seq;
-    int seg_len;              // decode split-KV segment length (tokens, multiple of 16)
-    int nseg_max;
+    int seg_len;              // decode split-KV segment (unit) length in tokens, a multiple of 16
+    int len_cap;              // decode context lengths are clamped to this (max_seq_len, block table)
+    int combine_chunks;       // most combine chunks a (sequence, kv head) can have
+    uint32_t seg_rcp;         // floor(2^32 / seg_len), for fast_div
+    uint32_t segb_rcp;        // floor(2^32 / (seg_len / 16)) (all ones for 1)
+    int wph_shift;            // log2(8 / H): consumer warps per kv head
     float softmax_scale;
     float c;                  // fp32(1 / sqrt(head_size))
 };
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
-cudaError_t launch_decode(const AttnParams& p, int head_size, DType q_dt, DType out_dt, cudaStream_t stream);
-cudaError_t launch_combine(const AttnParams& p, int head_size, DType out_dt, cudaStream_t stream);
+// Decode path: query rotation, the split-KV segment walker, and the combine that finishes every
+// decode sequence.  num_ctas is the walker's grid (decode_grid_size).
+cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
+                          cudaStream_t stream);
+int decode_grid_size(int64_t max_blocks_total, int64_t max_units);
+constexpr int kDecodeMaxUnits = 256;   // split-KV units one walker CTA may own
+constexpr int kDecodeChunkRecords = 8; // partial records one combine warp merges
+
+// One warp's unnormalised partial output of one split-KV unit of the decode path: D/16 row tiles
+// x 16 (32 when G == 8) lanes x 4 accumulators (shared by the host's workspace layout and the
+// kernels).
+inline constexpr uint32_t decode_po_floats(int D, int G) { return (uint32_t)(D / 16) * (G == 8 ? 32u : 16u) * 4u; }
+// One combine chunk partial: the same accumulators, then (max, sum) for 8 columns.
+inline constexpr uint32_t decode_cp_floats(int D, int G) { return decode_po_floats(D, G) + 16u; }
 cudaError_t launch_prefill(const AttnParams& p, int head_size, int max_query_len, DType q_dt, DType out_dt,
                            cudaStream_t stream);
 
 int num_sms();
+
+// floor(2^32 / d) for 1 <= d (all ones for d = 1): the multiplier fast_div expects.
+inline uint32_t div_rcp(uint32_t d) { return d <= 1 ? 0xFFFFFFFFu : (uint32_t)((1ull << 32) / d); }
 
 // Opt a kernel in to `bytes` of dynamic shared memory, once per device (so that launches issued
 // under stream capture contain nothing but the launch itself).

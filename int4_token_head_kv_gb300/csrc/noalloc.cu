@@ -39,7 +39,7 @@ extern "C" kv_int4_status kv_int4_paged_attention_noalloc(
     int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
     int32_t max_query_len, int32_t max_seq_len, float softmax_scale, const float* rht_signs, int32_t segment_len,
     void* out, kv_int4_dtype out_dtype, kv_int4_stream_t stream) {
-    const size_t need = kv_int4_attention_workspace_bytes(num_q_tokens, num_q_heads, head_size, num_seqs,
+    const size_t need = kv_int4_attention_workspace_bytes(num_q_heads, num_kv_heads, head_size, num_seqs,
                                                           max_seq_len, segment_len);
     if (need > KV_INT4_NOALLOC_SCRATCH_BYTES) return KV_INT4_EWORKSPACE;
     void* scratch = nullptr;

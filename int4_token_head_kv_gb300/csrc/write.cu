@@ -184,6 +184,10 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
     using Gm = Geo<D>;
     using Sm = WriteSmem<D>;
     extern __shared__ __align__(128) uint8_t smem[];
+    // Launched as a programmatic dependent: wait for the previous kernel of the stream (it may
+    // produce K, V or the slots), then let the next kernel start its own set-up.
+    griddep_wait();
+    griddep_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint8_t* wbuf = smem + warp * Sm::kPerWarp;
     uint32_t* sign_mask = reinterpret_cast<uint32_t*>(smem + kWriteWarps * Sm::kPerWarp);
@@ -293,8 +297,17 @@ cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
     if (blocks < 1) blocks = 1;
     cudaError_t err = opt_in_smem<write_kernel<D, T>>(Sm::kBytes);
     if (err != cudaSuccess) return err;
-    write_kernel<D, T><<<(unsigned)blocks, kWriteThreads, Sm::kBytes, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kWriteThreads);
+    cfg.dynamicSmemBytes = Sm::kBytes;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, write_kernel<D, T>, p);
 }
 
 }  // namespace

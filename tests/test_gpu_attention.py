@@ -116,6 +116,22 @@ def test_segment_lengths(segment_len):
     _run_case(wl, segment_len=segment_len)
 
 
+def test_segment_longer_than_the_staged_block_table():
+    # one 600-block segment: the walker stages the first 256 block ids in shared memory and looks
+    # the rest up in the block table as it goes
+    wl = workloads.make_attention_workload("bigseg", [9600, 700], [1, 1], 16, 4, 128, seed=12)
+    _run_case(wl, segment_len=9600)
+
+
+def test_many_short_sequences_per_cta():
+    # 3000 one-block decode sequences of 1..16 tokens: each walker CTA runs about ten sequences,
+    # cycling its rotated-query buffers
+    r = np.random.default_rng(13)
+    lens = r.integers(1, 17, 3000).tolist()
+    wl = workloads.make_attention_workload("short", lens, [1] * 3000, 8, 2, 64, seed=13)
+    _run_case(wl, segment_len=16, seqs=list(range(0, 3000, 37)))
+
+
 def test_segment_split_changes_only_rounding():
     from gpu_helpers import gpu_attention, gpu_cache, gpu_write
     wl = workloads.make_attention_workload("segs", [3000], [1], 32, 8, 128, seed=6)

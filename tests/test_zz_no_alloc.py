@@ -67,7 +67,7 @@ def test_noalloc_matches_regular_entry_point_twice():
         workloads.make_attention_workload("noalloc_b", [2600, 90, 1777], [1, 1, 1], 32, 8, 128, seed=22),
     ]
     for wl in batches:
-        assert kv.kv_int4_attention_workspace_bytes(wl.query.shape[0], 32, 128, len(wl.seq_lens), wl.max_seq_len,
+        assert kv.kv_int4_attention_workspace_bytes(32, 8, 128, len(wl.seq_lens), wl.max_seq_len,
                                                     seg) > 0   # the scratch really is used
         t = _device_inputs(wl, dev)
         ref = kv.kv_int4_paged_attention(t["q"], t["cache"], t["tables"], t["lens"], t["qsl"], wl.softmax_scale,
@@ -87,8 +87,8 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     wl = workloads.make_attention_workload("noalloc_big", [64], [1], 32, 8, 128, seed=23)
     t = _device_inputs(wl, dev)
     out = torch.empty((1, 32, 128), dtype=torch.float32, device=dev)
-    # 4096 sequences x 32 heads x 2048 segments of 16 tokens would need far more than the scratch
-    need = kv.kv_int4_attention_workspace_bytes(4096, 32, 128, 4096, 32768, 16)
+    # 4096 sequences x 2048 segments of 16 tokens would need far more than the scratch
+    need = kv.kv_int4_attention_workspace_bytes(32, 8, 128, 4096, 32768, 16)
     assert need > SCRATCH_BYTES
     rc = f(t["q"].data_ptr(), 1, 4096, 32, t["cache"].data_ptr(), wl.num_blocks, 8, 128, 16, t["tables"].data_ptr(),
            1, t["lens"].data_ptr(), t["qsl"].data_ptr(), 4096, 1, 32768, wl.softmax_scale, t["signs"].data_ptr(), 16,
