@@ -28,12 +28,17 @@
 //    its kv head itself (H_d D q in fp32, then fp16 high + low halves laid out as mma fragments
 //    through a small per-warp shared-memory scratch).
 //  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block pair when H < 8).
-//    Scores S^T[16 tokens x 8 columns] = (K - zp)[16 x D] . Q'^T come from mma.sync m16n8k16 on
-//    fp16 operands built straight from the packed bytes (codes and code - zp are exact in fp16);
-//    subtracting the zero-point while unpacking is the sum(Q) * zp correction folded in.
-//  * P^T is transposed in registers (movmatrix) into the B operand of O^T[D x 8] += (V - zp)^T P^T.
+//    Split-dot scores over the even and odd nibble streams: each code word is unpacked into the
+//    raw codes as exact fp16 integers (even codes through fp16 1024 + e, odd codes through
+//    1024 + 16 e, both brought back by one constant fp16x2 operation), and
+//    S^T[16 tokens x 8 columns] = Codes[16 x D] . Q'^T comes from mma.sync m16n8k16; the
+//    zero-point is then removed per key with the sum(Q') * zp correction.  (Leaving the 1024
+//    offsets in the mma operands saves the constant operations but costs the scores about 8 bits
+//    of fp32 accumulation precision, which heavy-tailed caches expose.)
+//  * P^T is transposed in registers (movmatrix) into the B operand of O^T[D x 8] += Codes_V^T P^T.
 //    V's per-key scale is folded into P (w = p * s'_V * 2^-E, E a running max exponent, so the
-//    fp16 weights never overflow); w and Q' are carried as fp16 high + low halves.
+//    fp16 weights never overflow); w and Q' are carried as fp16 high + low halves.  V's
+//    zero-points leave O through sum(w zp), kept per column alongside O.
 #include "attn_common.cuh"
 
 namespace kvi4 {
@@ -48,6 +53,10 @@ constexpr uint32_t kSmemPerSm = 233472;               // 228 KB of shared memory
 constexpr uint32_t kSmemPerCtaReserved = 1024;
 
 constexpr int kMaxHead = 128;
+// unpack_word operands that turn codes into exact fp16 integers: lo nibbles 1024 + e - 1024,
+// hi nibbles (1024 + 16 e) / 16 - 64
+constexpr uint32_t kCodeLo = 0x64006400u;   // (1024, 1024)
+constexpr uint32_t kCodeHi = 0xD400D400u;   // (-64, -64)
 
 // Ring depth and rows of a warp's query scratch.  With up to 4 query heads per kv head the
 // high and low halves pass through 4 rows one after the other, which leaves room for a fifth
@@ -382,7 +391,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     const bool lo_lane = !WIDE && t >= 2;   // this lane's P columns carry low halves
     uint32_t qb[Gm::KSTEPS][WIDE ? 4 : 2];
     const float lsc = p.c * p.softmax_scale * kLog2e;
-    float al0 = 0.0f, al1 = 0.0f;
+    float al0 = 0.0f, al1 = 0.0f;     // logit factor of columns hb, hb + 1
+    float qs0 = 0.0f, qs1 = 0.0f;     // sum(Q') of those columns (high + low halves as stored)
+    float WZ0 = 0.0f, WZ1 = 0.0f;     // sum(w zp) per column
     int run = -1, prev_seq = -1;
     bool stop = false;
 
@@ -434,6 +445,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             }
             al0 = 0.0f;
             al1 = 0.0f;
+            float qsum[NB];
 #pragma unroll
             for (int k = 0; k < NB; ++k) {
                 const int e = prescale_exponent(mx[k]);
@@ -441,6 +453,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 const float a = lsc * exp2i(-e);         // raw score -> log2-domain logit (before s'_K)
                 if (k == hb && k < G) al0 = a;
                 if (k == hb + 1 && k < G) al1 = a;
+                qsum[k] = 0.0f;                          // sum of the stored high + low halves
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    const float y = x[k][q] * mx[k];
+                    const float hi = __half2float(__float2half_rn(y));
+                    qsum[k] += hi + __half2float(__float2half_rn(y - hi));
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                for (int k = 0; k < NB; ++k) qsum[k] += __shfl_xor_sync(0xffffffffu, qsum[k], off);
+            }
+            qs0 = qs1 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                if (k == hb && k < G) qs0 = qsum[k];
+                if (k == hb + 1 && k < G) qs1 = qsum[k];
             }
             // Score-mma B fragments through the scratch: lane (g, t) feeds, for code word
             // W = t + 4 q of a key row (dims 8W .. 8W+7), the pairs (8W+2hh, 8W+2hh+4) and
@@ -513,6 +543,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         m1 = kNegBig;
         l0 = 0.0f;
         l1 = 0.0f;
+        WZ0 = WZ1 = 0.0f;
         eref = 0;
         const int li0 = ustart[j] - Bs;
         const int nbu = (u.w + kBlockSize - 1) / kBlockSize;
@@ -550,7 +581,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     kp[b] = ring + (size_t)st[b] * stage_bytes;
                     vp[b] = kp[b] + (size_t)kBlockSize * H * Gm::RB;
                 }
-                // ---- S^T = (K - zp) Q'^T for both blocks, high and low halves of Q'
+                // ---- scores Codes_K Q'^T for both blocks, high and low halves of Q'
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp[b] + (tk0 * H + h) * Gm::RB);
@@ -559,15 +590,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     float cl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     if (ok[b]) {
-                        const uint32_t z0l = zp_lo_half(ks0 & 15u), z0h = zp_hi_half(ks0 & 15u);
-                        const uint32_t z1l = zp_lo_half(ks1 & 15u), z1h = zp_hi_half(ks1 & 15u);
-                        const uint32_t zl0 = z0l | (z0l << 16), zh0 = z0h | (z0h << 16);
-                        const uint32_t zl1 = z1l | (z1l << 16), zh1 = z1h | (z1h << 16);
 #pragma unroll
                         for (int q = 0; q < Gm::KWPT; ++q) {
                             uint32_t a0[4], a1[4];
-                            unpack_word(kr0[t + 4 * q], zl0, zh0, a0);
-                            unpack_word(kr1[t + 4 * q], zl1, zh1, a1);
+                            unpack_word(kr0[t + 4 * q], kCodeLo, kCodeHi, a0);
+                            unpack_word(kr1[t + 4 * q], kCodeLo, kCodeHi, a1);
                             mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * q][0], qb[2 * q][1]);
                             mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][0], qb[2 * q + 1][1]);
                             if constexpr (WIDE) {
@@ -584,10 +611,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     const int tb = (k + b) * kBlockSize;   // token offset of this block in the unit
                     const bool v0 = ok[b] && tb + tk0 < u.w, v1 = ok[b] && tb + tk1 < u.w;
                     const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
-                    x[b][0] = v0 ? c[0] * sk0 * al0 : -INFINITY;
-                    x[b][1] = v0 ? c[1] * sk0 * al1 : -INFINITY;
-                    x[b][2] = v1 ? c[2] * sk1 * al0 : -INFINITY;
-                    x[b][3] = v1 ? c[3] * sk1 * al1 : -INFINITY;
+                    // score = S - zp sum(Q'), then the key's scale and the logit factor
+                    const float zk0 = (float)(ks0 & 15u), zk1 = (float)(ks1 & 15u);
+                    x[b][0] = v0 ? fmaf(-zk0, qs0, c[0]) * sk0 * al0 : -INFINITY;
+                    x[b][1] = v0 ? fmaf(-zk0, qs1, c[1]) * sk0 * al1 : -INFINITY;
+                    x[b][2] = v1 ? fmaf(-zk1, qs0, c[2]) * sk1 * al0 : -INFINITY;
+                    x[b][3] = v1 ? fmaf(-zk1, qs1, c[3]) * sk1 * al1 : -INFINITY;
                     const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp[b] + (tk0 * H + h) * Gm::RB);
                     const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp[b] + (tk1 * H + h) * Gm::RB);
                     vs0[b] = v0 ? vg0[Gm::KW] : 0u;   // invisible tokens: scale word 0 (exponent 0, weight 0)
@@ -634,18 +663,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         o[mt][2] *= f0;
                         o[mt][3] *= f1;
                     }
+                    WZ0 *= f0;
+                    WZ1 *= f1;
                 }
                 const float wsc = __uint_as_float((254u - eref) << 23);   // 2^(127 - eref)
-                // ---- O^T += (V - zp)^T P^T for both blocks
+                // ---- O^T += Codes_V^T P^T for both blocks
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     if (!ok[b]) continue;
                     const float sv0 = __uint_as_float(vs0[b] & 0xFFFFFFF0u) * wsc;
                     const float sv1 = __uint_as_float(vs1[b] & 0xFFFFFFF0u) * wsc;
                     // weights w = p * s'_V * 2^-E as fp16 high + low halves (invisible tokens: 0)
+                    const float wa0 = pr[b][0] * sv0, wa1 = pr[b][1] * sv0;   // token tk0
+                    const float wb0 = pr[b][2] * sv1, wb1 = pr[b][3] * sv1;   // token tk1
+                    const float zv0 = (float)(vs0[b] & 15u), zv1 = (float)(vs1[b] & 15u);
+                    WZ0 = fmaf(wa0, zv0, fmaf(wb0, zv1, WZ0));
+                    WZ1 = fmaf(wa1, zv0, fmaf(wb1, zv1, WZ1));
                     uint32_t xlo_h, xlo_l, xhi_h, xhi_l;
-                    split_f16x2(pr[b][0] * sv0, pr[b][1] * sv0, xlo_h, xlo_l);
-                    split_f16x2(pr[b][2] * sv1, pr[b][3] * sv1, xhi_h, xhi_l);
+                    split_f16x2(wa0, wa1, xlo_h, xlo_l);
+                    split_f16x2(wb0, wb1, xhi_h, xhi_l);
                     uint32_t bb0, bb1, bb0l = 0, bb1l = 0;
                     if constexpr (WIDE) {
                         bb0 = movmatrix_trans(xlo_h);
@@ -660,17 +696,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 4) * H + h) * Gm::RB);
                     const uint32_t* vr2 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 8) * H + h) * Gm::RB);
                     const uint32_t* vr3 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 12) * H + h) * Gm::RB);
-                    const uint32_t w0 = vr0[Gm::KW], w1 = vr1[Gm::KW], w2 = vr2[Gm::KW], w3 = vr3[Gm::KW];
-                    const uint32_t zl01 = zp_lo_half(w0 & 15u) | (zp_lo_half(w1 & 15u) << 16);
-                    const uint32_t zh01 = zp_hi_half(w0 & 15u) | (zp_hi_half(w1 & 15u) << 16);
-                    const uint32_t zl23 = zp_lo_half(w2 & 15u) | (zp_lo_half(w3 & 15u) << 16);
-                    const uint32_t zh23 = zp_hi_half(w2 & 15u) | (zp_hi_half(w3 & 15u) << 16);
                     if constexpr (D == 128) {
                         uint32_t ua[8], ubv[8], uc[8], ud[8];
-                        unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);            // d = 8g + i, tokens t, t+4
-                        unpack_word_pair(vr0[g + 8], vr1[g + 8], zl01, zh01, ubv);   // d = 64 + 8g + i
-                        unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);            // tokens t+8, t+12
-                        unpack_word_pair(vr2[g + 8], vr3[g + 8], zl23, zh23, ud);
+                        unpack_word_pair(vr0[g], vr1[g], kCodeLo, kCodeHi, ua);            // d = 8g + i, tokens t, t+4
+                        unpack_word_pair(vr0[g + 8], vr1[g + 8], kCodeLo, kCodeHi, ubv);   // d = 64 + 8g + i
+                        unpack_word_pair(vr2[g], vr3[g], kCodeLo, kCodeHi, uc);            // tokens t+8, t+12
+                        unpack_word_pair(vr2[g + 8], vr3[g + 8], kCodeLo, kCodeHi, ud);
 #pragma unroll
                         for (int mt = 0; mt < 8; ++mt) {
                             mma_f16_16816(o[mt], ua[mt], ubv[mt], uc[mt], ud[mt], bb0, bb1);
@@ -678,8 +709,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         }
                     } else {
                         uint32_t ua[8], uc[8];
-                        unpack_word_pair(vr0[g], vr1[g], zl01, zh01, ua);   // d = 8g + i
-                        unpack_word_pair(vr2[g], vr3[g], zl23, zh23, uc);
+                        unpack_word_pair(vr0[g], vr1[g], kCodeLo, kCodeHi, ua);   // d = 8g + i
+                        unpack_word_pair(vr2[g], vr3[g], kCodeLo, kCodeHi, uc);
 #pragma unroll
                         for (int mt = 0; mt < 4; ++mt) {
                             mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], bb0, bb1);
@@ -710,6 +741,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            WZ0 += __shfl_xor_sync(0xffffffffu, WZ0, off);
+            WZ1 += __shfl_xor_sync(0xffffffffu, WZ1, off);
         }
         if constexpr (!WIDE) {
 #pragma unroll
@@ -717,6 +750,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
             }
+        }
+        // O = sum(w code) - sum(w zp)
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            o[mt][0] -= WZ0;
+            o[mt][1] -= WZ1;
+            o[mt][2] -= WZ0;
+            o[mt][3] -= WZ1;
         }
         const float es = eref ? __uint_as_float(eref << 23) : 0.0f;   // 2^(eref - 127)
         const size_t recn = (size_t)u.z * kConsumerWarps + warp;
