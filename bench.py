@@ -183,7 +183,7 @@ def _gpu_arm(args):
     kv_bytes = int(wl.seq_lens.sum()) * 2 * H * rb
     qo_bytes = 2 * wl.query.numel() * wl.query.element_size()
     attn_bytes = kv_bytes + qo_bytes
-    launches_per_step = 1 + 3   # write; query rotation, segment walker, combine
+    launches_per_step = 3   # write; split-KV walker; combine
 
     def write(i):
         kv.kv_int4_write(t["k"], t["v"], t["slots"], t["signs"], caches[i % replicas])
