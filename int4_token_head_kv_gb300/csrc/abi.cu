@@ -127,11 +127,14 @@ int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int
     if (num_seqs < 0 || max_seq_len < 0 || segment_len < 0) return 0;
     if (segment_len > 0) return (segment_len % kBlockSize == 0) ? segment_len : 0;
     // About eight segments per walker CTA (two per SM) over the largest batch these sizes allow, so
-    // that the block-balanced split stays even when contexts are shorter than max_seq_len; a
-    // multiple of 32 tokens (whole block pairs), 32..4096.
+    // that the block-balanced split stays even when contexts are shorter than max_seq_len; four
+    // when a CTA's share is long (at least 64 blocks), where fewer partials pay more than the
+    // finer balance.  A multiple of 32 tokens (whole block pairs), 32..4096.
     const int64_t ctas = 2ll * num_sms();
     const int64_t work = (int64_t)num_seqs * (int64_t)max_seq_len;
-    int64_t seg = (work + 8 * ctas - 1) / (8 * ctas);
+    const int64_t per_cta = work / (ctas > 0 ? ctas : 1);
+    const int64_t k = per_cta >= 64 * kBlockSize ? 4 : 8;
+    int64_t seg = (work + k * ctas - 1) / (k * ctas);
     seg = ((seg + 31) / 32) * 32;
     if (seg < 32) seg = 32;
     if (seg > 4096) seg = 4096;

@@ -587,26 +587,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp[b] + (tk0 * H + h) * Gm::RB);
                     const uint32_t* kr1 = reinterpret_cast<const uint32_t*>(kp[b] + (tk1 * H + h) * Gm::RB);
                     const uint32_t ks0 = kr0[Gm::KW], ks1 = kr1[Gm::KW];
+                    // two independent accumulation chains per block: the high- and low-half tiles
+                    // when G = 8, the two halves of each code word otherwise
                     float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    float cl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    float c2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     if (ok[b]) {
 #pragma unroll
                         for (int q = 0; q < Gm::KWPT; ++q) {
                             uint32_t a0[4], a1[4];
                             unpack_word(kr0[t + 4 * q], kCodeLo, kCodeHi, a0);
                             unpack_word(kr1[t + 4 * q], kCodeLo, kCodeHi, a1);
-                            mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * q][0], qb[2 * q][1]);
-                            mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][0], qb[2 * q + 1][1]);
                             if constexpr (WIDE) {
-                                mma_f16_16816(cl, a0[0], a1[0], a0[1], a1[1], qb[2 * q][2], qb[2 * q][3]);
-                                mma_f16_16816(cl, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][2], qb[2 * q + 1][3]);
+                                mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * q][0], qb[2 * q][1]);
+                                mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][0], qb[2 * q + 1][1]);
+                                mma_f16_16816(c2, a0[0], a1[0], a0[1], a1[1], qb[2 * q][2], qb[2 * q][3]);
+                                mma_f16_16816(c2, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][2], qb[2 * q + 1][3]);
+                            } else {
+                                mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * q][0], qb[2 * q][1]);
+                                mma_f16_16816(c2, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][0], qb[2 * q + 1][1]);
                             }
                         }
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        if constexpr (WIDE) c[e] += cl[e];
-                        else c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);   // high + low columns
+                        c[e] += c2[e];
+                        if constexpr (!WIDE) c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);   // high + low columns
                     }
                     const int tb = (k + b) * kBlockSize;   // token offset of this block in the unit
                     const bool v0 = ok[b] && tb + tk0 < u.w, v1 = ok[b] && tb + tk1 < u.w;
