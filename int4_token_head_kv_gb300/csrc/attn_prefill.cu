@@ -4,16 +4,17 @@
 // test_triton_unified_attention_per_token_head_scale).
 //
 // One CTA per (query tile, kv head, sequence): 128 rows = (128 / G) query tokens x G query heads
-// of that kv head, 16 rows per warp.  Each warp walks the key blocks its rows can see (causal),
-// builds fp16 fragments of K - zp and V - zp directly from the packed bytes (read through L1, the
-// next block prefetched into registers), and runs
-//   S = Q' (K - zp)^T      mma.sync m16n8k16, Q' = rotated, power-of-two-prescaled queries as
-//                          fp16 high + low halves (two mma per step)
+// of that kv head, 16 rows per warp.  The CTA walks the key blocks its rows can see (causal) once:
+// all 256 threads dequantise a 16-token block into fp16 tiles K - zp and V - zp in shared memory
+// (exact integers, natural dimension order, rows padded so that ldmatrix is bank-conflict free),
+// double-buffered with one barrier per block, the codes of the block after next already in
+// flight.  Each warp then runs, for its 16 rows,
+//   S = Q' (K - zp)^T      mma.sync m16n8k16, B fragments by ldmatrix, Q' = rotated,
+//                          power-of-two-prescaled queries as fp16 high + low halves
 //   online softmax with the per-key scale s'_K and the causal mask
 //   O += P_w (V - zp)      P_w = p * s'_V * 2^-E as fp16 high + low halves, straight from S's
-//                          accumulator registers
-// and un-rotates its rows at the end.  The fragment layouts are the decode kernel's with the
-// operand roles swapped (queries on the M side, keys on N).
+//                          accumulator registers; V fragments by ldmatrix.trans
+// and un-rotates its rows at the end.
 #include "attn_common.cuh"
 
 namespace kvi4 {
@@ -24,47 +25,40 @@ constexpr int kPrefillThreads = kPrefillWarps * 32;
 constexpr int kRows = kPrefillWarps * 16;
 
 template <int D>
-struct BlockWords {
-    uint32_t k0[Geo<D>::KWPT], k1[Geo<D>::KWPT];   // code words of key rows tau(g), tau(g+8)
-    uint32_t ks0, ks1;                             // their scale words
-    uint32_t kc[4];                                // K scale words of tokens t, t+4, t+8, t+12
-    uint32_t vw[4][D == 128 ? 2 : 1];              // V code words (g[, g+8]) of those tokens
-    uint32_t vs[4];                                // their V scale words
-    int ok;
+struct PrefillSmem {
+    static constexpr int kTileStride = D + 8;                                 // halves per tile row
+    static constexpr int kTileHalves = kBlockSize * kTileStride;              // one 16-token tile
+    static constexpr size_t kStage = (size_t)kRows * D * 4;                   // q halves / output rows
+    static constexpr size_t kQlf = (size_t)kPrefillWarps * (D / 16) * 32 * 16;
+    static constexpr size_t kTiles = 2 * 2 * kTileHalves * 2;                 // [buf][plane] fp16 tiles
+    static constexpr size_t kScales = 2 * 2 * kBlockSize * 4 + 16;            // [buf][plane] scale words + flags
+    static constexpr size_t kBytes = kStage + kQlf + kTiles + kScales + kRows * 4 + D * 4;
 };
 
-template <int D>
-__device__ __forceinline__ void load_block(BlockWords<D>& b, const uint8_t* cache, int64_t blk, int H, int h, int g,
-                                           int t) {
-    using Gm = Geo<D>;
-    const int64_t plane_stride = (int64_t)kBlockSize * H * Gm::RB;
-    const uint8_t* kp = cache + blk * 2 * plane_stride + (int64_t)h * Gm::RB;
-    const uint8_t* vp = kp + plane_stride;
-    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(kp + (int64_t)block_token(g) * H * Gm::RB);
-    const uint32_t* r1 = reinterpret_cast<const uint32_t*>(kp + (int64_t)block_token(g + 8) * H * Gm::RB);
-#pragma unroll
-    for (int j = 0; j < Gm::KWPT; ++j) {
-        b.k0[j] = __ldg(r0 + t + 4 * j);
-        b.k1[j] = __ldg(r1 + t + 4 * j);
-    }
-    b.ks0 = __ldg(r0 + Gm::KW);
-    b.ks1 = __ldg(r1 + Gm::KW);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int tok = t + 4 * c;
-        const uint32_t* kr = reinterpret_cast<const uint32_t*>(kp + (int64_t)tok * H * Gm::RB);
-        const uint32_t* vr = reinterpret_cast<const uint32_t*>(vp + (int64_t)tok * H * Gm::RB);
-        b.kc[c] = __ldg(kr + Gm::KW);
-        b.vs[c] = __ldg(vr + Gm::KW);
-        b.vw[c][0] = __ldg(vr + g);
-        if constexpr (D == 128) b.vw[c][1] = __ldg(vr + g + 8);
-    }
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(row)));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(row)));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
 }
 
 template <int D, typename QT, typename OT>
 __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __grid_constant__ AttnParams p) {
     using Gm = Geo<D>;
-    constexpr int NT = 2 * Gm::MT;   // 8-wide output tiles over the head dimension
+    using Sm = PrefillSmem<D>;
+    constexpr int NT = D / 8;          // 8-wide output tiles over the head dimension
+    constexpr int KS = D / 16;         // 16-deep k-steps over the head dimension
+    constexpr int TS = Sm::kTileStride;
+    constexpr int WPP = kBlockSize * Gm::KW;   // code words of one plane of one block (one head)
     extern __shared__ __align__(128) uint8_t smem[];
     const int qtile = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
     const int q0 = __ldg(p.qsl + seq);
@@ -86,12 +80,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     }
     const int pos0 = L - qlen;   // position of query token 0
 
-    float* ostage = reinterpret_cast<float*>(smem);                         // [128][D] fp32 (epilogue)
-    __half* qh = reinterpret_cast<__half*>(smem);                           // [128][D] fp16 (prologue)
-    __half* ql = qh + kRows * D;                                            // [128][D] fp16 (prologue)
-    uint4* qlf = reinterpret_cast<uint4*>(smem + (size_t)kRows * D * 4);    // [warps][KSTEPS][32] low-half A fragments
-    float* alpha = reinterpret_cast<float*>(qlf + kPrefillWarps * Gm::KSTEPS * 32);   // [128]
-    float* sgn = alpha + kRows;                                             // [D]
+    float* ostage = reinterpret_cast<float*>(smem);                               // [128][D] fp32 (epilogue)
+    __half* qh = reinterpret_cast<__half*>(smem);                                 // [128][D] fp16 (prologue)
+    __half* ql = qh + kRows * D;                                                  // [128][D] fp16 (prologue)
+    uint4* qlf = reinterpret_cast<uint4*>(smem + Sm::kStage);                     // [warps][KS][32] low-half A fragments
+    __half* tiles = reinterpret_cast<__half*>(smem + Sm::kStage + Sm::kQlf);      // [buf][plane][16][TS]
+    uint32_t* scalew = reinterpret_cast<uint32_t*>(smem + Sm::kStage + Sm::kQlf + Sm::kTiles);   // [buf][plane][16]
+    int* tile_ok = reinterpret_cast<int*>(scalew + 2 * 2 * kBlockSize);          // [buf]
+    float* alpha = reinterpret_cast<float*>(smem + Sm::kStage + Sm::kQlf + Sm::kTiles + Sm::kScales);   // [128]
+    float* sgn = alpha + kRows;                                                   // [D]
     for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
     __syncthreads();
 
@@ -109,100 +106,141 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
         }
     }
     __syncwarp();
+    // A fragments of the rows (natural dimension order): a0 = (row g, k 2t..2t+1), a1 = (g+8, ..),
+    // a2 = (g, k 2t+8..2t+9), a3 = (g+8, ..) of each 16-deep k-step
     const int g = lane >> 2, t = lane & 3;
     const int Rg = warp * 16 + g, Rg8 = Rg + 8;
-    uint32_t qa[Gm::KSTEPS][4];
+    uint32_t qa[KS][4];
 #pragma unroll
-    for (int j = 0; j < Gm::KWPT; ++j) {
-        const int W = t + 4 * j;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int d0 = 8 * W + 2 * hh;
-            __half2 a0 = __halves2half2(qh[Rg * D + d0], qh[Rg * D + d0 + 4]);
-            __half2 a1 = __halves2half2(qh[Rg8 * D + d0], qh[Rg8 * D + d0 + 4]);
-            __half2 a2 = __halves2half2(qh[Rg * D + d0 + 1], qh[Rg * D + d0 + 5]);
-            __half2 a3 = __halves2half2(qh[Rg8 * D + d0 + 1], qh[Rg8 * D + d0 + 5]);
-            qa[2 * j + hh][0] = *reinterpret_cast<uint32_t*>(&a0);
-            qa[2 * j + hh][1] = *reinterpret_cast<uint32_t*>(&a1);
-            qa[2 * j + hh][2] = *reinterpret_cast<uint32_t*>(&a2);
-            qa[2 * j + hh][3] = *reinterpret_cast<uint32_t*>(&a3);
-            // the low halves go to a fragment-ordered area read once per k-step in the main loop
-            __half2 l0 = __halves2half2(ql[Rg * D + d0], ql[Rg * D + d0 + 4]);
-            __half2 l1 = __halves2half2(ql[Rg8 * D + d0], ql[Rg8 * D + d0 + 4]);
-            __half2 l2 = __halves2half2(ql[Rg * D + d0 + 1], ql[Rg * D + d0 + 5]);
-            __half2 l3 = __halves2half2(ql[Rg8 * D + d0 + 1], ql[Rg8 * D + d0 + 5]);
-            qlf[(warp * Gm::KSTEPS + 2 * j + hh) * 32 + lane] =
-                make_uint4(*reinterpret_cast<uint32_t*>(&l0), *reinterpret_cast<uint32_t*>(&l1),
-                           *reinterpret_cast<uint32_t*>(&l2), *reinterpret_cast<uint32_t*>(&l3));
-        }
+    for (int kk = 0; kk < KS; ++kk) {
+        const int d0 = 16 * kk + 2 * t;
+        qa[kk][0] = pack_h2(qh[Rg * D + d0], qh[Rg * D + d0 + 1]);
+        qa[kk][1] = pack_h2(qh[Rg8 * D + d0], qh[Rg8 * D + d0 + 1]);
+        qa[kk][2] = pack_h2(qh[Rg * D + d0 + 8], qh[Rg * D + d0 + 9]);
+        qa[kk][3] = pack_h2(qh[Rg8 * D + d0 + 8], qh[Rg8 * D + d0 + 9]);
+        // the low halves go to a fragment-ordered area read once per k-step in the main loop
+        qlf[(warp * KS + kk) * 32 + lane] =
+            make_uint4(pack_h2(ql[Rg * D + d0], ql[Rg * D + d0 + 1]), pack_h2(ql[Rg8 * D + d0], ql[Rg8 * D + d0 + 1]),
+                       pack_h2(ql[Rg * D + d0 + 8], ql[Rg * D + d0 + 9]),
+                       pack_h2(ql[Rg8 * D + d0 + 8], ql[Rg8 * D + d0 + 9]));
     }
-    const uint4* my_qlf = qlf + warp * Gm::KSTEPS * 32 + lane;
+    const uint4* my_qlf = qlf + warp * KS * 32 + lane;
     const float al_g = alpha[Rg], al_g8 = alpha[Rg8];
     const int qt_g = qt0 + Rg / G, qt_g8 = qt0 + Rg8 / G;
     const int lim_g = qt_g < qlen ? pos0 + qt_g : -1;     // last visible key of each row
     const int lim_g8 = qt_g8 < qlen ? pos0 + qt_g8 : -1;
-    __syncthreads();   // qh is dead from here on; the region becomes the output stage
+    const int lim_w = max(lim_g, lim_g8);
 
-    // keys this warp needs: up to the largest visible position among its rows
+    // keys this warp needs (up to the largest visible position among its rows) and the CTA
     const int last_qt = min(qlen - 1, qt0 + (warp * 16 + 15) / G);
     const int warp_lim = (qt0 + (warp * 16) / G < qlen) ? min(pos0 + last_qt, L - 1) : -1;
     const int nkb = warp_lim >= 0 ? warp_lim / kBlockSize + 1 : 0;
+    const int cta_lim = min(pos0 + min(qlen - 1, qt0 + (kRows - 1) / G), L - 1);
+    const int nkb_cta = cta_lim >= 0 ? cta_lim / kBlockSize + 1 : 0;
+
+    // ---- cooperative dequantisation: codes of block kb in flight in registers, then into tiles
+    const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+    constexpr int kWordsPerThread = (2 * WPP + kPrefillThreads - 1) / kPrefillThreads;
+    uint32_t cw[kWordsPerThread], sw[kWordsPerThread];
+    int cur_ok = 0;
+    auto fetch = [&](int kb) {   // this thread's code and scale words of block kb
+        const int blk = __ldg(table + kb);
+        cur_ok = blk >= 0 && (int64_t)blk < p.num_blocks;
+#pragma unroll
+        for (int u = 0; u < kWordsPerThread; ++u) {
+            const int i = threadIdx.x + u * kPrefillThreads;
+            cw[u] = 0u;
+            sw[u] = 0u;
+            if (i < 2 * WPP && cur_ok) {
+                const int plane = i / WPP, tok = (i / Gm::KW) % kBlockSize, w = i % Gm::KW;
+                const uint32_t* row = reinterpret_cast<const uint32_t*>(
+                    p.cache + (((int64_t)blk * 2 + plane) * kBlockSize + tok) * H * Gm::RB + (int64_t)h * Gm::RB);
+                cw[u] = __ldg(row + w);
+                sw[u] = __ldg(row + Gm::KW);
+            }
+        }
+    };
+    auto dequant = [&](int buf) {   // the fetched words -> fp16 (code - zp) in natural order
+#pragma unroll
+        for (int u = 0; u < kWordsPerThread; ++u) {
+            const int i = threadIdx.x + u * kPrefillThreads;
+            if (i < 2 * WPP) {
+                const int plane = i / WPP, tok = (i / Gm::KW) % kBlockSize, w = i % Gm::KW;
+                const uint32_t zp = sw[u] & 15u;
+                const uint32_t zl = zp_lo_half(zp) * 0x10001u, zh = zp_hi_half(zp) * 0x10001u;
+                uint32_t o[4];
+                unpack_word(cw[u], zl, zh, o);   // (e0,e4) (e1,e5) (e2,e6) (e3,e7)
+                uint4 v;
+                v.x = prmt(o[0], o[1], 0x5410u);   // (e0, e1)
+                v.y = prmt(o[2], o[3], 0x5410u);   // (e2, e3)
+                v.z = prmt(o[0], o[1], 0x7632u);   // (e4, e5)
+                v.w = prmt(o[2], o[3], 0x7632u);   // (e6, e7)
+                *reinterpret_cast<uint4*>(tiles + ((buf * 2 + plane) * kBlockSize + tok) * TS + 8 * w) = v;
+                if (w == 0) scalew[(buf * 2 + plane) * kBlockSize + tok] = sw[u];
+            }
+        }
+        if (threadIdx.x == 0) {
+            tile_ok[buf] = cur_ok;
+            if (!cur_ok) count_status(p.status, 1);
+        }
+    };
 
     float o[NT][4];
 #pragma unroll
     for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float m_g = kNegBig, m_g8 = kNegBig, l_g = 0.0f, l_g8 = 0.0f;
     uint32_t eref = 0;
-    const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
 
-    BlockWords<D> cur, nxt;
-    auto fetch = [&](BlockWords<D>& b, int kb) {
-        const int blk = __ldg(table + kb);
-        b.ok = blk >= 0 && (int64_t)blk < p.num_blocks;
-        if (b.ok) load_block<D>(b, p.cache, blk, H, h, g, t);
-        else if (lane == 0) count_status(p.status, 1);
-    };
-    if (nkb > 0) fetch(cur, 0);
-    for (int kb = 0; kb < nkb; ++kb) {
-        if (kb + 1 < nkb) fetch(nxt, kb + 1);
-        if (cur.ok) {
-            // ---- S = Q' (K - zp)^T over 16 keys (two 8-key tiles)
+    __syncthreads();   // the q halves are consumed; the tiles area was never part of them
+    if (nkb_cta > 0) {
+        fetch(0);
+        dequant(0);
+        if (nkb_cta > 1) fetch(1);
+    }
+    __syncthreads();
+    // ldmatrix row addresses: lane l serves row l % 8 of matrix l / 8
+    const int lm = lane >> 3, lr = lane & 7;
+    for (int kb = 0; kb < nkb_cta; ++kb) {
+        const int buf = kb & 1;
+        if (kb < nkb && tile_ok[buf]) {
+            const __half* kt = tiles + (buf * 2 + 0) * kBlockSize * TS;
+            const __half* vt = tiles + (buf * 2 + 1) * kBlockSize * TS;
+            const uint32_t* kscale = scalew + (buf * 2 + 0) * kBlockSize;
+            const uint32_t* vscale = scalew + (buf * 2 + 1) * kBlockSize;
+            // ---- S = Q' (K - zp)^T over 16 keys (two 8-key tiles); matrices: keys 0-7 / 8-15 x
+            // dims +0 / +8 of the k-step
+            // (high and low halves accumulate separately: four independent mma chains)
             float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
-                const uint32_t z0l = zp_lo_half(cur.ks0 & 15u), z0h = zp_hi_half(cur.ks0 & 15u);
-                const uint32_t z1l = zp_lo_half(cur.ks1 & 15u), z1h = zp_hi_half(cur.ks1 & 15u);
-                const uint32_t zl0 = z0l | (z0l << 16), zh0 = z0h | (z0h << 16);
-                const uint32_t zl1 = z1l | (z1l << 16), zh1 = z1h | (z1h << 16);
+            float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const __half* krow = kt + ((lm >> 1) * 8 + lr) * TS + (lm & 1) * 8;
 #pragma unroll
-                for (int j = 0; j < Gm::KWPT; ++j) {
-                    uint32_t b0[4], b1[4];
-                    unpack_word(cur.k0[j], zl0, zh0, b0);
-                    unpack_word(cur.k1[j], zl1, zh1, b1);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const uint32_t* a = qa[2 * j + hh];
-                        const uint4 al = my_qlf[(2 * j + hh) * 32];
-                        mma_f16_16816(s[0], a[0], a[1], a[2], a[3], b0[2 * hh], b0[2 * hh + 1]);
-                        mma_f16_16816(s[1], a[0], a[1], a[2], a[3], b1[2 * hh], b1[2 * hh + 1]);
-                        mma_f16_16816(s[0], al.x, al.y, al.z, al.w, b0[2 * hh], b0[2 * hh + 1]);
-                        mma_f16_16816(s[1], al.x, al.y, al.z, al.w, b1[2 * hh], b1[2 * hh + 1]);
-                    }
-                }
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t b[4];
+                ldmatrix_x4(b, krow + 16 * kk);
+                const uint4 al = my_qlf[kk * 32];
+                mma_f16_16816(s[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b[0], b[1]);
+                mma_f16_16816(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b[2], b[3]);
+                mma_f16_16816(sl[0], al.x, al.y, al.z, al.w, b[0], b[1]);
+                mma_f16_16816(sl[1], al.x, al.y, al.z, al.w, b[2], b[3]);
             }
-            // ---- logits, causal mask, online softmax over rows g and g+8
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] += sl[nt][e];
+            }
+            // ---- logits, causal mask, online softmax over rows g and g+8; s[nt][e] is key
+            // 8 nt + 2t + (e & 1) of row g (e < 2) or g + 8
             const int kbase = kb * kBlockSize;
             float x[2][4];
-            float sk[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) sk[c] = __uint_as_float(cur.kc[c] & 0xFFFFFFF0u);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int c = 2 * nt + e;            // key token t + 4c
-                    const int key = kbase + t + 4 * c;
-                    x[nt][e] = key <= lim_g ? s[nt][e] * sk[c] * al_g : -INFINITY;
-                    x[nt][2 + e] = key <= lim_g8 ? s[nt][2 + e] * sk[c] * al_g8 : -INFINITY;
+                    const int kt_ = 8 * nt + 2 * t + e;
+                    const int key = kbase + kt_;
+                    const float sk = __uint_as_float(kscale[kt_] & 0xFFFFFFF0u);
+                    x[nt][e] = key <= lim_g ? s[nt][e] * sk * al_g : -INFINITY;
+                    x[nt][2 + e] = key <= lim_g8 ? s[nt][2 + e] * sk * al_g8 : -INFINITY;
                 }
             }
             float bm_g = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -226,12 +264,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
             }
             l_g = l_g * r_g + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
             l_g8 = l_g8 * r_g8 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
-            // ---- V scale exponent reference (keys a row cannot see contribute nothing)
+            // ---- V scale exponent reference over this lane's keys a row of the warp can see
+            // (keys no row can see may sit in never-written slots: keep their words out)
+            uint32_t svw[4];
             uint32_t emax = 0;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int key = kbase + t + 4 * c;
-                if (key <= max(lim_g, lim_g8)) emax = max(emax, (cur.vs[c] >> 23) & 0xFFu);
+                const int kt_ = 2 * t + (c & 1) + 8 * (c >> 1);   // keys 2t, 2t+1, 2t+8, 2t+9
+                svw[c] = kbase + kt_ <= lim_w ? vscale[kt_] : 0u;
+                emax = max(emax, (svw[c] >> 23) & 0xFFu);
             }
             const uint32_t eblk = __reduce_max_sync(0xffffffffu, emax);
             float escale = 1.0f;
@@ -250,51 +291,32 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
                 }
             }
             const float wsc = __uint_as_float((254u - eref) << 23);
-            // keys no row of this thread can see may sit in never-written slots: keep their
-            // (possibly NaN) scale words out of the products
             float sv[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                sv[c] = (kbase + t + 4 * c <= max(lim_g, lim_g8)) ? __uint_as_float(cur.vs[c] & 0xFFFFFFF0u) * wsc : 0.0f;
-            // P_w as the A operand (C layout of two 8-key tiles == A layout of one 16-key tile)
-            // (high and low fp16 halves, as for the queries)
+            for (int c = 0; c < 4; ++c) sv[c] = __uint_as_float(svw[c] & 0xFFFFFFF0u) * wsc;
+            // P_w as the A operand (C layout of two 8-key tiles == A layout of one 16-key tile),
+            // high and low fp16 halves as for the queries
             uint32_t pa0, pa1, pa2, pa3, pl0, pl1, pl2, pl3;
-            split_f16x2(pr[0][0] * sv[0], pr[0][1] * sv[1], pa0, pl0);
-            split_f16x2(pr[0][2] * sv[0], pr[0][3] * sv[1], pa1, pl1);
-            split_f16x2(pr[1][0] * sv[2], pr[1][1] * sv[3], pa2, pl2);
-            split_f16x2(pr[1][2] * sv[2], pr[1][3] * sv[3], pa3, pl3);
-            // ---- O += P_w (V - zp)
-            const uint32_t zl01 = zp_lo_half(cur.vs[0] & 15u) | (zp_lo_half(cur.vs[1] & 15u) << 16);
-            const uint32_t zh01 = zp_hi_half(cur.vs[0] & 15u) | (zp_hi_half(cur.vs[1] & 15u) << 16);
-            const uint32_t zl23 = zp_lo_half(cur.vs[2] & 15u) | (zp_lo_half(cur.vs[3] & 15u) << 16);
-            const uint32_t zh23 = zp_hi_half(cur.vs[2] & 15u) | (zp_hi_half(cur.vs[3] & 15u) << 16);
-            if constexpr (D == 128) {
-                uint32_t ua[8], ub[8], uc[8], ud[8];
-                unpack_word_pair(cur.vw[0][0], cur.vw[1][0], zl01, zh01, ua);   // d = 8g' + i, keys t, t+4
-                unpack_word_pair(cur.vw[0][1], cur.vw[1][1], zl01, zh01, ub);   // d = 64 + 8g' + i
-                unpack_word_pair(cur.vw[2][0], cur.vw[3][0], zl23, zh23, uc);   // keys t+8, t+12
-                unpack_word_pair(cur.vw[2][1], cur.vw[3][1], zl23, zh23, ud);
+            split_f16x2(pr[0][0] * sv[0], pr[0][1] * sv[1], pa0, pl0);   // row g, keys 2t, 2t+1
+            split_f16x2(pr[0][2] * sv[0], pr[0][3] * sv[1], pa1, pl1);   // row g+8
+            split_f16x2(pr[1][0] * sv[2], pr[1][1] * sv[3], pa2, pl2);   // row g, keys 2t+8, 2t+9
+            split_f16x2(pr[1][2] * sv[2], pr[1][3] * sv[3], pa3, pl3);   // row g+8
+            // ---- O += P_w (V - zp); matrices: keys 0-7 / 8-15 x dims +0 / +8, transposed
+            const __half* vrow = vt + ((lm & 1) * 8 + lr) * TS + (lm >> 1) * 8;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    mma_f16_16816(o[i], pa0, pa1, pa2, pa3, ua[i], uc[i]);
-                    mma_f16_16816(o[8 + i], pa0, pa1, pa2, pa3, ub[i], ud[i]);
-                    mma_f16_16816(o[i], pl0, pl1, pl2, pl3, ua[i], uc[i]);
-                    mma_f16_16816(o[8 + i], pl0, pl1, pl2, pl3, ub[i], ud[i]);
-                }
-            } else {
-                uint32_t ua[8], uc[8];
-                unpack_word_pair(cur.vw[0][0], cur.vw[1][0], zl01, zh01, ua);
-                unpack_word_pair(cur.vw[2][0], cur.vw[3][0], zl23, zh23, uc);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    mma_f16_16816(o[i], pa0, pa1, pa2, pa3, ua[i], uc[i]);
-                    mma_f16_16816(o[4 + i], pa0, pa1, pa2, pa3, ua[4 + i], uc[4 + i]);
-                    mma_f16_16816(o[i], pl0, pl1, pl2, pl3, ua[i], uc[i]);
-                    mma_f16_16816(o[4 + i], pl0, pl1, pl2, pl3, ua[4 + i], uc[4 + i]);
-                }
+            for (int nd = 0; nd < KS; ++nd) {
+                uint32_t b[4];
+                ldmatrix_x4_trans(b, vrow + 16 * nd);
+                mma_f16_16816(o[2 * nd], pa0, pa1, pa2, pa3, b[0], b[1]);
+                mma_f16_16816(o[2 * nd + 1], pa0, pa1, pa2, pa3, b[2], b[3]);
+                mma_f16_16816(o[2 * nd], pl0, pl1, pl2, pl3, b[0], b[1]);
+                mma_f16_16816(o[2 * nd + 1], pl0, pl1, pl2, pl3, b[2], b[3]);
             }
         }
-        if (kb + 1 < nkb) cur = nxt;
+        // the next block's tiles, then the codes of the block after it
+        if (kb + 1 < nkb_cta) dequant(buf ^ 1);
+        if (kb + 2 < nkb_cta) fetch(kb + 2);
+        __syncthreads();
     }
 
     // ---- epilogue: normalise, stage rows, un-rotate and store
@@ -307,14 +329,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     const float sc_g = l_g > 0.0f ? es / l_g : 0.0f, sc_g8 = l_g8 > 0.0f ? es / l_g8 : 0.0f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        // tile nt covers d = base + 8 n' for n' = 0..7 (base = mt or 64 + mt, D=64: mt or 4 + mt)
-        const int mt = nt % Gm::MT, half = nt / Gm::MT;
-        const int base = (D == 128) ? (half ? 64 + mt : mt) : (half ? 4 + mt : mt);
-        const int d0 = base + 8 * (2 * t), d1 = base + 8 * (2 * t + 1);
+        const int d0 = 8 * nt + 2 * t;
         ostage[Rg * D + d0] = o[nt][0] * sc_g;
-        ostage[Rg * D + d1] = o[nt][1] * sc_g;
+        ostage[Rg * D + d0 + 1] = o[nt][1] * sc_g;
         ostage[Rg8 * D + d0] = o[nt][2] * sc_g8;
-        ostage[Rg8 * D + d1] = o[nt][3] * sc_g8;
+        ostage[Rg8 * D + d0 + 1] = o[nt][3] * sc_g8;
     }
     __syncwarp();
     for (int r = 0; r < 16; ++r) {
@@ -330,7 +349,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
 
 template <int D, typename QT, typename OT>
 cudaError_t launch_prefill_t(const AttnParams& p, int max_query_len, cudaStream_t stream) {
-    const size_t smem = (size_t)kRows * D * 4 + (size_t)kPrefillWarps * Geo<D>::KSTEPS * 32 * 16 + kRows * 4 + D * 4;
+    const size_t smem = PrefillSmem<D>::kBytes;
     auto kern = prefill_kernel<D, QT, OT>;
     cudaError_t err = opt_in_smem<prefill_kernel<D, QT, OT>>(smem);
     if (err != cudaSuccess) return err;
