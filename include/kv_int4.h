@@ -112,9 +112,8 @@ size_t kv_int4_attention_workspace_bytes(int32_t num_q_heads, int32_t num_kv_hea
 
 /*
  * The KV-token length of one split-KV segment that kv_int4_paged_attention uses for these sizes
- * (segment_len 0 = the library's choice: about eight segments per resident CTA over
- * num_seqs * max_seq_len tokens, four when that is at least 1024 tokens per CTA; a multiple of 32
- * in 32..4096; otherwise segment_len itself).
+ * (segment_len 0 = the library's choice: about four segments per resident CTA over
+ * num_seqs * max_seq_len tokens, a multiple of 32 in 32..4096; otherwise segment_len itself).
  * 0 if invalid.
  */
 int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len);

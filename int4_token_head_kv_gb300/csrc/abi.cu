@@ -126,15 +126,12 @@ kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, 
 int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
     if (num_seqs < 0 || max_seq_len < 0 || segment_len < 0) return 0;
     if (segment_len > 0) return (segment_len % kBlockSize == 0) ? segment_len : 0;
-    // About eight segments per walker CTA (two per SM) over the largest batch these sizes allow, so
-    // that the block-balanced split stays even when contexts are shorter than max_seq_len; four
-    // when a CTA's share is long (at least 64 blocks), where fewer partials pay more than the
-    // finer balance.  A multiple of 32 tokens (whole block pairs), 32..4096.
+    // About four segments per walker CTA (two per SM) over the largest batch these sizes allow: finer
+    // segments balance the block split better but every segment costs a partial to write and to
+    // merge.  A multiple of 32 tokens (whole block pairs), 32..4096.
     const int64_t ctas = 2ll * num_sms();
     const int64_t work = (int64_t)num_seqs * (int64_t)max_seq_len;
-    const int64_t per_cta = work / (ctas > 0 ? ctas : 1);
-    const int64_t k = per_cta >= 64 * kBlockSize ? 4 : 8;
-    int64_t seg = (work + k * ctas - 1) / (k * ctas);
+    int64_t seg = (work + 4 * ctas - 1) / (4 * ctas);
     seg = ((seg + 31) / 32) * 32;
     if (seg < 32) seg = 32;
     if (seg > 4096) seg = 4096;
@@ -147,15 +144,12 @@ namespace {
 
 // Workspace of the decode path, in 256-byte-aligned regions:
 //   meta  [num_seqs + 1] int32             first unit of each sequence
-//   cnt   [num_seqs, H] int32              combine chunks finished
 //   po    [units, 8, po_floats]            unnormalised partial outputs
 //   pml   [units, 8, 16] fp32              partial (max, sum) per column
-//   cp    [num_seqs, H, chunks, cp_floats] combine chunk partials
-// units <= num_seqs * ceil(max_seq_len / segment_len); a (sequence, kv head) has at most
-// chunks = ceil(ceil(max_seq_len / segment_len) * (8 / H) / 8) combine chunks.
+// units <= num_seqs * ceil(max_seq_len / segment_len).
 struct WsLayout {
-    size_t meta, cnt, po, pml, cp, total;
-    int64_t chunks;
+    size_t meta, po, pml, total;
+    int64_t records;   // most partial records of one (sequence, kv head)
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -167,16 +161,11 @@ bool ws_layout(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int
     const int G = num_q_heads / num_kv_heads;
     const int64_t seg_per_seq = ((int64_t)max_seq_len + seg - 1) / seg;
     const int64_t max_units = (int64_t)num_seqs * seg_per_seq;
-    const int64_t recs = seg_per_seq * (8 / num_kv_heads);
-    w->chunks = recs > 0 ? (recs + kDecodeChunkRecords - 1) / kDecodeChunkRecords : 1;
+    w->records = seg_per_seq * (8 / num_kv_heads);
     w->meta = 0;
-    w->cnt = align256((size_t)(num_seqs + 1) * 4);
-    w->po = w->cnt + align256((size_t)num_seqs * num_kv_heads * 4);
+    w->po = align256((size_t)(num_seqs + 1) * 4);
     w->pml = w->po + align256((size_t)max_units * 8 * decode_po_floats(head_size, G) * 4);
-    w->cp = w->pml + align256((size_t)max_units * 8 * 16 * 4);
-    const size_t cp_bytes =
-        w->chunks > 1 ? (size_t)num_seqs * num_kv_heads * w->chunks * decode_cp_floats(head_size, G) * 4 : 0;
-    w->total = w->cp + cp_bytes;
+    w->total = w->pml + (size_t)max_units * 8 * 16 * 4;
     return true;
 }
 
@@ -240,15 +229,16 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     p.out = out;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.ws_meta = reinterpret_cast<int32_t*>(ws + w.meta);
-    p.ws_cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
     p.ws_po = reinterpret_cast<float*>(ws + w.po);
     p.ws_pml = reinterpret_cast<float*>(ws + w.pml);
-    p.ws_cp = reinterpret_cast<float*>(ws + w.cp);
-    p.combine_chunks = (int)w.chunks;
+    {   // warps per (sequence, kv head) in the combine: about one per four records, 1..16
+        int cw = 1;
+        while (cw < 16 && (int64_t)cw * 4 < w.records) cw <<= 1;
+        p.combine_warps = cw;
+    }
     p.seg_rcp = div_rcp((uint32_t)seg);
     p.segb_rcp = div_rcp((uint32_t)(seg / kBlockSize));
     p.wph_shift = num_kv_heads == 8 ? 0 : num_kv_heads == 4 ? 1 : num_kv_heads == 2 ? 2 : 3;
-    if ((int64_t)num_seqs * num_kv_heads * w.chunks >= ((int64_t)1 << 31)) return KV_INT4_EUNSUPPORTED;
     p.status = status_ptr();
     p.num_blocks = num_blocks;
     p.num_q_tokens = num_q_tokens;

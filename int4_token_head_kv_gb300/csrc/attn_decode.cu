@@ -361,14 +361,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                       qraw_bytes, &qfull[qs], policy_evict_first());
     };
     griddep_wait();   // the cache (and the query) are produced by earlier kernels of the stream
-    if (blockIdx.x == 0) {   // the combine's sequence index and chunk counters
+    if (blockIdx.x == 0) {   // the combine's sequence index
         uint32_t ub = ub_t;
         for (int b = b0; b < b1; ++b) {
             p.ws_meta[b] = (int)ub;
             ub += fast_div((uint32_t)(own_info(b - b0, false).x + S - 1), (uint32_t)S, p.seg_rcp);
         }
         if (threadIdx.x == 0) p.ws_meta[N] = (int)U;
-        for (int i = threadIdx.x; i < N * H; i += kDecodeThreads) p.ws_cnt[i] = 0;
     }
     if (threadIdx.x == 0) {   // the first query rows, then the first blocks
         for (int r = 0; r < min(nq, nruns); ++r) produce_q(r);
@@ -794,49 +793,62 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 
 // ------------------------------------------------------------------ 2. combine
 
-constexpr int kCombineWarps = 8;
+constexpr int kCombineWarps = 16;
 
-// One warp per (decode sequence, kv head h, chunk of kDecodeChunkRecords records), a record
-// being (unit, warp of kv head h); grid (chunk groups, kv heads, sequences), min(8, chunks)
-// warps per CTA.  Lane l owns the accumulator slots l + 32 k of the partial
-// outputs (whole 512-byte rows per k, so every load is coalesced) and merges its chunk's records
-// in order with an online rescaling.  A sequence with one chunk is finished by that warp; with
-// several, each chunk is published to the workspace and the last chunk to arrive (counted
-// atomically, nothing waits) merges all chunks in chunk order.  Every sum's order depends only on
-// the sequence, never on the batch or on which warp finished last.
+// Dynamic shared memory of a combine CTA whose groups of W warps each own one (sequence, kv head).
+template <int D, bool WIDE>
+__host__ __device__ inline size_t combine_smem_bytes(int W, int G) {
+    const int NT = Geo<D>::MT * (WIDE ? 32 : 16);
+    return (size_t)kCombineWarps * NT * 16            // per-warp accumulator slots
+           + (size_t)kCombineWarps * 4 * 16           // per-warp (m, l) of 8 columns
+           + (size_t)(kCombineWarps / W) * G * (D + 4) * 4;   // normalised outputs per group
+}
+
+// A CTA of 16 warps in groups of W (a power of two, sized for the batch's longest sequence);
+// group k owns (sequence, kv head) item blockIdx.x * 16 / W + k, a record being (segment, walker
+// warp of that kv head).  The merge tree depends only on the item's own record count R, never on
+// the batch: the records form nc = min(16, pow2 >= ceil(R / 4)) <= W contiguous chunks of
+// ceil(R / nc); warp c folds chunk c in record order with an online rescaling, each lane owning
+// the accumulator slots lane + 32 j of the fragment-ordered partials (whole 512-byte rows, so
+// every load is coalesced, several records in flight), and the chunk states are then folded in
+// chunk order through shared memory, normalised, and the G outputs un-rotated by the group's warps.
 template <int D, bool WIDE, typename OT>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttnParams p) {
     constexpr int NLS = WIDE ? 32 : 16;
     constexpr int NT = Geo<D>::MT * NLS;   // float4 slots of one record
     constexpr int SPL = NT / 32;           // slots per lane
     constexpr int UNR = WIDE ? 2 : 4;      // records in flight per lane
-    constexpr int CPF = NT * 4 + 16;       // floats of a chunk partial: slots, then (m, l) per column
     constexpr int SO = D + 4;
     __shared__ float sgn[D];
-    extern __shared__ __align__(16) float sout_all[];   // [warps][8 * SO]
+    extern __shared__ __align__(16) float4 cbuf[];
+    float4* sacc = cbuf;                                   // [16 warps][NT]
+    float4* sml = cbuf + kCombineWarps * NT;               // [16 warps][4]
+    float* sout = reinterpret_cast<float*>(sml + kCombineWarps * 4);   // [groups][G][SO]
     griddep_wait();
     griddep_launch_dependents();   // the next call's walker may start its set-up
     for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int H = p.H, G = p.G, Hq = p.Hq, C = p.combine_chunks;
-    const int c = blockIdx.x * (blockDim.x >> 5) + warp, h = blockIdx.y, seq = blockIdx.z;
-    if (c >= C) return;
-    const int q0 = __ldg(p.qsl + seq);
-    if (__ldg(p.qsl + seq + 1) - q0 != 1 || q0 < 0 || (int64_t)q0 >= p.num_q_tokens) return;
-    const int L = min(max(__ldg(p.seq_lens + seq), 0), p.len_cap);
-    const int nseg = (int)fast_div((uint32_t)(L + p.seg_len - 1), (uint32_t)p.seg_len, p.seg_rcp);
-    const int64_t obase = ((int64_t)q0 * Hq + (int64_t)h * G) * D;
-    if (nseg == 0) {   // empty context: zero output
-        if (c == 0)
-            for (int i = lane; i < G * D; i += 32) store_elem<OT>(p.out, obase + i, 0.0f);
-        return;
+    const int W = p.combine_warps, grp = warp / W, sub = warp % W;
+    const int H = p.H, G = p.G, Hq = p.Hq;
+    const int64_t item = (int64_t)blockIdx.x * (kCombineWarps / W) + grp;
+    const int h = (int)(item % H);
+    const int seq = (int)(item / H);
+    // Items past the batch, non-decode sequences and empty contexts do no merging, but every
+    // thread reaches the barriers below.
+    int nseg = 0, q0 = 0;
+    bool active = seq < p.num_seqs;
+    if (active) {
+        q0 = __ldg(p.qsl + seq);
+        active = __ldg(p.qsl + seq + 1) - q0 == 1 && q0 >= 0 && (int64_t)q0 < p.num_q_tokens;
     }
+    if (active) {
+        const int L = min(max(__ldg(p.seq_lens + seq), 0), p.len_cap);
+        nseg = (int)fast_div((uint32_t)(L + p.seg_len - 1), (uint32_t)p.seg_len, p.seg_rcp);
+    }
+    const int64_t obase = ((int64_t)q0 * Hq + (int64_t)h * G) * D;
     const int ws = p.wph_shift;
     const int R = nseg << ws;
-    const int nch = (R + kDecodeChunkRecords - 1) / kDecodeChunkRecords;
-    if (c >= nch) return;
-    const int ub = p.ws_meta[seq];
+    const int ub = R > 0 ? p.ws_meta[seq] : 0;
     auto rec_of = [&](int r) -> size_t {
         return (size_t)(ub + (r >> ws)) * kConsumerWarps + h + (r & ((1 << ws) - 1)) * H;
     };
@@ -864,13 +876,17 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     };
     const float4* po = reinterpret_cast<const float4*>(p.ws_po);
     const float4* pml = reinterpret_cast<const float4*>(p.ws_pml);
-    const int r_end = min(R, (c + 1) * kDecodeChunkRecords);
-    for (int r0 = c * kDecodeChunkRecords; r0 < r_end; r0 += UNR) {
+    int nc = 1;
+    while (nc < 16 && nc * 4 < R) nc <<= 1;
+    const int K = (R + nc - 1) / nc;
+    const int r_lo = sub < nc ? sub * K : R, r_hi = sub < nc ? min(R, (sub + 1) * K) : R;
+    for (int r0 = r_lo; r0 < r_hi; r0 += UNR) {
         float4 ml[UNR], ov[UNR][SPL];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
-            const bool live = r0 + u < r_end;
-            const size_t rc = rec_of(live ? r0 + u : r0);
+            const int r = r0 + u;
+            const bool live = r < r_hi;
+            const size_t rc = rec_of(live ? r : r0);
             ml[u] = live ? pml[rc * 4 + tq] : make_float4(kNegBig, 0.0f, kNegBig, 0.0f);
 #pragma unroll
             for (int k = 0; k < SPL; ++k) ov[u][k] = live ? po[rc * NT + lane + 32 * k] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -878,66 +894,59 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
 #pragma unroll
         for (int u = 0; u < UNR; ++u) merge(ml[u], ov[u]);
     }
-
-    if (nch > 1) {
-        const int64_t pair = (int64_t)seq * H + h;
-        float4* cp = reinterpret_cast<float4*>(p.ws_cp + (pair * C + c) * CPF);
+    // the warps' states through shared memory; the group's threads then merge its slots
 #pragma unroll
-        for (int k = 0; k < SPL; ++k) cp[lane + 32 * k] = acc[k];
-        if (lane < (WIDE ? 4 : 2)) cp[NT + tq] = make_float4(m0, l0, m1, l1);
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(p.ws_cnt + pair, 1) == nch - 1;
-        if (!__shfl_sync(0xffffffffu, last, 0)) return;
-        __threadfence();
-        m0 = kNegBig;
-        m1 = kNegBig;
-        l0 = 0.0f;
-        l1 = 0.0f;
-#pragma unroll
-        for (int k = 0; k < SPL; ++k) acc[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        const float4* cps = reinterpret_cast<const float4*>(p.ws_cp + pair * C * CPF);
-        for (int c0 = 0; c0 < nch; c0 += UNR) {
-            float4 ml[UNR], ov[UNR][SPL];
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                const bool live = c0 + u < nch;
-                const float4* q = cps + (size_t)(live ? c0 + u : c0) * (CPF / 4);
-                ml[u] = live ? __ldcg(q + NT + tq) : make_float4(kNegBig, 0.0f, kNegBig, 0.0f);
-#pragma unroll
-                for (int k = 0; k < SPL; ++k) ov[u][k] = live ? __ldcg(q + lane + 32 * k) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int k = 0; k < SPL; ++k) sacc[warp * NT + lane + 32 * k] = acc[k];
+    if (lane < (WIDE ? 4 : 2)) sml[warp * 4 + tq] = make_float4(m0, l0, m1, l1);
+    __syncthreads();
+    float* gout = sout + (size_t)grp * G * SO;
+    if (R > 0) {
+        const int w0 = grp * W;
+        for (int slot = sub * 32 + lane; slot < NT; slot += W * 32) {
+            const int mt = slot / NLS, ls = slot % NLS;
+            const int sq = WIDE ? (ls & 3) : (ls & 1), gq = WIDE ? (ls >> 2) : (ls >> 1);
+            float M0 = kNegBig, M1 = kNegBig;
+            for (int w = 0; w < W; ++w) {
+                M0 = fmaxf(M0, sml[(w0 + w) * 4 + sq].x);
+                M1 = fmaxf(M1, sml[(w0 + w) * 4 + sq].z);
             }
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) merge(ml[u], ov[u]);
+            float L0 = 0.0f, L1 = 0.0f;
+            float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (int w = 0; w < W; ++w) {
+                const float4 v = sml[(w0 + w) * 4 + sq], o = sacc[(w0 + w) * NT + slot];
+                const float e0 = fast_exp2(v.x - M0), e1 = fast_exp2(v.z - M1);
+                L0 += v.y * e0;
+                L1 += v.w * e1;
+                a.x += o.x * e0;
+                a.z += o.z * e0;
+                a.y += o.y * e1;
+                a.w += o.w * e1;
+            }
+            const int c0 = 2 * sq, c1 = c0 + 1;
+            const int dlo = 8 * gq + mt;
+            const int dhi = (D == 128) ? 64 + 8 * gq + mt : 8 * gq + 4 + mt;
+            if (c0 < G) {
+                const float inv = L0 > 0.0f ? 1.0f / L0 : 0.0f;
+                gout[c0 * SO + dlo] = a.x * inv;
+                gout[c0 * SO + dhi] = a.z * inv;
+            }
+            if (c1 < G) {
+                const float inv = L1 > 0.0f ? 1.0f / L1 : 0.0f;
+                gout[c1 * SO + dlo] = a.y * inv;
+                gout[c1 * SO + dhi] = a.w * inv;
+            }
         }
     }
-
-    // normalise, transpose through shared memory, un-rotate each of the G outputs
-    float* so = sout_all + warp * 8 * SO;
-    const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
-    const int c0 = 2 * tq, c1 = c0 + 1;
-#pragma unroll
-    for (int k = 0; k < SPL; ++k) {
-        const int slot = lane + 32 * k;
-        const int mt = slot / NLS, ls = slot % NLS;
-        const int gq = WIDE ? (ls >> 2) : (ls >> 1);
-        const int dlo = 8 * gq + mt;
-        const int dhi = (D == 128) ? 64 + 8 * gq + mt : 8 * gq + 4 + mt;
-        if (c0 < G) {
-            so[c0 * SO + dlo] = acc[k].x * inv0;
-            so[c0 * SO + dhi] = acc[k].z * inv0;
-        }
-        if (c1 < G) {
-            so[c1 * SO + dlo] = acc[k].y * inv1;
-            so[c1 * SO + dhi] = acc[k].w * inv1;
-        }
+    __syncthreads();
+    if (!active) return;
+    if (R == 0) {   // empty context: zero output
+        for (int i = sub * 32 + lane; i < G * D; i += W * 32) store_elem<OT>(p.out, obase + i, 0.0f);
+        return;
     }
-    __syncwarp();
-    for (int col = 0; col < G; ++col) {
+    for (int col = sub; col < G; col += W) {
         float x[D / 32];
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) x[k] = so[col * SO + lane + 32 * k];
+        for (int k = 0; k < D / 32; ++k) x[k] = gout[col * SO + lane + 32 * k];
         unrotate_store<D, OT>(x, 1.0f, sgn, p.c, p.out, obase + (int64_t)col * D);
     }
 }
@@ -964,11 +973,16 @@ cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stre
     err = cudaLaunchKernelEx(&wcfg, decode_kernel<D, WIDE, QT>, p);
     if (err != cudaSuccess) return err;
 
-    const int warps = p.combine_chunks < kCombineWarps ? p.combine_chunks : kCombineWarps;
+    const int W = p.combine_warps;
+    const int64_t items = (int64_t)p.num_seqs * p.H;
+    const int64_t per_cta = kCombineWarps / W;
+    const size_t csmem = combine_smem_bytes<D, WIDE>(W, p.G);
+    err = opt_in_smem<combine_kernel<D, WIDE, OT>>(csmem);
+    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.combine_chunks + warps - 1) / warps), (unsigned)p.H, (unsigned)p.num_seqs);
-    cfg.blockDim = dim3(warps * 32);
-    cfg.dynamicSmemBytes = (size_t)warps * 8 * (D + 4) * 4;
+    cfg.gridDim = dim3((unsigned)((items + per_cta - 1) / per_cta));
+    cfg.blockDim = dim3(kCombineWarps * 32);
+    cfg.dynamicSmemBytes = csmem;
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;

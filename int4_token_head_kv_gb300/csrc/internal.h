@@ -36,8 +36,6 @@ struct AttnParams {
     const float* signs;
     void* out;
     int32_t* ws_meta;         // [num_seqs + 1] first split-KV unit of each sequence (exclusive prefix)
-    int32_t* ws_cnt;          // [num_seqs, H] combine chunks finished (zeroed by the walker)
-    float* ws_cp;             // [num_seqs, H, combine_chunks, ...] combine chunk partials
     float* ws_po;             // [units, 8 warps, po_floats] unnormalised partial outputs (fragment order)
     float* ws_pml;            // [units, 8 warps, 8 columns, 2] partial (max in log2 units, sum)
     uint32_t* status;
@@ -51,7 +49,7 @@ struct AttnParams {
     int max_blocks_per_seq;
     int seg_len;              // decode split-KV segment (unit) length in tokens, a multiple of 16
     int len_cap;              // decode context lengths are clamped to this (max_seq_len, block table)
-    int combine_chunks;       // most combine chunks a (sequence, kv head) can have
+    int combine_warps;        // combine warps per (sequence, kv head): a power of two, 1..16
     uint32_t seg_rcp;         // floor(2^32 / seg_len), for fast_div
     uint32_t segb_rcp;        // floor(2^32 / (seg_len / 16)) (all ones for 1)
     int wph_shift;            // log2(8 / H): consumer warps per kv head
@@ -67,14 +65,12 @@ cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DTyp
                           cudaStream_t stream);
 int decode_grid_size(int64_t max_blocks_total, int64_t max_units);
 constexpr int kDecodeMaxUnits = 256;   // split-KV units one walker CTA may own
-constexpr int kDecodeChunkRecords = 8; // partial records one combine warp merges
 
 // One warp's unnormalised partial output of one split-KV unit of the decode path: D/16 row tiles
 // x 16 (32 when G == 8) lanes x 4 accumulators (shared by the host's workspace layout and the
 // kernels).
 inline constexpr uint32_t decode_po_floats(int D, int G) { return (uint32_t)(D / 16) * (G == 8 ? 32u : 16u) * 4u; }
-// One combine chunk partial: the same accumulators, then (max, sum) for 8 columns.
-inline constexpr uint32_t decode_cp_floats(int D, int G) { return decode_po_floats(D, G) + 16u; }
+
 cudaError_t launch_prefill(const AttnParams& p, int head_size, int max_query_len, DType q_dt, DType out_dt,
                            cudaStream_t stream);
 
