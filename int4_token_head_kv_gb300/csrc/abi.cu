@@ -144,11 +144,12 @@ namespace {
 
 // Workspace of the decode path, in 256-byte-aligned regions:
 //   meta  [num_seqs + 1] int32             first unit of each sequence
+//   q     [num_seqs, qrec_words]           rotated-query records
 //   po    [units, 8, po_floats]            unnormalised partial outputs
 //   pml   [units, 8, 16] fp32              partial (max, sum) per column
 // units <= num_seqs * ceil(max_seq_len / segment_len).
 struct WsLayout {
-    size_t meta, po, pml, total;
+    size_t meta, q, po, pml, total;
     int64_t records;   // most partial records of one (sequence, kv head)
 };
 
@@ -163,7 +164,8 @@ bool ws_layout(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int
     const int64_t max_units = (int64_t)num_seqs * seg_per_seq;
     w->records = seg_per_seq * (8 / num_kv_heads);
     w->meta = 0;
-    w->po = align256((size_t)(num_seqs + 1) * 4);
+    w->q = align256((size_t)(num_seqs + 1) * 4);
+    w->po = w->q + align256((size_t)num_seqs * decode_qrec_words(head_size, num_kv_heads, G) * 4);
     w->pml = w->po + align256((size_t)max_units * 8 * decode_po_floats(head_size, G) * 4);
     w->total = w->pml + (size_t)max_units * 8 * 16 * 4;
     return true;
@@ -229,6 +231,8 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     p.out = out;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.ws_meta = reinterpret_cast<int32_t*>(ws + w.meta);
+    p.ws_q = reinterpret_cast<uint32_t*>(ws + w.q);
+    p.qrec_words = (int)decode_qrec_words(head_size, num_kv_heads, G);
     p.ws_po = reinterpret_cast<float*>(ws + w.po);
     p.ws_pml = reinterpret_cast<float*>(ws + w.pml);
     {   // warps per (sequence, kv head) in the combine: about one per four records, 1..16

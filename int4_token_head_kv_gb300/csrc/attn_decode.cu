@@ -8,7 +8,10 @@
 // (max, sum, accumulator) partials are combined afterwards ("3D" segment reduction of the
 // unified-attention interface, test_triton_unified_attention_per_token_head_scale).
 //
-// GB300 design, two launches per call:
+// GB300 design, three launches per call:
+//  0. qrot_kernel rotates each decode query once (v = H_d D q, power-of-two prescale, fp16 high +
+//     low halves laid out as the score mma's B fragments, the per-head logit factor and sum(q')).
+//     It only reads the queries, so it may run while the cache write that precedes it finishes.
 //  1. decode_kernel walks split-KV units.  Unit sigma of sequence b is its KV tokens
 //     [sigma S, (sigma + 1) S), S = seg_len.  A fixed grid of about two CTAs per SM takes
 //     contiguous runs of units, balanced by cache blocks (CTA c owns the units whose first block
@@ -23,10 +26,8 @@
 //    async copies (cp.async.bulk + mbarrier transaction counts, L2 evict-first).  The ring runs
 //    across unit boundaries.  There is no producer warp: the CTA's block ids are staged in shared
 //    memory up front, four lanes issue the first four copies, and the last consumer warp to
-//    finish with a stage issues its next block.  The raw query rows of each run of units of one
-//    sequence arrive the same way (double-buffered), and each warp rotates the query vectors of
-//    its kv head itself (H_d D q in fp32, then fp16 high + low halves laid out as mma fragments
-//    through a small per-warp shared-memory scratch).
+//    finish with a stage issues its next block.  The rotated-query record of each run of units of
+//    one sequence arrives the same way.
 //  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block pair when H < 8).
 //    Split-dot scores over the even and odd nibble streams: each code word is unpacked into the
 //    raw codes as exact fp16 integers (even codes through fp16 1024 + e, odd codes through
@@ -58,21 +59,18 @@ constexpr int kMaxHead = 128;
 constexpr uint32_t kCodeLo = 0x64006400u;   // (1024, 1024)
 constexpr uint32_t kCodeHi = 0xD400D400u;   // (-64, -64)
 
-// Ring depth and rows of a warp's query scratch.  With up to 4 query heads per kv head the
-// high and low halves pass through 4 rows one after the other, which leaves room for a fifth
-// ring stage at two CTAs per SM; 8 heads per kv head need 8 rows and keep 4 stages.
+// Ring depth: 5 stages with up to 4 query heads per kv head, 4 with 8 (whose query records are
+// twice as large), so that two CTAs fit an SM.
 template <bool WIDE>
 struct WalkerShape {
     static constexpr int kStages = WIDE ? 4 : 5;
-    static constexpr int kScrRows = WIDE ? 8 : 4;
 };
 
 struct DecodeSmem {
     uint32_t stage_bytes;   // one block (K + V planes)
-    uint32_t qraw_bytes;    // one sequence's query rows (Hq x D, 16-bit)
+    uint32_t qrec_bytes;    // one sequence's rotated-query record
     uint32_t nq;            // query buffers (2 when two CTAs still fit an SM, else 1)
     uint32_t q_off;
-    uint32_t scr_off;       // per-warp scratch: scratch rows x (D + 8) halves
     uint32_t state_off;     // barriers, counters, unit list, block-table window
     uint32_t total;
 };
@@ -90,12 +88,11 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
     using Sh = WalkerShape<WIDE>;
     DecodeSmem s;
     s.stage_bytes = 2u * kBlockSize * (uint32_t)H * Geo<D>::RB;
-    s.qraw_bytes = (uint32_t)Hq * D * 2u;
+    s.qrec_bytes = decode_qrec_words(D, H, Hq / H) * 4u;
     s.q_off = (Sh::kStages * s.stage_bytes + 127u) & ~127u;
     s.nq = 2;
     for (;;) {
-        s.scr_off = (s.q_off + s.nq * s.qraw_bytes + 127u) & ~127u;
-        s.state_off = (s.scr_off + kConsumerWarps * Sh::kScrRows * (D + 8) * 2u + 127u) & ~127u;
+        s.state_off = (s.q_off + s.nq * s.qrec_bytes + 127u) & ~127u;
         s.total = s.state_off + ((kStateBytes + 127u) & ~127u);
         if (s.nq == 1 || 2u * (s.total + kSmemPerCtaReserved) <= kSmemPerSm) break;
         s.nq = 1;
@@ -131,16 +128,134 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
+// ------------------------------------------------------------------ 0. query rotation
+
+// One CTA per sequence; only decode sequences (one query token) are rotated.  Record of a sequence
+// (32-bit words): for kv head h, 32-dimension group j and lane, the QW fp16x2 words that lane feeds
+// to the score mma; then alpha[Hq rounded up to 4] (raw score -> log2-domain logit, before the
+// key's scale) and qsum[Hq rounded up to 4] (sum of the stored high + low halves of each vector).
+template <int D, bool WIDE, typename QT>
+__global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnParams p) {
+    constexpr int QW = WIDE ? 8 : 4, KWPT = D / 32;
+    extern __shared__ __align__(128) uint8_t smem[];
+    griddep_launch_dependents();   // the walker's set-up reads only metadata
+    const int seq = blockIdx.x;
+    const int q0 = __ldg(p.qsl + seq);
+    const bool decode = __ldg(p.qsl + seq + 1) - q0 == 1 && q0 >= 0 && (int64_t)q0 < p.num_q_tokens;
+    if (decode) {   // uniform over the CTA
+        const int H = p.H, G = p.G, Hq = p.Hq, Hq4 = (Hq + 3) & ~3;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        float* sgn = reinterpret_cast<float*>(smem);
+        float* alpha = sgn + D;
+        float* qsum = alpha + Hq4;
+        __half* qh = reinterpret_cast<__half*>(qsum + Hq4);
+        __half* ql = qh + Hq * D;
+        for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
+        __syncthreads();
+        const float lsc = p.c * p.softmax_scale * kLog2e;
+        for (int v0 = warp; v0 < Hq; v0 += 4 * 8) {   // four vectors per warp at a time
+            float x[4][D / 32];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int v = v0 + 8 * k;
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j)
+                    x[k][j] = v < Hq ? load_elem<QT>(p.q, ((int64_t)q0 * Hq + v) * D + lane + 32 * j) * sgn[lane + 32 * j]
+                                     : 0.0f;
+            }
+            // v = H_d D q; a power-of-two prescale brings max|v| into [2^14, 2^15) for the halves
+            warp_fwht_batch<D, 4>(x);
+            float mx[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mx[k] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) mx[k] = fmaxf(mx[k], fabsf(x[k][j]));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], off));
+            }
+            float sum[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int v = v0 + 8 * k;
+                const int e = prescale_exponent(mx[k]);
+                const float sc = exp2i(e);
+                sum[k] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) {
+                    const float y = x[k][j] * sc;
+                    const __half hi = __float2half_rn(y);
+                    const __half lo = __float2half_rn(y - __half2float(hi));
+                    sum[k] += __half2float(hi) + __half2float(lo);
+                    if (v < Hq) {
+                        qh[v * D + lane + 32 * j] = hi;
+                        ql[v * D + lane + 32 * j] = lo;
+                    }
+                }
+                if (lane == 0 && v < Hq) alpha[v] = lsc * exp2i(-e);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sum[k] += __shfl_xor_sync(0xffffffffu, sum[k], off);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (lane == 0 && v0 + 8 * k < Hq) qsum[v0 + 8 * k] = sum[k];
+        }
+        __syncthreads();
+        // Score-mma B fragments.  Lane (g, t) of kv head h's warp feeds, for code word W = t + 4 j
+        // of a key row (dims 8W .. 8W+7), the pairs (8W+2hh, 8W+2hh+4) and (8W+2hh+1, 8W+2hh+5)
+        // of its column's vector, hh = 0, 1.  Columns: G == 8, head g (high halves; the low
+        // halves follow as a second tile); otherwise head g & 3, high halves for g < 4 and low
+        // halves for g >= 4.
+        uint32_t* rec = p.ws_q + (size_t)seq * p.qrec_words;
+        for (int idx = threadIdx.x; idx < H * KWPT * 32; idx += blockDim.x) {
+            const int ln = idx & 31, j = (idx >> 5) % KWPT, h = idx / (32 * KWPT);
+            const int g = ln >> 2, t = ln & 3;
+            const int head = WIDE ? g : (g & 3);
+            const bool live = head < G;
+            const int vrow = (h * G + (live ? head : 0)) * D;
+            const __half* qv = (WIDE || g < 4 ? qh : ql) + vrow;
+            const __half* qv2 = ql + vrow;
+            const int W = t + 4 * j;
+            uint32_t w[QW];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int d0 = 8 * W + 2 * hh;
+                w[2 * hh] = live ? pack_halves(qv[d0], qv[d0 + 4]) : 0u;
+                w[2 * hh + 1] = live ? pack_halves(qv[d0 + 1], qv[d0 + 5]) : 0u;
+                if constexpr (WIDE) {
+                    w[4 + 2 * hh] = live ? pack_halves(qv2[d0], qv2[d0 + 4]) : 0u;
+                    w[5 + 2 * hh] = live ? pack_halves(qv2[d0 + 1], qv2[d0 + 5]) : 0u;
+                }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(rec) + (size_t)idx * (QW / 4);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            if constexpr (WIDE) dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        float* ralpha = reinterpret_cast<float*>(rec + (size_t)H * D * QW);
+        for (int v = threadIdx.x; v < Hq4; v += blockDim.x) {
+            ralpha[v] = v < Hq ? alpha[v] : 0.0f;
+            ralpha[Hq4 + v] = v < Hq ? qsum[v] : 0.0f;
+        }
+    }
+    // Complete only after the previous kernel of the stream (the cache write, typically) has:
+    // whoever waits for this kernel then also sees that kernel's results.
+    griddep_wait();
+}
+
 // ------------------------------------------------------------------ 1. split-KV unit walker
 
-template <int D, bool WIDE, typename QT>
+template <int D, bool WIDE>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ AttnParams p) {
     using Gm = Geo<D>;
-    constexpr int NB = WIDE ? 8 : 4;      // query vectors a warp rotates (its kv head's group)
+    constexpr int QW = WIDE ? 8 : 4;      // fragment words per lane per 32-dimension group
     constexpr int NLS = WIDE ? 32 : 16;
-    constexpr int SR = D + 8;             // scratch row stride (halves), staggers banks
     constexpr int kStages = WalkerShape<WIDE>::kStages;
-    constexpr int kScrRows = WalkerShape<WIDE>::kScrRows;
     constexpr uint32_t PO = decode_po_floats(D, WIDE ? 8 : 1);
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = p.H, G = p.G;
@@ -150,7 +265,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     const int nq = (int)lay.nq;
     uint8_t* ring = smem;
     uint8_t* qbuf = smem + lay.q_off;
-    __half* qscr = reinterpret_cast<__half*>(smem + lay.scr_off) + warp * kScrRows * SR;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.state_off);
     uint64_t* qfull = full + kMaxStages;
     unsigned long long* wsum = reinterpret_cast<unsigned long long*>(qfull + 2);
@@ -162,9 +276,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     int4* units = reinterpret_cast<int4*>(info + 8);     // (seq, first block in seq, global unit, tokens)
     int* ustart = reinterpret_cast<int*>(units + kMaxUnits);   // first block, in the batch's block order
     int* run_first = ustart + kMaxUnits;                 // first unit of each run of one sequence
-    int* run_q0 = run_first + kMaxUnits;                 // that sequence's query row
-    int* tbl = run_q0 + kMaxUnits;                       // block ids of the CTA's first kTableWin blocks
-    float* sgn = reinterpret_cast<float*>(tbl + kTableWin);
+    int* run_seq = run_first + kMaxUnits;                // that sequence
+    int* tbl = run_seq + kMaxUnits;                      // block ids of the CTA's first kTableWin blocks
 
     // Launched as a programmatic dependent (of the cache write, typically): everything up to
     // griddep_wait() below reads only the host-provided metadata (query_start_loc, seq_lens, block
@@ -172,7 +285,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     // waits for this grid before reading anything, and its CTAs become resident as walker CTAs
     // retire.
     griddep_launch_dependents();
-    const float sg_in = threadIdx.x < D ? __ldg(p.signs + threadIdx.x) : 0.0f;   // consumed below
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -225,7 +337,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             }
         }
     }
-    if (threadIdx.x < D) sgn[threadIdx.x] = sg_in < 0.0f ? -1.0f : 1.0f;
     __syncthreads();
     // (L, q0) of this thread's i-th sequence, and of any sequence b
     auto own_info = [&](int i, bool count) -> int2 {
@@ -312,7 +423,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         const int r = (int)block_exclusive_scan(first ? 1ull : 0ull, wsum, &nruns_ll);
         if (first) {
             run_first[r] = j;
-            run_q0[r] = seq_info(units[j].x).y;
+            run_seq[r] = units[j].x;
         }
     }
     const int nruns = (int)nruns_ll;
@@ -333,7 +444,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     for (int i = threadIdx.x; i < min(nb_cta, kTableWin); i += kDecodeThreads) tbl[i] = block_id(i);
     __syncthreads();
 
-    const uint32_t stage_bytes = lay.stage_bytes, qraw_bytes = lay.qraw_bytes;
+    const uint32_t stage_bytes = lay.stage_bytes, qrec_bytes = lay.qrec_bytes;
     // Ring refill rule: block i goes to stage i % kStages.  The first kStages blocks are issued up
     // front; afterwards the LAST consumer warp to finish with block i (counted in released[])
     // issues block i + kStages into the same stage, so no warp ever blocks waiting to refill.
@@ -352,15 +463,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             mbar_arrive(&full[st]);
         }
     };
-    // Query rows of run r go to buffer r % nq, refilled the same way once every warp has read them.
+    // The query record of run r goes to buffer r % nq, refilled the same way once every warp has
+    // read it.
     auto produce_q = [&](int r) {
         const int qs = r & (nq - 1);
         atomicMax(&flags[2], r + 1);
-        mbar_arrive_expect_tx(&qfull[qs], qraw_bytes);
-        bulk_copy_g2s(qbuf + (size_t)qs * qraw_bytes, static_cast<const uint8_t*>(p.q) + (size_t)run_q0[r] * qraw_bytes,
-                      qraw_bytes, &qfull[qs], policy_evict_first());
+        mbar_arrive_expect_tx(&qfull[qs], qrec_bytes);
+        bulk_copy_g2s(qbuf + (size_t)qs * qrec_bytes, p.ws_q + (size_t)run_seq[r] * p.qrec_words, qrec_bytes,
+                      &qfull[qs], policy_evict_first());
     };
-    griddep_wait();   // the cache (and the query) are produced by earlier kernels of the stream
+    griddep_wait();   // the query records, and through them the cache, come from earlier kernels
     if (blockIdx.x == 0) {   // the combine's sequence index
         uint32_t ub = ub_t;
         for (int b = b0; b < b1; ++b) {
@@ -389,7 +501,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     const int hb = WIDE ? 2 * t : 2 * (t & 1);
     const bool lo_lane = !WIDE && t >= 2;   // this lane's P columns carry low halves
     uint32_t qb[Gm::KSTEPS][WIDE ? 4 : 2];
-    const float lsc = p.c * p.softmax_scale * kLog2e;
     float al0 = 0.0f, al1 = 0.0f;     // logit factor of columns hb, hb + 1
     float qs0 = 0.0f, qs1 = 0.0f;     // sum(Q') of those columns (high + low halves as stored)
     float WZ0 = 0.0f, WZ1 = 0.0f;     // sum(w zp) per column
@@ -398,7 +509,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 
     for (int j = 0; j < nunits && !stop; ++j) {
         const int4 u = units[j];
-        if (u.x != prev_seq) {   // a new sequence: rotate its query vectors of kv head h
+        if (u.x != prev_seq) {   // a new sequence: its rotated-query record from the buffer
             prev_seq = u.x;
             ++run;
             const int qs = run & (nq - 1);
@@ -409,15 +520,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 }
                 break;
             }
-            const uint8_t* raw = qbuf + (size_t)qs * qraw_bytes;
-            float x[NB][D / 32];
+            const uint8_t* rec = qbuf + (size_t)qs * qrec_bytes;
+            const uint4* fr = reinterpret_cast<const uint4*>(rec) + ((size_t)h * Gm::KWPT * 32 + lane) * (QW / 4);
 #pragma unroll
-            for (int k = 0; k < NB; ++k) {
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q)
-                    x[k][q] = k < G ? load_elem<QT>(raw, (int64_t)(h * G + k) * D + lane + 32 * q) * sgn[lane + 32 * q]
-                                    : 0.0f;
+            for (int k = 0; k < Gm::KWPT; ++k) {
+                const uint4 a = fr[k * 32 * (QW / 4)];
+                qb[2 * k][0] = a.x;
+                qb[2 * k][1] = a.y;
+                qb[2 * k + 1][0] = a.z;
+                qb[2 * k + 1][1] = a.w;
+                if constexpr (WIDE) {
+                    const uint4 b = fr[k * 32 * (QW / 4) + 1];
+                    qb[2 * k][2] = b.x;
+                    qb[2 * k][3] = b.y;
+                    qb[2 * k + 1][2] = b.z;
+                    qb[2 * k + 1][3] = b.w;
+                }
             }
+            const float* alpha = reinterpret_cast<const float*>(rec) + (size_t)H * D * QW;
+            const float* qsum = alpha + ((p.Hq + 3) & ~3);
+            al0 = (hb < G) ? alpha[h * G + hb] : 0.0f;
+            al1 = (hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
+            qs0 = (hb < G) ? qsum[h * G + hb] : 0.0f;
+            qs1 = (hb + 1 < G) ? qsum[h * G + hb + 1] : 0.0f;
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();   // this warp's reads of the buffer come before the count
@@ -428,112 +553,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     if (run + nq < nruns && !*(volatile int*)flags) produce_q(run + nq);
                 }
             }
-            // v = H_d D q; a power-of-two prescale brings max|v| into [2^14, 2^15) for the fp16 halves
-            warp_fwht_batch<D, NB>(x);
-            float mx[NB];
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                mx[k] = 0.0f;
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) mx[k] = fmaxf(mx[k], fabsf(x[k][q]));
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-                for (int k = 0; k < NB; ++k) mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], off));
-            }
-            al0 = 0.0f;
-            al1 = 0.0f;
-            float qsum[NB];
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                const int e = prescale_exponent(mx[k]);
-                mx[k] = exp2i(e);                        // now the scale
-                const float a = lsc * exp2i(-e);         // raw score -> log2-domain logit (before s'_K)
-                if (k == hb && k < G) al0 = a;
-                if (k == hb + 1 && k < G) al1 = a;
-                qsum[k] = 0.0f;                          // sum of the stored high + low halves
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    const float y = x[k][q] * mx[k];
-                    const float hi = __half2float(__float2half_rn(y));
-                    qsum[k] += hi + __half2float(__float2half_rn(y - hi));
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-                for (int k = 0; k < NB; ++k) qsum[k] += __shfl_xor_sync(0xffffffffu, qsum[k], off);
-            }
-            qs0 = qs1 = 0.0f;
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                if (k == hb && k < G) qs0 = qsum[k];
-                if (k == hb + 1 && k < G) qs1 = qsum[k];
-            }
-            // Score-mma B fragments through the scratch: lane (g, t) feeds, for code word
-            // W = t + 4 q of a key row (dims 8W .. 8W+7), the pairs (8W+2hh, 8W+2hh+4) and
-            // (8W+2hh+1, 8W+2hh+5) of its column's vector, hh = 0, 1.
-            auto build = [&](int slot, int row) {
-                const int head = WIDE ? g : (g & 3);
-                const bool live = head < G;
-                const __half* qv = qscr + row * SR;
-#pragma unroll
-                for (int q = 0; q < Gm::KWPT; ++q) {
-                    const int W = t + 4 * q;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int d0 = 8 * W + 2 * hh;
-                        qb[2 * q + hh][slot] = live ? pack_halves(qv[d0], qv[d0 + 4]) : 0u;
-                        qb[2 * q + hh][slot + 1] = live ? pack_halves(qv[d0 + 1], qv[d0 + 5]) : 0u;
-                    }
-                }
-            };
-            if constexpr (!WIDE) {
-                // rows 0-3 hold the high halves of heads 0-3 for lanes g < 4, then the low
-                // halves for lanes g >= 4
-#pragma unroll
-                for (int k = 0; k < NB; ++k) {
-                    if (k >= G) continue;
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) qscr[k * SR + lane + 32 * q] = __float2half_rn(x[k][q] * mx[k]);
-                }
-                __syncwarp();
-                if (g < 4) build(0, g & 3);
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < NB; ++k) {
-                    if (k >= G) continue;
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        const float y = x[k][q] * mx[k];
-                        qscr[k * SR + lane + 32 * q] = __float2half_rn(y - __half2float(__float2half_rn(y)));
-                    }
-                }
-                __syncwarp();
-                if (g >= 4) build(0, g & 3);
-            } else {
-                // high halves of heads 0-7, then (rows reused) their low halves
-#pragma unroll
-                for (int k = 0; k < NB; ++k) {
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) qscr[k * SR + lane + 32 * q] = __float2half_rn(x[k][q] * mx[k]);
-                }
-                __syncwarp();
-                build(0, g);
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < NB; ++k) {
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        const float y = x[k][q] * mx[k];
-                        qscr[k * SR + lane + 32 * q] = __float2half_rn(y - __half2float(__float2half_rn(y)));
-                    }
-                }
-                __syncwarp();
-                build(2, g);
-            }
-            __syncwarp();   // the scratch is free for the next run
         }
 
 #pragma unroll
@@ -956,13 +975,24 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
 template <int D, bool WIDE, typename QT, typename OT>
 cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stream) {
     const DecodeSmem lay = decode_smem_layout<D, WIDE>(p.H, p.Hq);
-    cudaError_t err = opt_in_smem<decode_kernel<D, WIDE, QT>>(lay.total);
+    cudaError_t err = opt_in_smem<decode_kernel<D, WIDE>>(lay.total);
     if (err != cudaSuccess) return err;
-    // Both kernels are programmatic dependents of their predecessor: each starts its set-up while
-    // the previous kernel finishes and waits for it (griddep_wait) before touching its results.
+    // All three kernels are programmatic dependents of their predecessor: each starts its set-up
+    // while the previous kernel finishes and waits for it (griddep_wait) before touching its
+    // results.
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
+    const size_t qsm = D * 4 + 2 * (size_t)((p.Hq + 3) & ~3) * 4 + 2 * (size_t)p.Hq * D * 2;
+    cudaLaunchConfig_t qcfg = {};
+    qcfg.gridDim = dim3((unsigned)p.num_seqs);
+    qcfg.blockDim = dim3(256);
+    qcfg.dynamicSmemBytes = qsm;
+    qcfg.stream = stream;
+    qcfg.attrs = &attr;
+    qcfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&qcfg, qrot_kernel<D, WIDE, QT>, p);
+    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t wcfg = {};
     wcfg.gridDim = dim3((unsigned)num_ctas);
     wcfg.blockDim = dim3(kDecodeThreads);
@@ -970,7 +1000,7 @@ cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stre
     wcfg.stream = stream;
     wcfg.attrs = &attr;
     wcfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&wcfg, decode_kernel<D, WIDE, QT>, p);
+    err = cudaLaunchKernelEx(&wcfg, decode_kernel<D, WIDE>, p);
     if (err != cudaSuccess) return err;
 
     const int W = p.combine_warps;

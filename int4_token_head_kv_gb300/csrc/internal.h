@@ -36,6 +36,7 @@ struct AttnParams {
     const float* signs;
     void* out;
     int32_t* ws_meta;         // [num_seqs + 1] first split-KV unit of each sequence (exclusive prefix)
+    uint32_t* ws_q;           // [num_seqs, qrec_words] rotated-query records of the decode sequences
     float* ws_po;             // [units, 8 warps, po_floats] unnormalised partial outputs (fragment order)
     float* ws_pml;            // [units, 8 warps, 8 columns, 2] partial (max in log2 units, sum)
     uint32_t* status;
@@ -50,6 +51,7 @@ struct AttnParams {
     int seg_len;              // decode split-KV segment (unit) length in tokens, a multiple of 16
     int len_cap;              // decode context lengths are clamped to this (max_seq_len, block table)
     int combine_warps;        // combine warps per (sequence, kv head): a power of two, 1..16
+    int qrec_words;           // 32-bit words of one rotated-query record
     uint32_t seg_rcp;         // floor(2^32 / seg_len), for fast_div
     uint32_t segb_rcp;        // floor(2^32 / (seg_len / 16)) (all ones for 1)
     int wph_shift;            // log2(8 / H): consumer warps per kv head
@@ -66,6 +68,12 @@ cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DTyp
 int decode_grid_size(int64_t max_blocks_total, int64_t max_units);
 constexpr int kDecodeMaxUnits = 256;   // split-KV units one walker CTA may own
 
+// Rotated-query record of one decode sequence (32-bit words): per kv head, 32-dimension group and
+// lane the 4 (8 when G == 8) fp16x2 words that lane feeds to the score mma, then the Hq logit
+// factors and the Hq sums of the stored query halves (each padded to a multiple of 4).
+inline constexpr uint32_t decode_qrec_words(int D, int H, int G) {
+    return (uint32_t)H * (uint32_t)D * (G == 8 ? 8u : 4u) + 2u * (((uint32_t)(H * G) + 3u) & ~3u);
+}
 // One warp's unnormalised partial output of one split-KV unit of the decode path: D/16 row tiles
 // x 16 (32 when G == 8) lanes x 4 accumulators (shared by the host's workspace layout and the
 // kernels).
