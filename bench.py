@@ -13,7 +13,7 @@ whole cache.
           device->host.
   write   the write-throughput workload (65536 tokens, 8 kv heads, d 128, bf16, per-token
           magnitudes 10^U(-2,2), random slots over 8192 blocks): tokens/s and GB/s.
-  roofline  for the dominant kernel call (the attention: decode kernel + segment combine), bytes
+  roofline  for the dominant kernel call (the attention: query rotation + decode kernel + segment combine), bytes
           per launch over its CUDA-event time on the launching stream, against the measured HBM
           copy bandwidth; ``traffic`` is the ncu DRAM byte count of the decode kernel when a
           summary with it is committed under profiles/, else null.
@@ -183,7 +183,7 @@ def _gpu_arm(args):
     kv_bytes = int(wl.seq_lens.sum()) * 2 * H * rb
     qo_bytes = 2 * wl.query.numel() * wl.query.element_size()
     attn_bytes = kv_bytes + qo_bytes
-    launches_per_step = 3   # write; split-KV walker; combine
+    launches_per_step = 4   # write; query rotation; split-KV walker; combine
 
     def write(i):
         kv.kv_int4_write(t["k"], t["v"], t["slots"], t["signs"], caches[i % replicas])
@@ -204,7 +204,7 @@ def _gpu_arm(args):
     torch.cuda.synchronize()
     # One CUDA graph per cache replica holding one whole step (write + attention), and one holding
     # the attention call alone; decode steps are replayed as graphs, which takes the Python and
-    # launch overhead of three library calls per step off the GPU's critical path.
+    # launch overhead of the four kernel launches per step off the GPU's critical path.
     step_graphs, attn_graphs = [], []
     for r in range(replicas):
         g = torch.cuda.CUDAGraph()
@@ -294,7 +294,7 @@ def _gpu_arm(args):
                 "ms_per_step": round(e2e_ms, 5)},
         "roofline": {"bound": "hbm", "achieved": round(roof_achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(roof_achieved / peak, 4), "traffic": traffic,
-                     "kernel": "attention call (decode kernel + segment combine), graph-replayed back to back",
+                     "kernel": "attention call (query rotation + decode kernel + segment combine), graph-replayed back to back",
                      "peak_source": peak_kind,
                      "bytes_per_launch": attn_bytes, "avg_ms": round(attn_avg_ms, 5)},
         "write": wres,

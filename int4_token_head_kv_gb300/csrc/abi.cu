@@ -258,7 +258,8 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     p.c = (float)(1.0 / std::sqrt((double)head_size));
 
     const int64_t max_units = (int64_t)num_seqs * (((int64_t)max_seq_len + seg - 1) / seg);
-    const int ctas = decode_grid_size(max_blocks_total, max_units);
+    // balance weight bound: the blocks, plus at most one padded unit per sequence
+    const int ctas = decode_grid_size(max_blocks_total + (int64_t)num_seqs * (seg / kBlockSize), max_units);
     const DType qd = q_dtype == KV_INT4_BF16 ? DType::BF16 : DType::F16;
     const DType od = out_dtype == KV_INT4_BF16 ? DType::BF16 : (out_dtype == KV_INT4_F16 ? DType::F16 : DType::F32);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

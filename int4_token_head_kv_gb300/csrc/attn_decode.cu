@@ -14,8 +14,9 @@
 //     It only reads the queries, so it may run while the cache write that precedes it finishes.
 //  1. decode_kernel walks split-KV units.  Unit sigma of sequence b is its KV tokens
 //     [sigma S, (sigma + 1) S), S = seg_len.  A fixed grid of about two CTAs per SM takes
-//     contiguous runs of units, balanced by cache blocks (CTA c owns the units whose first block
-//     falls in [c T / n, (c + 1) T / n) of the batch's T decode blocks), and every unit writes
+//     contiguous runs of units, balanced by cache blocks (CTA c owns the units that start in
+//     [c W / n, (c + 1) W / n) of the batch's W decode blocks, a sequence's partial last unit
+//     counting as a whole one when the sequence has several), and every unit writes
 //     its own (max, sum, unnormalised output) partial.  A unit's arithmetic does not depend on
 //     the CTA that runs it, so a sequence's output does not depend on the rest of the batch.
 //  2. combine_kernel merges the units of each sequence in a fixed order and un-rotates.
@@ -348,26 +349,37 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         if (staged) return meta[(b % per) * kDecodeThreads + b / per];
         return decode_of(__ldg(p.qsl + b), __ldg(p.qsl + b + 1), __ldg(p.seq_lens + b), false);
     };
-    uint32_t my_units = 0, my_blocks = 0;
+    // Balance weight of a sequence: its blocks, except that the last (partial) unit of a sequence
+    // with several units weighs a whole unit.  A CTA's share then rarely ends with two whole
+    // units after a short tail unit (a common 2.5-unit overload when shares hold about two units).
+    auto weight_of = [&](uint32_t nblk, uint32_t nseg) -> uint32_t {
+        return nseg > 1u ? nseg * (uint32_t)SB : nblk;
+    };
+    uint32_t my_units = 0, my_blocks = 0, my_weight = 0;
     for (int b = b0; b < b1; ++b) {
         const int L = own_info(b - b0, blockIdx.x == 0).x;
-        my_units += fast_div((uint32_t)(L + S - 1), (uint32_t)S, p.seg_rcp);
-        my_blocks += (uint32_t)((L + kBlockSize - 1) / kBlockSize);
+        const uint32_t nseg = fast_div((uint32_t)(L + S - 1), (uint32_t)S, p.seg_rcp);
+        const uint32_t nblk = (uint32_t)((L + kBlockSize - 1) / kBlockSize);
+        my_units += nseg;
+        my_blocks += nblk;
+        my_weight += weight_of(nblk, nseg);
     }
-    unsigned long long tot;
+    unsigned long long tot, wtot;
     const unsigned long long pre =
         block_exclusive_scan(((unsigned long long)my_blocks << 32) | my_units, wsum, &tot);
-    const uint32_t U = (uint32_t)tot, T = (uint32_t)(tot >> 32);
+    const uint32_t wb_t = (uint32_t)block_exclusive_scan(my_weight, wsum, &wtot);
+    const uint32_t U = (uint32_t)tot, Wt = (uint32_t)wtot;
     const uint32_t ub_t = (uint32_t)pre, bb_t = (uint32_t)(pre >> 32);
 
-    // This CTA's share of the batch's blocks, [f(c), f(c+1)) with f(c) = c T / n in fp32: any
-    // monotone f with f(0) = 0 and f(n) = T splits the blocks exactly, and every CTA evaluates
-    // the shared boundary the same way.  Then the units that start inside it.
-    const float per_cta = (float)T / (float)gridDim.x;
+    // This CTA's share of the batch's weight, [f(c), f(c+1)) with f(c) = c Wt / n in fp32: any
+    // monotone f with f(0) = 0 and f(n) = Wt splits it exactly, and every CTA evaluates the
+    // shared boundary the same way.  Then the units that start inside it (unit k of a sequence
+    // starts at its weight offset + k SB).
+    const float per_cta = (float)Wt / (float)gridDim.x;
     auto boundary = [&](uint32_t c) -> uint32_t {
-        if (c >= gridDim.x) return T;
+        if (c >= gridDim.x) return Wt;
         const uint32_t f = (uint32_t)((float)c * per_cta);
-        return f < T ? f : T;
+        return f < Wt ? f : Wt;
     };
     const uint32_t A = boundary(blockIdx.x), E = boundary(blockIdx.x + 1);
     auto units_before = [&](uint32_t X, uint32_t bb, uint32_t nseg) -> uint32_t {
@@ -377,15 +389,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     };
     uint32_t below_a = 0, below_e = 0;
     {
-        uint32_t bb = bb_t, ub = ub_t;
+        uint32_t wb = wb_t;
         for (int b = b0; b < b1; ++b) {
             const int L = own_info(b - b0, false).x;
             const uint32_t nseg = fast_div((uint32_t)(L + S - 1), (uint32_t)S, p.seg_rcp);
             const uint32_t nblk = (uint32_t)((L + kBlockSize - 1) / kBlockSize);
-            below_a += units_before(A, bb, nseg);
-            below_e += units_before(E, bb, nseg);
-            bb += nblk;
-            ub += nseg;
+            below_a += units_before(A, wb, nseg);
+            below_e += units_before(E, wb, nseg);
+            wb += weight_of(nblk, nseg);
         }
     }
     unsigned long long lohi;
@@ -513,7 +524,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             prev_seq = u.x;
             ++run;
             const int qs = run & (nq - 1);
-            if (!mbar_wait(&qfull[qs], (uint32_t)(run >> (nq - 1)) & 1u)) {
+            const bool qok = mbar_wait(&qfull[qs], (uint32_t)(run >> (nq - 1)) & 1u);
+            if (__any_sync(0xffffffffu, !qok)) {   // warp-uniform
                 if (lane == 0) {
                     count_status(p.status, 3);
                     atomicExch(flags, 1);
@@ -579,7 +591,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             for (int b = 0; b < npair; ++b) {
                 if (!mbar_wait(&full[st[b]], (uint32_t)((i + b) / kStages) & 1u)) timed_out = true;
             }
-            if (timed_out) {
+            if (__any_sync(0xffffffffu, timed_out)) {   // warp-uniform
                 if (lane == 0) {
                     count_status(p.status, 3);
                     atomicExch(flags, 1);
@@ -1036,10 +1048,11 @@ cudaError_t decode_by_q(const AttnParams& p, int num_ctas, DType q_dt, DType out
 
 }  // namespace
 
-int decode_grid_size(int64_t max_blocks_total, int64_t max_units) {
+int decode_grid_size(int64_t max_weight_total, int64_t max_units) {
     int64_t n = 2ll * num_sms();
     if (n > max_units) n = max_units;
-    const int64_t need = (max_blocks_total + kMaxUnits - 1) / kMaxUnits;   // at most kMaxUnits unit starts per CTA
+    // a share of weight w holds at most w + 2 unit starts (every unit weighs at least one block)
+    const int64_t need = (max_weight_total + kMaxUnits - 3) / (kMaxUnits - 2);
     if (n < need) n = need;
     if (n < 1) n = 1;
     return n > 0x7FFFFFFF ? 0x7FFFFFFF : (int)n;

@@ -65,7 +65,7 @@ cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStre
 // decode sequence.  num_ctas is the walker's grid (decode_grid_size).
 cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
                           cudaStream_t stream);
-int decode_grid_size(int64_t max_blocks_total, int64_t max_units);
+int decode_grid_size(int64_t max_weight_total, int64_t max_units);
 constexpr int kDecodeMaxUnits = 256;   // split-KV units one walker CTA may own
 
 // Rotated-query record of one decode sequence (32-bit words): per kv head, 32-dimension group and

@@ -123,6 +123,19 @@ def test_segment_longer_than_the_staged_block_table():
     _run_case(wl, segment_len=9600)
 
 
+def test_units_longer_than_a_cta_share():
+    # 6 x 5000 tokens in segments of 2048: 18 units of up to 128 blocks over 18 CTAs whose shares
+    # are about 104 blocks, so most units straddle a boundary (some two) and are taken at run time
+    wl = workloads.make_attention_workload("strad", [5000, 4999, 4097, 5000, 2049, 5000], [1] * 6, 32, 8, 128,
+                                           seed=14)
+    out, _ = _run_case(wl, segment_len=2048)
+    from gpu_helpers import gpu_attention, gpu_cache, gpu_write
+    cache = gpu_cache(wl.num_blocks, 16, 8, 128)
+    gpu_write(wl.key, wl.value, wl.slot_mapping, wl.signs, cache)
+    for _ in range(3):   # whichever CTA takes a shared unit, its arithmetic is the same
+        assert torch.equal(gpu_attention(wl, cache, segment_len=2048), out)
+
+
 def test_many_short_sequences_per_cta():
     # 3000 one-block decode sequences of 1..16 tokens: each walker CTA runs about ten sequences,
     # cycling its rotated-query buffers
