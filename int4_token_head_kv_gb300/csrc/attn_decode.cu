@@ -483,6 +483,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         bulk_copy_g2s(qbuf + (size_t)qs * qrec_bytes, p.ws_q + (size_t)run_seq[r] * p.qrec_words, qrec_bytes,
                       &qfull[qs], policy_evict_first());
     };
+    // Warm L2 with the first blocks while the previous kernels finish: the copies issued after the
+    // wait then hit L2.  (A block the cache write is still updating is safe to prefetch: the copy
+    // after the wait reads L2, where that write lands.)
+    if (threadIdx.x < min(nb_cta, kStages)) {
+        const int blk = tbl[threadIdx.x];
+        if (blk >= 0 && (int64_t)blk < p.num_blocks) bulk_prefetch_l2(p.cache + (int64_t)blk * stage_bytes, stage_bytes);
+    }
     griddep_wait();   // the query records, and through them the cache, come from earlier kernels
     if (blockIdx.x == 0) {   // the combine's sequence index
         uint32_t ub = ub_t;
