@@ -60,12 +60,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     constexpr int TS = Sm::kTileStride;
     constexpr int WPP = kBlockSize * Gm::KW;   // code words of one plane of one block (one head)
     extern __shared__ __align__(128) uint8_t smem[];
-    const int qtile = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+    // blockIdx.x runs over (query tile, kv head) with the last (causally heaviest) tiles first, so
+    // the light tiles fill the end of the schedule; blockIdx.z is the sequence.
+    const int ntile = (int)(gridDim.x / (unsigned)p.H);
+    const int qtile = ntile - 1 - (int)(blockIdx.x / (unsigned)p.H), h = (int)(blockIdx.x % (unsigned)p.H);
+    const int seq = blockIdx.z;
     const int q0 = __ldg(p.qsl + seq);
     const int qlen = __ldg(p.qsl + seq + 1) - q0;
     if (qlen <= 1) return;   // decode sequences (and empty ones) are not this kernel's
     if (q0 < 0 || (int64_t)q0 + qlen > p.num_q_tokens || qlen > p.max_query_len) {
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) count_status(p.status, 2);
+        if (qtile == 0 && h == 0 && threadIdx.x == 0) count_status(p.status, 2);
         if (q0 < 0 || (int64_t)q0 + qlen > p.num_q_tokens) return;
     }
     const int G = p.G, Hq = p.Hq, H = p.H;
@@ -354,7 +358,7 @@ cudaError_t launch_prefill_t(const AttnParams& p, int max_query_len, cudaStream_
     cudaError_t err = opt_in_smem<prefill_kernel<D, QT, OT>>(smem);
     if (err != cudaSuccess) return err;
     const int BQ = kRows / p.G;
-    dim3 grid((max_query_len + BQ - 1) / BQ, p.H, p.num_seqs);
+    dim3 grid((unsigned)(((max_query_len + BQ - 1) / BQ) * p.H), 1, p.num_seqs);
     kern<<<grid, kPrefillThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
