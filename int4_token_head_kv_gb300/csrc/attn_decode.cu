@@ -857,15 +857,41 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     constexpr int SPL = NT / 32;           // slots per lane
     constexpr int UNR = WIDE ? 2 : 4;      // records in flight per lane
     constexpr int SO = D + 4;
+    constexpr int kThreads = kCombineWarps * 32;
     __shared__ float sgn[D];
+    __shared__ int wsum_c[kCombineWarps];
+    __shared__ int first_unit[kThreads];   // batches of up to kThreads sequences: first unit of each
     extern __shared__ __align__(16) float4 cbuf[];
     float4* sacc = cbuf;                                   // [16 warps][NT]
     float4* sml = cbuf + kCombineWarps * NT;               // [16 warps][4]
     float* sout = reinterpret_cast<float*>(sml + kCombineWarps * 4);   // [groups][G][SO]
-    griddep_wait();
-    griddep_launch_dependents();   // the next call's walker may start its set-up
+    // Up to the wait on the walker this kernel reads only host inputs, so it overlaps the walker's
+    // last CTAs on the SMs they have left.
     for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // decode segments of sequence b (0 for other sequences), as the walker counts them
+    auto segments_of = [&](int b) -> int {
+        const int qb = __ldg(p.qsl + b);
+        if (__ldg(p.qsl + b + 1) - qb != 1 || qb < 0 || (int64_t)qb >= p.num_q_tokens) return 0;
+        const int L = min(max(__ldg(p.seq_lens + b), 0), p.len_cap);
+        return (int)fast_div((uint32_t)(L + p.seg_len - 1), (uint32_t)p.seg_len, p.seg_rcp);
+    };
+    const bool local_first = p.num_seqs <= kThreads;   // else the walker's index in ws_meta
+    if (local_first) {
+        const int b = threadIdx.x;
+        const int ns = b < p.num_seqs ? segments_of(b) : 0;
+        int x = ns;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum_c[warp] = x;
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += wsum_c[w];
+        first_unit[b] = before + x - ns;
+    }
     const int W = p.combine_warps, grp = warp / W, sub = warp % W;
     const int H = p.H, G = p.G, Hq = p.Hq;
     const int64_t item = (int64_t)blockIdx.x * (kCombineWarps / W) + grp;
@@ -886,7 +912,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     const int64_t obase = ((int64_t)q0 * Hq + (int64_t)h * G) * D;
     const int ws = p.wph_shift;
     const int R = nseg << ws;
-    const int ub = R > 0 ? p.ws_meta[seq] : 0;
+    __syncthreads();   // first_unit complete
+    griddep_wait();
+    griddep_launch_dependents();   // the next call's kernels may start their set-up
+    const int ub = R > 0 ? (local_first ? first_unit[seq] : p.ws_meta[seq]) : 0;
     auto rec_of = [&](int r) -> size_t {
         return (size_t)(ub + (r >> ws)) * kConsumerWarps + h + (r & ((1 << ws) - 1)) * H;
     };
