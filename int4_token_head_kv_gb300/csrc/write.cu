@@ -132,7 +132,8 @@ __device__ __forceinline__ void encode_vector(float (&u)[D], float c, uint32_t (
 // Work split: vectors are numbered v = (t * 2 + plane) * H + h, so H consecutive vectors are one
 // (token, plane) row group, contiguous in the cache.  Each warp owns tiles of 32 consecutive
 // vectors and works through them on its own (no CTA-wide barriers): it prefetches the next tile's
-// inputs with coalesced 16-byte cp.async copies into one of two padded shared-memory buffers
+// inputs, one bulk async copy of 2D bytes per lane (its vector) completing on the buffer's
+// mbarrier, into one of two padded shared-memory buffers
 // (row stride 2D + 16 bytes, so the 16-byte reads of 8 neighbouring rows hit distinct banks),
 // encodes the current tile with one vector per lane, stages the encoded rows in the buffer it just
 // read, and writes each row group with one bulk async store (when H divides 32 and a group is a
@@ -145,14 +146,10 @@ struct WriteSmem {
     static constexpr int kRowPad = 2 * D + 16;
     static constexpr int kBuf = kWarpVecs * kRowPad;            // one tile of inputs
     static constexpr int kPerWarp = 2 * kBuf;
-    static constexpr int kBytes = kWriteWarps * kPerWarp + (D / 2) * 4;
+    static constexpr int kBars = kWriteWarps * kPerWarp;        // two mbarriers per warp
+    static constexpr int kBytes = kBars + kWriteWarps * 2 * 8 + (D / 2) * 4;
 };
 
-__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 __device__ __forceinline__ void bulk_store_s2g(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
@@ -190,7 +187,13 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
     griddep_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint8_t* wbuf = smem + warp * Sm::kPerWarp;
-    uint32_t* sign_mask = reinterpret_cast<uint32_t*>(smem + kWriteWarps * Sm::kPerWarp);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::kBars) + warp * 2;   // this warp's [buffer]
+    uint32_t* sign_mask = reinterpret_cast<uint32_t*>(smem + Sm::kBars + kWriteWarps * 2 * 8);
+    if (lane == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
     for (int j = tid; j < D / 2; j += kWriteThreads) {
         const float s0 = p.signs[2 * j], s1 = p.signs[2 * j + 1];
         sign_mask[j] = ((__float_as_uint(s0) >> 31) << 15) | ((__float_as_uint(s1) >> 31) << 31);
@@ -206,42 +209,42 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
     const uint32_t nvec = (uint32_t)(p.num_tokens * H * 2);
     const uint32_t ntiles = (nvec + kWarpVecs - 1) / kWarpVecs;
     const uint32_t gwarp = blockIdx.x * kWriteWarps + warp, nwarps = gridDim.x * kWriteWarps;
-    constexpr int kChunks = D * 2 / 16;                 // 16-byte chunks per input vector
     const uint32_t group_bytes = H * Gm::RB;
     const bool grouped = vx.hshift >= 0 && H <= (uint32_t)kWarpVecs && (group_bytes % 16) == 0;
     const uint8_t* kin = static_cast<const uint8_t*>(p.k);
     const uint8_t* vin = static_cast<const uint8_t*>(p.v);
 
-    // lane copies chunks lane + 32 k of the tile: vector (lane + 32 k) / kChunks, chunk (lane % kChunks)
-    auto prefetch = [&](uint32_t tile, uint8_t* buf) {
+    // lane copies its vector of the tile (2D bytes) into row lane of the buffer
+    auto prefetch = [&](uint32_t tile, uint8_t* buf, uint64_t* bar) {
         const uint32_t v0 = tile * kWarpVecs;
-#pragma unroll
-        for (int k = 0; k < kChunks; ++k) {
-            const uint32_t ci = lane + 32 * k;
-            const uint32_t vl = ci / kChunks, c = ci % kChunks;
-            if (v0 + vl < nvec) {
-                uint32_t tok, h, pl;
-                vx.split(v0 + vl, tok, h, pl);
-                const uint8_t* src = (pl ? vin : kin) + ((uint64_t)(tok * H + h) * (D * 2) + c * 16);
-                cp_async_16(buf + vl * Sm::kRowPad + c * 16, src);
-            }
+        const uint32_t live_vecs = min((uint32_t)kWarpVecs, nvec - v0);
+        if (lane == 0) mbar_arrive_expect_tx(bar, live_vecs * (uint32_t)(D * 2));
+        __syncwarp();
+        if ((uint32_t)lane < live_vecs) {
+            uint32_t tok, h, pl;
+            vx.split(v0 + lane, tok, h, pl);
+            bulk_copy_g2s(buf + lane * Sm::kRowPad, (pl ? vin : kin) + (uint64_t)(tok * H + h) * (D * 2), D * 2, bar,
+                          policy_evict_first());
         }
-        cp_async_commit();
     };
 
     uint32_t tile = gwarp;
     int it = 0;
-    if (tile < ntiles) prefetch(tile, wbuf);
+    bool waited_out = false;
+    if (tile < ntiles) prefetch(tile, wbuf, &bars[0]);
     for (; tile < ntiles; tile += nwarps, ++it) {
         uint8_t* cur = wbuf + (it & 1) * Sm::kBuf;
         uint8_t* nxt = wbuf + ((it + 1) & 1) * Sm::kBuf;
         // the other buffer was last an output stage: its bulk stores must have read it
         if (grouped) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncwarp();
-        if (tile + nwarps < ntiles) prefetch(tile + nwarps, nxt);
-        else cp_async_commit();   // keep one group per iteration
-        cp_async_wait_1();
-        __syncwarp();
+        if (tile + nwarps < ntiles) prefetch(tile + nwarps, nxt, &bars[(it + 1) & 1]);
+        // this tile's rows: use (it >> 1) of buffer it & 1
+        if (__any_sync(0xffffffffu, !mbar_wait(&bars[it & 1], (uint32_t)(it >> 1) & 1u))) {
+            if (lane == 0) count_status(p.status, 3);
+            waited_out = true;
+            break;
+        }
         const uint32_t v = tile * kWarpVecs + lane;
         const bool live = v < nvec;
         float u[D];
@@ -282,7 +285,9 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
             }
         }
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (waited_out && tile + nwarps < ntiles) {   // let the copy in flight land before the warp exits
+        (void)mbar_wait(&bars[(it + 1) & 1], (uint32_t)((it + 1) >> 1) & 1u);
+    }
     if (grouped) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     (void)kRoundMagicBits;
 }
