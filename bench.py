@@ -426,6 +426,23 @@ def _extra(torch, kv, workloads, dev, args):
     return res
 
 
+def _only(args):
+    """One workload's attention call, timed as in --extra, on its own (no decode-batch steps)."""
+    import torch
+
+    import int4_token_head_kv_gb300 as kv
+    import workloads
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    peak, _ = _peaks()
+    wl = getattr(workloads, args.only)(seed=args.seed)
+    ms, seg = _attention_only(torch, kv, wl, dev, reps=10)
+    kvb = int(wl.seq_lens.sum()) * 2 * wl.num_kv_heads * kv.kv_int4_row_bytes(wl.head_size) + 2 * wl.query.numel() * 2
+    print(json.dumps({"only": args.only, "ms": round(ms, 4), "GB/s": round(kvb / ms / 1e6, 1),
+                      "frac": round(kvb / ms / 1e6 / peak, 4), "bytes": kvb, "segment_len": seg}))
+
+
 def _cpu_baseline(kind, args, nsample=None):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
     n = nsample if nsample is not None else (2 if kind == "decode" else 2048)
@@ -511,7 +528,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra", action="store_true",
                     help="also time the long-context and mixed prefill+decode workloads (attention call only)")
+    ap.add_argument("--only", choices=["long_context_decode", "mixed_prefill_decode"],
+                    help="time just this workload's attention call and print its own JSON line (for profiling)")
     args = ap.parse_args()
+    if args.only:
+        _only(args)
+        return
     if args.impl == "reference":
         # the oracle runs single-threaded; fix BLAS threads before numpy loads
         for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
