@@ -134,7 +134,8 @@ int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int
  * into segments of segment_len tokens (segment k of a sequence holds its tokens
  * [k segment_len, (k+1) segment_len)), a grid of about two CTAs per SM walks the batch's segments
  * in runs balanced by cache blocks, each segment writes a (max, sum, output) partial, and a
- * combine step merges each sequence's partials in segment order.  A segment's arithmetic does not
+ * combine step merges each sequence's partials in an order fixed by that sequence's segment count
+ * alone.  A segment's arithmetic does not
  * depend on the rest of the batch, so for a fixed segment_len a sequence's output is the same
  * alone or in any batch.  Sequences with more than one query token take the chunked-prefill
  * kernel.

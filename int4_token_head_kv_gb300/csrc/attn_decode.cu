@@ -23,12 +23,13 @@
 //
 // Walker CTA:
 //  * All kv heads of a 16-token block are one contiguous, 16-byte-aligned region (K plane then V
-//    plane, 2 * 16 * H * (D/2+4) bytes) streamed through a 4-stage shared-memory ring by 1-D bulk
-//    async copies (cp.async.bulk + mbarrier transaction counts, L2 evict-first).  The ring runs
-//    across unit boundaries.  There is no producer warp: the CTA's block ids are staged in shared
-//    memory up front, four lanes issue the first four copies, and the last consumer warp to
-//    finish with a stage issues its next block.  The rotated-query record of each run of units of
-//    one sequence arrives the same way.
+//    plane, 2 * 16 * H * (D/2+4) bytes) streamed through a shared-memory ring (5 stages, 4 with
+//    eight query heads per kv head) by 1-D bulk async copies (cp.async.bulk + mbarrier
+//    transaction counts, L2 evict-first).  The ring runs across unit boundaries.  There is no
+//    producer warp: the CTA's block ids are staged in shared memory up front (and its first
+//    blocks prefetched into L2 while the previous kernels finish), thread 0 issues the first
+//    copies, and the last consumer warp to finish with a stage issues its next block.  The
+//    rotated-query record of each run of units of one sequence arrives the same way.
 //  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block pair when H < 8).
 //    Split-dot scores over the even and odd nibble streams: each code word is unpacked into the
 //    raw codes as exact fp16 integers (even codes through fp16 1024 + e, odd codes through
