@@ -355,6 +355,33 @@ def _write_bench(torch, kv, workloads, dev, stream, args):
                          "peak_source": kind}}
 
 
+def _int8_write_bench(torch, kv, workloads, dev, args):
+    """The INT8 per-(token, head) comparator's write on the same workload (cache rows d + 4 bytes)."""
+    wl = workloads.write_throughput(seed=args.seed)
+    H, d = wl.num_kv_heads, wl.head_size
+    k, v = wl.key.to(dev), wl.value.to(dev)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    cache = torch.zeros(kv.kv_int8_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+    nbytes = wl.num_tokens * (2 * H * d * k.element_size() + 2 * H * kv.kv_int8_row_bytes(d) + 8)
+    reps = 200
+    for _ in range(5):
+        kv.kv_int8_write(k, v, slots, cache)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        kv.kv_int8_write(k, v, slots, cache)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    peak, _ = _peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"tokens_per_s": round(wl.num_tokens / (ms * 1e-3), 1), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "ms_per_call": round(ms, 5), "bytes_per_call": nbytes,
+            "cache_bytes_per_token": 2 * H * kv.kv_int8_row_bytes(d),
+            "int4_cache_bytes_per_token": 2 * H * kv.kv_int4_row_bytes(d)}
+
+
 # ------------------------------------------------------------------------------- CPU oracle
 
 def _attention_only(torch, kv, wl, dev, reps, rows=None, segment_len=0):
@@ -423,6 +450,7 @@ def _extra(torch, kv, workloads, dev, args):
     ms_p, _ = _attention_only(torch, kv, pre, dev, reps=10)
     res["mixed_prefill_decode"]["prefill_part_ms"] = round(ms_p, 4)
     res["mixed_prefill_decode"]["prefill_part_TFLOP/s"] = round(flops / ms_p / 1e9, 1)
+    res["int8_write_comparator"] = _int8_write_bench(torch, kv, workloads, dev, args)
     return res
 
 

@@ -4,6 +4,7 @@
  * Two operations, both asynchronous on the caller's CUDA stream:
  *
  *   kv_int4_write            rotate, quantise and pack new K/V head vectors into a paged cache;
+ *   kv_int8_write            the INT8 per-(token, head) comparator's cache write;
  *   kv_int4_paged_attention  causal attention of queries over that cache (decode, split-KV
  *                            segments, chunked prefill).
  *
@@ -98,6 +99,31 @@ kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, 
                              int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
                              const float* rht_signs, uint8_t* cache, int64_t num_blocks,
                              int32_t block_size, kv_int4_stream_t stream);
+
+/*
+ * INT8 per-(token, head) comparator rows: head_size int8 codes, then the fp32 scale word
+ * (head_size + 4 bytes; "PR #40835 report", get_kv_cache_shape for the non-INT4 per-token-head
+ * modes).
+ */
+int32_t kv_int8_row_bytes(int32_t head_size);
+
+/*
+ * kv_int8_write -- the INT8 per-(token, head) cache write, the comparator the pages measure the
+ * INT4 mode against ("tests/quantization/test_per_token_kv_cache.py", INT8_CONFIG and
+ * _quantize_per_token_head_ref; the round-half-away fix of the INT8 reshape kernel in
+ * "[Feature] Triton INT4 / INT2 per-token-head KV cache quantization").  No rotation and no
+ * zero-point: per (token, kv head, plane) vector x,
+ *   s = max(fp32(max|x_i| / 127), 1e-6), r = fp32(1 / s),
+ *   q_i = clamp(trunc(fp32(fp32(x_i * r) + (x_i * r >= 0 ? 0.5 : -0.5))), -128, 127),
+ * stored as q_0 .. q_{d-1} (two's complement) then the little-endian bits of s, at
+ * cache[slot / 16][plane][slot % 16][head] of a (num_blocks, 2, 16, num_kv_heads, head_size + 4)
+ * uint8 cache.  Arguments, validation, skipped slots and error behaviour as kv_int4_write (there
+ * are no signs).
+ */
+kv_int4_status kv_int8_write(const void* k, const void* v, kv_int4_dtype dtype, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
+                             uint8_t* cache, int64_t num_blocks, int32_t block_size,
+                             kv_int4_stream_t stream);
 
 /*
  * Bytes of workspace kv_int4_paged_attention needs for these sizes (same arguments as the

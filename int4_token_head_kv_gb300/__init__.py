@@ -42,6 +42,10 @@ def _load():
     lib.kv_int4_status_string.restype = ctypes.c_char_p
     lib.kv_int4_write.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, vp, vp, i64, i32, vp]
     lib.kv_int4_write.restype = ctypes.c_int
+    lib.kv_int8_row_bytes.argtypes = [i32]
+    lib.kv_int8_row_bytes.restype = i32
+    lib.kv_int8_write.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, vp, i64, i32, vp]
+    lib.kv_int8_write.restype = ctypes.c_int
     lib.kv_int4_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.kv_int4_attention_workspace_bytes.restype = szt
     lib.kv_int4_attention_segment_len.argtypes = [i32, i32, i32]
@@ -119,6 +123,35 @@ def kv_int4_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Te
                             rht_signs.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2],
                             _stream(stream))
     _check("kv_int4_write", st)
+
+
+def kv_int8_row_bytes(head_size: int) -> int:
+    return int(load().kv_int8_row_bytes(head_size))
+
+
+def kv_int8_cache_shape(num_blocks: int, block_size: int, num_kv_heads: int, head_size: int):
+    """INT8 per-(token, head) comparator cache: (num_blocks, 2, block_size, H, head_size + 4) uint8."""
+    return (num_blocks, 2, block_size, num_kv_heads, kv_int8_row_bytes(head_size))
+
+
+def kv_int8_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor, kv_cache: torch.Tensor,
+                  stream=None) -> None:
+    """Quantise ``key``/``value`` [T, H, d] to INT8 per-(token, head) rows of ``kv_cache`` at ``slot_mapping``."""
+    _cuda(key, "key", (torch.float16, torch.bfloat16))
+    _cuda(value, "value", (key.dtype,))
+    _cuda(slot_mapping, "slot_mapping", (torch.int64,))
+    _cuda(kv_cache, "kv_cache", (torch.uint8,))
+    if key.dim() != 3 or value.shape != key.shape:
+        raise ValueError("key and value must both be [num_tokens, num_kv_heads, head_size]")
+    T, H, d = key.shape
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.shape[3] != H or \
+            kv_cache.shape[4] != kv_int8_row_bytes(d):
+        raise ValueError(f"kv_cache must be {kv_int8_cache_shape('NB', 'bs', H, d)}")
+    st = load().kv_int8_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
+                            kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], _stream(stream))
+    _check("kv_int8_write", st)
 
 
 def kv_int4_attention_segment_len(num_seqs: int, max_seq_len: int, segment_len: int = 0) -> int:

@@ -123,6 +123,33 @@ kv_int4_status kv_int4_write(const void* k, const void* v, kv_int4_dtype dtype, 
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int32_t kv_int8_row_bytes(int32_t head_size) { return head_size > 0 ? head_size + 4 : 0; }
+
+kv_int4_status kv_int8_write(const void* k, const void* v, kv_int4_dtype dtype, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping, uint8_t* cache,
+                             int64_t num_blocks, int32_t block_size, kv_int4_stream_t stream) {
+    if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0) return KV_INT4_EINVAL;
+    if (head_size != 64 && head_size != 128) return KV_INT4_EUNSUPPORTED;
+    if (block_size != kBlockSize || num_kv_heads > 64 || !valid_dtype_16(dtype)) return KV_INT4_EUNSUPPORTED;
+    if (num_tokens == 0) return KV_INT4_OK;
+    if (num_tokens * num_kv_heads * 2 >= (int64_t)1 << 31) return KV_INT4_EUNSUPPORTED;   // 32-bit vector index
+    if (!k || !v || !slot_mapping || !cache) return KV_INT4_EINVAL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(cache)) return KV_INT4_EALIGN;
+    WriteParams p;
+    p.k = k;
+    p.v = v;
+    p.slots = slot_mapping;
+    p.signs = nullptr;
+    p.cache = cache;
+    p.status = status_ptr();
+    p.num_tokens = num_tokens;
+    p.num_slots = num_blocks * block_size;
+    p.H = num_kv_heads;
+    p.c = 1.0f;
+    return from_cuda(launch_write_int8(p, head_size, dtype == KV_INT4_BF16 ? DType::BF16 : DType::F16,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
     if (num_seqs < 0 || max_seq_len < 0 || segment_len < 0) return 0;
     if (segment_len > 0) return (segment_len % kBlockSize == 0) ? segment_len : 0;

@@ -61,6 +61,8 @@ struct AttnParams {
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
+// INT8 per-(token, head) comparator rows (D codes + fp32 scale); p.signs and p.c are not used.
+cudaError_t launch_write_int8(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
 // Decode path: query rotation, the split-KV segment walker, and the combine that finishes every
 // decode sequence.  num_ctas is the walker's grid (decode_grid_size).
 cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,

@@ -129,6 +129,53 @@ __device__ __forceinline__ void encode_vector(float (&u)[D], float c, uint32_t (
     words[Gm::KW] = sb | zp;
 }
 
+// INT8 per-(token, head) comparator ("tests/quantization/test_per_token_kv_cache.py",
+// _quantize_per_token_head_ref with INT8_CONFIG; rounding as in the INT8 reshape-kernel fix of
+// "[Feature] Triton INT4 / INT2 per-token-head KV cache quantization"): no rotation, no zero-point,
+//   s = max(fp32(max|x| / 127), 1e-6); r = fp32(1 / s);
+//   q = clamp(trunc(fp32(fp32(x * r) + (x * r >= 0 ? 0.5 : -0.5))), -128, 127),
+// stored as D two's-complement bytes then the bits of s.
+template <int D, typename T>
+__device__ __forceinline__ void load_vector_raw(const uint4* src, float (&u)[D]) {
+#pragma unroll
+    for (int cc = 0; cc < D / 8; ++cc) {
+        const uint4 q = src[cc];
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = upcast_pair<T>(w4[e]);
+            u[2 * (cc * 4 + e)] = x.x;
+            u[2 * (cc * 4 + e) + 1] = x.y;
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void encode_vector_int8(const float (&u)[D], uint32_t (&words)[D / 4 + 1]) {
+    float a0 = fabsf(u[0]), a1 = fabsf(u[1]);
+#pragma unroll
+    for (int i = 2; i < D; i += 4) {
+        a0 = max3(a0, fabsf(u[i]), fabsf(u[i + 1]));
+        if (i + 3 < D) a1 = max3(a1, fabsf(u[i + 2]), fabsf(u[i + 3]));
+    }
+    float s = __fdiv_rn(fmaxf(a0, a1), 127.0f);
+    if (!(s >= 1e-6f)) s = 1e-6f;
+    const float r = __frcp_rn(s);
+#pragma unroll
+    for (int wi = 0; wi < D / 4; ++wi) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float v = __fmul_rn(u[wi * 4 + k], r);
+            int c = __float2int_rz(__fadd_rn(v, v >= 0.0f ? 0.5f : -0.5f));
+            c = c < -128 ? -128 : (c > 127 ? 127 : c);
+            w |= ((uint32_t)c & 0xFFu) << (8 * k);
+        }
+        words[wi] = w;
+    }
+    words[D / 4] = __float_as_uint(s);
+}
+
 // Work split: vectors are numbered v = (t * 2 + plane) * H + h, so H consecutive vectors are one
 // (token, plane) row group, contiguous in the cache.  Each warp owns tiles of 32 consecutive
 // vectors and works through them on its own (no CTA-wide barriers): it prefetches the next tile's
@@ -176,9 +223,11 @@ struct VecIndex {
     }
 };
 
-template <int D, typename T>
+template <int D, typename T, bool INT8>
 __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_constant__ WriteParams p) {
     using Gm = Geo<D>;
+    constexpr int RB = INT8 ? D + 4 : Gm::RB;       // cache row bytes
+    constexpr int NW = INT8 ? D / 4 : Gm::KW;       // code words per row (then the scale word)
     using Sm = WriteSmem<D>;
     extern __shared__ __align__(128) uint8_t smem[];
     // Launched as a programmatic dependent: wait for the previous kernel of the stream (it may
@@ -194,7 +243,7 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
         mbar_init(&bars[1], 1);
         fence_mbar_init();
     }
-    for (int j = tid; j < D / 2; j += kWriteThreads) {
+    for (int j = tid; j < (INT8 ? 0 : D / 2); j += kWriteThreads) {   // INT8 rows take no signs
         const float s0 = p.signs[2 * j], s1 = p.signs[2 * j + 1];
         sign_mask[j] = ((__float_as_uint(s0) >> 31) << 15) | ((__float_as_uint(s1) >> 31) << 31);
         if (blockIdx.x == 0 && ((fabsf(s0) != 1.0f) || (fabsf(s1) != 1.0f))) count_status(p.status, 4);
@@ -209,7 +258,7 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
     const uint32_t nvec = (uint32_t)(p.num_tokens * H * 2);
     const uint32_t ntiles = (nvec + kWarpVecs - 1) / kWarpVecs;
     const uint32_t gwarp = blockIdx.x * kWriteWarps + warp, nwarps = gridDim.x * kWriteWarps;
-    const uint32_t group_bytes = H * Gm::RB;
+    const uint32_t group_bytes = H * RB;
     const bool grouped = vx.hshift >= 0 && H <= (uint32_t)kWarpVecs && (group_bytes % 16) == 0;
     const uint8_t* kin = static_cast<const uint8_t*>(p.k);
     const uint8_t* vin = static_cast<const uint8_t*>(p.v);
@@ -248,17 +297,23 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
         const uint32_t v = tile * kWarpVecs + lane;
         const bool live = v < nvec;
         float u[D];
-        if (live) load_vector<D, T>(reinterpret_cast<const uint4*>(cur + lane * Sm::kRowPad), sign_mask, u);
-        __syncwarp();   // the tile's inputs are in registers; its buffer becomes the output stage
-        uint32_t words[Gm::KW + 1];
-        if (live) encode_vector<D>(u, p.c, words);
+        uint32_t words[NW + 1];
+        if constexpr (INT8) {
+            if (live) load_vector_raw<D, T>(reinterpret_cast<const uint4*>(cur + lane * Sm::kRowPad), u);
+            __syncwarp();   // the tile's inputs are in registers; its buffer becomes the output stage
+            if (live) encode_vector_int8<D>(u, words);
+        } else {
+            if (live) load_vector<D, T>(reinterpret_cast<const uint4*>(cur + lane * Sm::kRowPad), sign_mask, u);
+            __syncwarp();   // the tile's inputs are in registers; its buffer becomes the output stage
+            if (live) encode_vector<D>(u, p.c, words);
+        }
         uint32_t tok = 0, h = 0, pl = 0;
         if (live) vx.split(v, tok, h, pl);
         if (grouped) {
-            uint32_t* orow = reinterpret_cast<uint32_t*>(cur + lane * Gm::RB);
+            uint32_t* orow = reinterpret_cast<uint32_t*>(cur + lane * RB);
             if (live) {
 #pragma unroll
-                for (int wi = 0; wi <= Gm::KW; ++wi) orow[wi] = words[wi];
+                for (int wi = 0; wi <= NW; ++wi) orow[wi] = words[wi];
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staged rows -> bulk store
             __syncwarp();
@@ -270,7 +325,7 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
                 } else if (slot >= 0) {
                     const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
                     bulk_store_s2g(p.cache + ((blk * 2 + pl) * kBlockSize + off) * (int64_t)group_bytes,
-                                   cur + lane * Gm::RB, group_bytes);
+                                   cur + lane * RB, group_bytes);
                 }
             }
         } else if (live) {
@@ -279,9 +334,9 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
                 if (pl == 0 && h == 0) count_status(p.status, 0);
             } else if (slot >= 0) {
                 const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-                uint32_t* row = reinterpret_cast<uint32_t*>(p.cache + (((blk * 2 + pl) * kBlockSize + off) * H + h) * Gm::RB);
+                uint32_t* row = reinterpret_cast<uint32_t*>(p.cache + (((blk * 2 + pl) * kBlockSize + off) * H + h) * RB);
 #pragma unroll
-                for (int wi = 0; wi <= Gm::KW; ++wi) row[wi] = words[wi];
+                for (int wi = 0; wi <= NW; ++wi) row[wi] = words[wi];
             }
         }
     }
@@ -292,7 +347,7 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
     (void)kRoundMagicBits;
 }
 
-template <int D, typename T>
+template <int D, typename T, bool INT8>
 cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
     using Sm = WriteSmem<D>;
     const int64_t ntiles = (p.num_tokens * p.H * 2 + kWarpVecs - 1) / kWarpVecs;
@@ -300,7 +355,7 @@ cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
     const int64_t cap = (int64_t)num_sms() * 3;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    cudaError_t err = opt_in_smem<write_kernel<D, T>>(Sm::kBytes);
+    cudaError_t err = opt_in_smem<write_kernel<D, T, INT8>>(Sm::kBytes);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -312,16 +367,29 @@ cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, write_kernel<D, T>, p);
+    return cudaLaunchKernelEx(&cfg, write_kernel<D, T, INT8>, p);
 }
 
 }  // namespace
 
-cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
+namespace {
+template <bool INT8>
+cudaError_t launch_write_mode(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
     if (head_size == 128) {
-        return dt == DType::BF16 ? launch_write_t<128, __nv_bfloat16>(p, stream) : launch_write_t<128, __half>(p, stream);
+        return dt == DType::BF16 ? launch_write_t<128, __nv_bfloat16, INT8>(p, stream)
+                                 : launch_write_t<128, __half, INT8>(p, stream);
     }
-    return dt == DType::BF16 ? launch_write_t<64, __nv_bfloat16>(p, stream) : launch_write_t<64, __half>(p, stream);
+    return dt == DType::BF16 ? launch_write_t<64, __nv_bfloat16, INT8>(p, stream)
+                             : launch_write_t<64, __half, INT8>(p, stream);
+}
+}  // namespace
+
+cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
+    return launch_write_mode<false>(p, head_size, dt, stream);
+}
+
+cudaError_t launch_write_int8(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
+    return launch_write_mode<true>(p, head_size, dt, stream);
 }
 
 }  // namespace kvi4

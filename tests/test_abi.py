@@ -48,6 +48,19 @@ def test_host_side_validation(lib):
     assert lib.kv_int4_write(fake + 2, fake, 1, 4, 2, 128, fake, fake, fake, 8, 16, None) == 3
     # nothing to do
     assert lib.kv_int4_write(None, None, 1, 0, 2, 128, None, None, None, 8, 16, None) == 0
+    # the INT8 comparator's write validates the same way (no signs argument)
+    lib.kv_int8_write.restype = ctypes.c_int
+    lib.kv_int8_write.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                          ctypes.c_int32, ctypes.c_void_p]
+    assert lib.kv_int8_write(fake, fake, 1, 4, 2, 96, fake, fake, 8, 16, None) == 2
+    assert lib.kv_int8_write(fake, fake, 1, 4, 2, 128, fake, fake, 8, 32, None) == 2
+    assert lib.kv_int8_write(fake, fake, 1, -1, 2, 128, fake, fake, 8, 16, None) == 1
+    assert lib.kv_int8_write(fake, None, 1, 4, 2, 128, fake, fake, 8, 16, None) == 1
+    assert lib.kv_int8_write(fake, fake + 8, 1, 4, 2, 128, fake, fake, 8, 16, None) == 3
+    assert lib.kv_int8_write(None, None, 1, 0, 2, 128, None, None, 8, 16, None) == 0
+    lib.kv_int8_row_bytes.restype = ctypes.c_int32
+    assert lib.kv_int8_row_bytes(128) == 132 and lib.kv_int8_row_bytes(64) == 68
 
 
 def test_attention_validation_and_workspace_policy(lib):
