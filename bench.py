@@ -1,35 +1,42 @@
 """Benchmark of the INT4 per-(token, head) KV cache on GB300; prints ONE JSON line (rank 0).
 
-A step is one pass of the whole hot path over one batch of the GQA decode workload
-(32 sequences with lengths uniform in [512, 4096], 32 q / 8 kv heads, head size 128, block 16,
-bf16, 4 loud K channels per kv head): write the step's 32 new tokens into the paged INT4 cache
-(rotation, quantisation, packing), then run causal paged attention of the 32 queries over the
-whole cache.
+Headline: the long-context decode workload (8 sequences x 131072 tokens, 64 q / 8 kv heads, head
+size 128, block 16, bf16 Student-t(3) K/V, randomly permuted blocks).  A step is one pass of the
+whole hot path over one batch: write the step's 8 new tokens (one per sequence) into the paged
+INT4 cache (rotation, quantisation, packing), then run causal paged attention of the 8 queries over
+the whole cache (query rotation, split-KV walker, segment combine).
 
-  value   packed-KV GB/s of the decode step: bytes of packed K/V rows (codes + scales) the
-          attention reads, plus Q and O, per step, over the device-timed step (write included).
-  e2e     the same bytes over a step timed through the public API from pinned host buffers:
-          each step copies its new K/V, slots, queries and tables host->device (one copy of the
-          packed step inputs) and the output device->host; the step (copies included) is replayed
-          as a CUDA graph, as a serving loop runs decode steps (the eager Python loop is reported
-          beside it).
-  write   the write-throughput workload (65536 tokens, 8 kv heads, d 128, bf16, per-token
-          magnitudes 10^U(-2,2), random slots over 8192 blocks): tokens/s and GB/s.
-  roofline  for the dominant kernel call (the attention: query rotation + decode kernel + segment combine), bytes
-          per launch over its CUDA-event time on the launching stream, against the measured HBM
-          copy bandwidth; ``traffic`` is the ncu DRAM byte count of the decode kernel when a
-          summary with it is committed under profiles/, else null.
+  value     packed-KV GB/s of the step: bytes of packed K/V rows (codes + scales) the attention
+            reads, plus Q and O, per step, over the device-timed step (write included).  The cache
+            (1.14 GB) is larger than L2, so no flush is needed between steps.
+  e2e       the same bytes over a step timed through the public API from pinned host buffers: each
+            step copies its new K/V, slots, queries and tables host->device (one copy of the packed
+            step inputs) and the output device->host, replayed as one CUDA graph per step.
+  roofline  the attention call (query rotation + walker + combine) timed back to back on its stream,
+            algorithmic bytes per call over its CUDA-event time, against MEASURED_PEAKS.json's HBM
+            copy bandwidth; ``traffic`` is the ncu DRAM byte count per call from profiles/traffic.json,
+            null when the kernel sources changed since it was taken.
+  cpu_baseline  the oracle on a bounded sample of the same workload: single-threaded, and on all host
+            cores (one process per core).
 
-L2 (129 MB) is defeated by rotating the steps over several independent cache replicas whose total
-exceeds twice the L2 size.  Runs as N independent replicas under torchrun (the path does not
-shard across GPUs; each rank runs the same workload, no collective on the data path).
-``--impl reference`` times the CPU oracle on a bounded sample of the same workload instead.
+Sub-objects (each with its own roofline): ``gqa_decode_batch`` (32 sequences, lengths U[512, 4096],
+32 q / 8 kv heads, steps rotated over cache replicas larger than 2x L2), ``write`` (65536 tokens,
+8 kv heads), ``mixed_prefill_decode`` (4 prefill chunks of 2048 queries over 4096 keys + 60 decode
+sequences: whole-call HBM fraction and the prefill part's dense-equivalent TFLOP/s against the
+measured bf16 tensor peak), ``int8_comparator`` (the INT8 per-(token, head) cache write on the
+write workload).
+
+Runs as N independent replicas under torchrun (the path does not shard across GPUs; no collective on
+the data path); ``--gpus N`` without torchrun starts the N local ranks itself.  ``--impl reference``
+times the CPU oracle on a bounded sample of the headline workload instead.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -42,25 +49,41 @@ if ROOT not in sys.path:
 METRIC = "decode attn packed-KV GB/s (% HBM peak) at 1 GB300; write tokens/s"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+CSRC = os.path.join(ROOT, "int4_token_head_kv_gb300", "csrc")
 
 
 def _peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, source) from MEASURED_PEAKS.json, else the fallback figures."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def _traffic(kernel_key):
-    """DRAM bytes per launch from a committed ncu summary (profiles/traffic.json), if present."""
+def sources_sha() -> str:
+    """Digest of the CUDA sources: a committed ncu traffic figure is valid only for this digest."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(key):
+    """DRAM bytes per launch from profiles/traffic.json when taken on the current sources, else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
-        return t.get(kernel_key)
+        e = t.get(key)
+        if isinstance(e, dict) and e.get("sources_sha") == sources_sha():
+            return e.get("bytes")
     except Exception:
-        return None
+        pass
+    return None
 
 
 class ClockSampler:
@@ -129,10 +152,46 @@ def _dist():
     return world, rank, local
 
 
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_local_ranks(nproc: int, argv) -> int:
+    """Run this script as ``nproc`` local ranks under torch.distributed.run (rendezvous on 127.0.0.1)
+    and return the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={nproc}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd, cwd=ROOT)
+
+
 # ----------------------------------------------------------------------------------- GPU arm
 
+def _timed(torch, stream, fn, n):
+    """Device time (ms) of ``n`` calls of fn(i), CUDA events on the launching stream, synchronised on
+    both sides."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def _write_history(torch, kv, wl, dev, signs, cache, rows):
+    step = 1 << 18
+    for r0 in range(0, len(rows), step):
+        idx = rows[r0:r0 + step]
+        kv.kv_int4_write(wl.key[idx].to(dev), wl.value[idx].to(dev),
+                         torch.from_numpy(wl.slot_mapping[idx]).to(dev), signs, cache)
+
+
 def _decode_setup(torch, kv, wl, dev, replicas):
-    """Cache replicas holding every sequence's history, and the step's device inputs."""
+    """Cache replicas holding every sequence's history, and the step's device inputs (one packed
+    device buffer filled from one pinned host buffer)."""
     H, d = wl.num_kv_heads, wl.head_size
     signs = torch.from_numpy(wl.signs).to(dev)
     hist = wl.history_token_rows()
@@ -140,8 +199,7 @@ def _decode_setup(torch, kv, wl, dev, replicas):
     caches = []
     for _ in range(replicas):
         c = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, wl.block_size, H, d), dtype=torch.uint8, device=dev)
-        kv.kv_int4_write(wl.key[hist].to(dev), wl.value[hist].to(dev),
-                         torch.from_numpy(wl.slot_mapping[hist]).to(dev), signs, c)
+        _write_history(torch, kv, wl, dev, signs, c, hist)
         caches.append(c)
     parts = {
         "k": wl.key[new].contiguous(),
@@ -152,8 +210,6 @@ def _decode_setup(torch, kv, wl, dev, replicas):
         "lens": torch.from_numpy(wl.seq_lens.copy()),
         "qsl": torch.from_numpy(wl.query_start_loc.copy()),
     }
-    # A step's inputs live in one pinned host buffer and one device buffer (256-byte aligned
-    # slices), so a step uploads them with a single copy.
     offs, total = {}, 0
     for k, v in parts.items():
         offs[k] = total
@@ -171,35 +227,21 @@ def _decode_setup(torch, kv, wl, dev, replicas):
     return caches, host, devt
 
 
-def _gpu_arm(args):
-    import torch
-
-    import int4_token_head_kv_gb300 as kv
-    import workloads
-
-    world, rank, local = _dist()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
+def _decode_steps(torch, kv, wl, dev, args, replicas, world, with_e2e=False, sample_clocks=False, local=0):
+    """Time decode steps (write the step's new tokens + attention) on ``wl``: whole steps, the
+    attention call alone, the eager loop, and (optionally) end to end from host buffers."""
     stream = torch.cuda.current_stream()
-
-    wl = workloads.gqa_decode_batch(seed=args.seed)
     H, d, Hq = wl.num_kv_heads, wl.head_size, wl.num_q_heads
     rb = kv.kv_int4_row_bytes(d)
-    cache_bytes = wl.num_blocks * 2 * 16 * H * rb
-    replicas = max(2, -(-2 * L2_BYTES // cache_bytes))
     caches, host, t = _decode_setup(torch, kv, wl, dev, replicas)
-    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, args.segment_len)
-    nseg = -(-wl.max_seq_len // seg)
-    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(Hq, H, d, len(wl.seq_lens), wl.max_seq_len, seg)),
+    S = len(wl.seq_lens)
+    seg = kv.kv_int4_attention_segment_len(S, wl.max_seq_len, args.segment_len)
+    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(Hq, H, d, S, wl.max_seq_len, seg)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((wl.query.shape[0], Hq, d), dtype=wl.query.dtype, device=dev)
     kv_bytes = int(wl.seq_lens.sum()) * 2 * H * rb
     qo_bytes = 2 * wl.query.numel() * wl.query.element_size()
     attn_bytes = kv_bytes + qo_bytes
-    launches_per_step = 4   # write; query rotation; split-KV walker; combine
 
     def write(i):
         kv.kv_int4_write(t["k"], t["v"], t["slots"], t["signs"], caches[i % replicas])
@@ -218,9 +260,8 @@ def _gpu_arm(args):
         write(i)
         attend(i)
     torch.cuda.synchronize()
-    # One CUDA graph per cache replica holding one whole step (write + attention), and one holding
-    # the attention call alone; decode steps are replayed as graphs, which takes the Python and
-    # launch overhead of the four kernel launches per step off the GPU's critical path.
+    # One CUDA graph per cache replica holding a whole step (write + attention) and one holding the
+    # attention call alone: decode steps replay as graphs, as a serving loop runs them.
     step_graphs, attn_graphs = [], []
     for r in range(replicas):
         g = torch.cuda.CUDAGraph()
@@ -235,122 +276,143 @@ def _gpu_arm(args):
     for i in range(args.warmup):
         step_graphs[i % replicas].replay()
         attn_graphs[i % replicas].replay()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # ---- device-timed steps (the headline)
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.06)
+    sampler = ClockSampler(local) if sample_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.06)
     barrier()
-    e0.record(stream)
-    for i in range(args.steps):
-        step_graphs[i % replicas].replay()
-    e1.record(stream)
+    ms_step = _timed(torch, stream, lambda i: step_graphs[i % replicas].replay(), args.steps) / args.steps
     barrier()
-    clocks = sampler.stop()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-    value = whole_job_gbs(attn_bytes, world, ms_step)
-    # ---- the attention call alone, back to back (roofline of the dominant kernel call)
-    barrier()
-    e0.record(stream)
-    for i in range(args.steps):
-        attn_graphs[i % replicas].replay()
-    e1.record(stream)
-    barrier()
-    attn_avg_ms = e0.elapsed_time(e1) / args.steps
-    # ---- the same steps issued eagerly through the Python API (no graph)
-    barrier()
-    e0.record(stream)
-    for i in range(args.steps):
+    clocks = sampler.stop() if sampler else None
+    ms_step = max_over_ranks(ms_step, dev)
+    attn_ms = _timed(torch, stream, lambda i: attn_graphs[i % replicas].replay(), args.steps) / args.steps
+
+    def eager(i):
         write(i)
         attend(i)
-    e1.record(stream)
-    barrier()
-    eager_ms = e0.elapsed_time(e1) / args.steps
+    eager_ms = _timed(torch, stream, eager, args.steps) / args.steps
+    res = {"ms_step": ms_step, "attn_ms": attn_ms, "eager_ms": eager_ms, "clocks": clocks, "seg": seg,
+           "nseg": -(-wl.max_seq_len // seg), "kv_bytes": kv_bytes, "qo_bytes": qo_bytes, "attn_bytes": attn_bytes,
+           "cache_bytes": wl.num_blocks * 2 * 16 * H * rb, "replicas": replicas}
+    if with_e2e:
+        h2d = host.numel()
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d2h = host_out.numel() * host_out.element_size()
 
-    # ---- end to end through the public API from pinned host buffers: every step uploads its
-    # packed inputs, runs the write and the attention and reads the output back.  Timed eagerly
-    # (Python issuing each step) and, as a serving loop would run decode steps, as one CUDA graph
-    # per cache replica holding the whole step including both copies.
-    h2d = host.numel()
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d2h = host_out.numel() * host_out.element_size()
+        def e2e_step(i):
+            t["_buf"].copy_(host, non_blocking=True)
+            write(i)
+            attend(i)
+            host_out.copy_(out, non_blocking=True)
 
-    def e2e_step(i):
-        t["_buf"].copy_(host, non_blocking=True)
-        write(i)
-        attend(i)
-        host_out.copy_(out, non_blocking=True)
+        e2e_eager_ms = _timed(torch, stream, e2e_step, args.steps) / args.steps
+        e2e_graphs = []
+        for r in range(replicas):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                e2e_step(r)
+            e2e_graphs.append(g)
+        for i in range(args.warmup):
+            e2e_graphs[i % replicas].replay()
+        barrier()
+        e2e_ms = _timed(torch, stream, lambda i: e2e_graphs[i % replicas].replay(), args.steps) / args.steps
+        barrier()
+        res.update(e2e_ms=max_over_ranks(e2e_ms, dev), e2e_eager_ms=e2e_eager_ms, h2d=h2d, d2h=d2h)
+    del caches, ws, t
+    torch.cuda.empty_cache()
+    return res
 
-    barrier()
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(stream)
-    barrier()
-    e2e_eager_ms = e0.elapsed_time(e1) / args.steps
-    e2e_graphs = []
-    for r in range(replicas):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            e2e_step(r)
-        e2e_graphs.append(g)
-    for i in range(args.warmup):
-        e2e_graphs[i % replicas].replay()
-    barrier()
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_graphs[i % replicas].replay()
-    e1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-    e2e_value = attn_bytes * world / (e2e_ms * 1e-3) / 1e9
 
-    # ---- write-throughput workload
-    wres = _write_bench(torch, kv, workloads, dev, stream, args)
+def _gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
 
-    peak, peak_kind = _peaks()
-    roof_achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
-    traffic = _traffic("decode_gqa_batch")
+
+def _roof(achieved, peak, kind, traffic, **extra):
+    d = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+         "traffic": traffic, "peak_source": kind + " (MEASURED_PEAKS.json hbm_gbs)" if kind == "measured" else kind}
+    d.update(extra)
+    return d
+
+
+def _gpu_arm(args):
+    import torch
+
+    import int4_token_head_kv_gb300 as kv
+    import workloads
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    hbm, bf16, kind = _peaks()
+
+    # ---- headline: long-context decode steps
+    wl = workloads.long_context_decode(seed=args.seed)
+    r = _decode_steps(torch, kv, wl, dev, args, replicas=1, world=world, with_e2e=True, sample_clocks=True,
+                      local=local)
+    attn_bytes = r["attn_bytes"]
+    value = whole_job_gbs(attn_bytes, world, r["ms_step"])
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int4-kv/f16-mma/f32", "data": "synthetic",
-        "config": {"workload": "gqa_decode_batch: 32 seqs, seq_len U[512,4096] (sum %d), 32 q / 8 kv heads, "
-                               "head 128, block 16, bf16 N(0,1) with 4 K channels x10 per kv head, "
-                               "permuted blocks; step = write 32 new tokens + decode attention"
-                               % int(wl.seq_lens.sum()),
-                   "segment_len": seg, "segments_max": nseg, "packed_kv_bytes_per_step": kv_bytes,
-                   "qo_bytes_per_step": qo_bytes,
-                   "l2": f"{replicas} cache replicas rotated per step ({replicas * cache_bytes / 2**20:.0f} MiB "
-                         f"> 2 x 129 MB L2)",
+        "config": {"workload": "long_context_decode: 8 seqs x 131072 tokens, 64 q / 8 kv heads, head 128, block 16, "
+                               "bf16 Student-t(3) K/V, N(0,1) Q, permuted blocks; step = write 8 new tokens + "
+                               "decode attention",
+                   "segment_len": r["seg"], "segments_per_seq": r["nseg"], "packed_kv_bytes_per_step": r["kv_bytes"],
+                   "qo_bytes_per_step": r["qo_bytes"],
+                   "l2": f"inputs larger than L2 (cache {r['cache_bytes'] / 2**20:.0f} MiB > 129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "steps replayed as one CUDA graph per step (write + attention)",
-                   "eager_ms_per_step": round(eager_ms, 5),
-                   "eager_value": round(attn_bytes * world / (eager_ms * 1e-3) / 1e9, 2)},
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 5), "timing": "one CUDA graph per step: packed input upload, write, "
-                "attention, output read-back", "eager_ms_per_step": round(e2e_eager_ms, 5),
-                "eager_value": round(attn_bytes * world / (e2e_eager_ms * 1e-3) / 1e9, 2)},
-        "roofline": {"bound": "hbm", "achieved": round(roof_achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(roof_achieved / peak, 4), "traffic": traffic,
-                     "kernel": "attention call (query rotation + decode kernel + segment combine), graph-replayed back to back",
-                     "peak_source": peak_kind,
-                     "bytes_per_launch": attn_bytes, "avg_ms": round(attn_avg_ms, 5)},
-        "write": wres,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+                   "eager_ms_per_step": round(r["eager_ms"], 5),
+                   "eager_value": round(_gbs(attn_bytes * world, r["eager_ms"]), 2)},
+        "e2e": {"value": round(_gbs(attn_bytes * world, r["e2e_ms"]), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 5),
+                "timing": "one CUDA graph per step: packed input upload, write, attention, output read-back",
+                "eager_ms_per_step": round(r["e2e_eager_ms"], 5),
+                "eager_value": round(_gbs(attn_bytes * world, r["e2e_eager_ms"]), 2)},
+        "roofline": _roof(_gbs(attn_bytes, r["attn_ms"]), hbm, kind, _traffic("long_context_decode"),
+                          kernel="attention call (query rotation + split-KV walker + combine), graph-replayed "
+                                 "back to back", bytes_per_launch=attn_bytes, avg_ms=round(r["attn_ms"], 5)),
+        "gpu_launches": 4 * args.steps,
+        "clocks": r["clocks"],
     }
-    if args.extra:
-        result["extra"] = _extra(torch, kv, workloads, dev, args)
+    del wl
+
+    # ---- sub-objects (rank-local figures)
+    if not args.headline_only:
+        result["gqa_decode_batch"] = _gqa_bench(torch, kv, workloads, dev, args, world, hbm, kind)
+        result["write"] = _write_bench(torch, kv, workloads, dev, args, hbm, kind)
+        result["mixed_prefill_decode"] = _mixed_bench(torch, kv, workloads, dev, args, hbm, bf16, kind)
+        result["int8_comparator"] = _int8_write_bench(torch, kv, workloads, dev, args, hbm)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = _cpu_baseline("decode", args)
+        result["cpu_baseline"] = _cpu_baseline(args)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(result))
 
 
-def _write_bench(torch, kv, workloads, dev, stream, args):
+def _gqa_bench(torch, kv, workloads, dev, args, world, hbm, kind):
+    wl = workloads.gqa_decode_batch(seed=args.seed)
+    rb = kv.kv_int4_row_bytes(wl.head_size)
+    cache_bytes = wl.num_blocks * 2 * 16 * wl.num_kv_heads * rb
+    replicas = max(2, -(-2 * L2_BYTES // cache_bytes))
+    r = _decode_steps(torch, kv, wl, dev, args, replicas=replicas, world=world)
+    return {"workload": "gqa_decode_batch: 32 seqs, seq_len U[512,4096] (sum %d), 32 q / 8 kv heads, head 128, "
+                        "block 16, bf16 N(0,1) with 4 K channels x10 per kv head, permuted blocks; step = write 32 "
+                        "new tokens + decode attention" % int(wl.seq_lens.sum()),
+            "GB/s": round(_gbs(r["attn_bytes"], r["ms_step"]), 2), "ms_per_step": round(r["ms_step"], 5),
+            "segment_len": r["seg"], "bytes_per_step": r["attn_bytes"],
+            "l2": f"{replicas} cache replicas rotated per step ({replicas * cache_bytes / 2**20:.0f} MiB > 2 x 129 MB)",
+            "roofline": _roof(_gbs(r["attn_bytes"], r["attn_ms"]), hbm, kind, _traffic("gqa_decode_batch"),
+                              kernel="attention call, graph-replayed back to back over the replicas",
+                              bytes_per_launch=r["attn_bytes"], avg_ms=round(r["attn_ms"], 5))}
+
+
+def _write_bench(torch, kv, workloads, dev, args, hbm, kind):
     wl = workloads.write_throughput(seed=args.seed)
     H, d = wl.num_kv_heads, wl.head_size
     signs = torch.from_numpy(wl.signs).to(dev)
@@ -359,29 +421,99 @@ def _write_bench(torch, kv, workloads, dev, stream, args):
     cache = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
     per_tok = 2 * H * d * k.element_size() + 2 * H * kv.kv_int4_row_bytes(d) + 8
     nbytes = wl.num_tokens * per_tok
-    reps = max(3, args.steps // 4)
+    reps = max(50, min(2000, args.steps))
     for _ in range(max(3, args.warmup)):
         kv.kv_int4_write(k, v, slots, signs, cache)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        kv.kv_int4_write(k, v, slots, signs, cache)   # inputs (268 MB) exceed L2
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    peak, kind = _peaks()
-    gbs = nbytes / (ms * 1e-3) / 1e9
+    ms = _timed(torch, torch.cuda.current_stream(), lambda i: kv.kv_int4_write(k, v, slots, signs, cache), reps) / reps
+    gbs = _gbs(nbytes, ms)
     return {"workload": "write_throughput: 65536 tokens, 8 kv heads, head 128, bf16, magnitudes 10^U(-2,2), "
-                        "random slots over 8192 blocks of 16",
+                        "random slots over 8192 blocks of 16 (inputs 268 MB > L2)",
             "tokens_per_s": round(wl.num_tokens / (ms * 1e-3), 1), "GB/s": round(gbs, 1), "ms_per_call": round(ms, 5),
             "bytes_per_call": nbytes, "launches": reps,
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": _traffic("write_throughput"),
-                         "peak_source": kind}}
+            "roofline": _roof(gbs, hbm, kind, _traffic("write_throughput"), kernel="write_kernel",
+                              bytes_per_launch=nbytes, avg_ms=round(ms, 5))}
 
 
-def _int8_write_bench(torch, kv, workloads, dev, args):
+def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=None):
+    """Write every token of ``wl`` (untimed), then time ``reps`` back-to-back attention calls captured in
+    one CUDA graph, over the whole batch or over the sequences ``sub`` (same cache).  Returns ms per call
+    and the segment length."""
+    H, d = wl.num_kv_heads, wl.head_size
+    signs = torch.from_numpy(wl.signs).to(dev)
+    cache = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+    import numpy as np
+    _write_history(torch, kv, wl, dev, signs, cache, np.arange(wl.key.shape[0]))
+    results = {}
+    for name, seqs in (sub or {"all": None}).items():
+        if seqs is None:
+            seqs = list(range(len(wl.seq_lens)))
+        qrows = np.concatenate([np.arange(wl.query_start_loc[b], wl.query_start_loc[b + 1]) for b in seqs])
+        q = wl.query[qrows].to(dev)
+        lens_np = wl.seq_lens[seqs]
+        qlens = wl.query_lens[seqs]
+        qsl = torch.from_numpy(np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)).to(dev)
+        tables, lens = torch.from_numpy(wl.block_tables[seqs].copy()).to(dev), torch.from_numpy(lens_np).to(dev)
+        max_len, max_q = int(lens_np.max()), int(qlens.max())
+        seg = kv.kv_int4_attention_segment_len(len(seqs), max_len, segment_len)
+        ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(wl.num_q_heads, H, d, len(seqs), max_len, seg)),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+
+        def call():
+            kv.kv_int4_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, signs, max_query_len=max_q,
+                                       max_seq_len=max_len, out=out, segment_len=seg, workspace=ws)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                call()
+        g.replay()
+        ms = _timed(torch, torch.cuda.current_stream(), lambda i: g.replay(), 1) / reps
+        kvb = int(lens_np.sum()) * 2 * H * kv.kv_int4_row_bytes(d) + 2 * q.numel() * q.element_size()
+        results[name] = {"ms": ms, "seg": seg, "bytes": kvb, "seqs": seqs, "qlens": qlens, "lens": lens_np}
+        del g, ws, out, q
+    del cache
+    torch.cuda.empty_cache()
+    return results
+
+
+def _prefill_flops(res, num_q_heads, d):
+    """Dense-equivalent attention FLOPs of the prefill chunks: 4 d per visible (query, key) pair per q head."""
+    pairs = sum(int(q) * (int(L) - int(q)) + int(q) * (int(q) + 1) // 2
+                for L, q in zip(res["lens"], res["qlens"]) if q > 1)
+    return 4 * d * pairs * num_q_heads
+
+
+def _mixed_bench(torch, kv, workloads, dev, args, hbm, bf16, kind):
+    wl = workloads.mixed_prefill_decode(seed=args.seed)
+    nseq = len(wl.seq_lens)
+    pre = [b for b in range(nseq) if wl.query_lens[b] > 1]
+    dec = [b for b in range(nseq) if wl.query_lens[b] == 1]
+    reps = 10
+    res = _attention_calls(torch, kv, wl, dev, reps, sub={"all": None, "prefill": pre, "decode": dec})
+    a, p, dd = res["all"], res["prefill"], res["decode"]
+    flops = _prefill_flops(p, wl.num_q_heads, wl.head_size)
+    tfs = flops / (p["ms"] * 1e-3) / 1e12
+    return {"workload": "mixed_prefill_decode: 4 prefill seqs (2048 cached + 2048-query causal chunk) + 60 decode "
+                        "seqs U[1,32768], 32 q / 8 kv heads, head 128, bf16 N(0,1); one attention call over the batch",
+            "ms_per_call": round(a["ms"], 4), "GB/s": round(_gbs(a["bytes"], a["ms"]), 1), "bytes_per_call": a["bytes"],
+            "segment_len": a["seg"],
+            "roofline": _roof(_gbs(a["bytes"], a["ms"]), hbm, kind, _traffic("mixed_prefill_decode"),
+                              kernel="whole attention call (decode kernels + prefill kernel), graph-replayed",
+                              bytes_per_launch=a["bytes"], avg_ms=round(a["ms"], 4)),
+            "prefill_part": {"ms": round(p["ms"], 4), "dense_equiv_TFLOP": round(flops / 1e12, 4),
+                             "roofline": {"bound": "tensor", "achieved": round(tfs, 1), "peak": bf16,
+                                          "unit": "TFLOP/s", "frac": round(tfs / bf16, 4), "traffic": None,
+                                          "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst; fp16 and bf16 "
+                                                         "dense rates are equal)" if kind == "measured" else kind,
+                                          "kernel": "prefill_kernel on the 4 prefill sequences alone"}},
+            "decode_part": {"ms": round(dd["ms"], 4), "GB/s": round(_gbs(dd["bytes"], dd["ms"]), 1),
+                            "frac": round(_gbs(dd["bytes"], dd["ms"]) / hbm, 4), "segment_len": dd["seg"]}}
+
+
+def _int8_write_bench(torch, kv, workloads, dev, args, hbm):
     """The INT8 per-(token, head) comparator's write on the same workload (cache rows d + 4 bytes)."""
     wl = workloads.write_throughput(seed=args.seed)
     H, d = wl.num_kv_heads, wl.head_size
@@ -389,134 +521,52 @@ def _int8_write_bench(torch, kv, workloads, dev, args):
     slots = torch.from_numpy(wl.slot_mapping).to(dev)
     cache = torch.zeros(kv.kv_int8_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
     nbytes = wl.num_tokens * (2 * H * d * k.element_size() + 2 * H * kv.kv_int8_row_bytes(d) + 8)
-    reps = 200
+    reps = max(50, min(2000, args.steps))
     for _ in range(5):
         kv.kv_int8_write(k, v, slots, cache)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        kv.kv_int8_write(k, v, slots, cache)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    peak, _ = _peaks()
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"tokens_per_s": round(wl.num_tokens / (ms * 1e-3), 1), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-            "ms_per_call": round(ms, 5), "bytes_per_call": nbytes,
+    ms = _timed(torch, torch.cuda.current_stream(), lambda i: kv.kv_int8_write(k, v, slots, cache), reps) / reps
+    gbs = _gbs(nbytes, ms)
+    return {"write": {"tokens_per_s": round(wl.num_tokens / (ms * 1e-3), 1), "GB/s": round(gbs, 1),
+                      "frac": round(gbs / hbm, 4), "ms_per_call": round(ms, 5), "bytes_per_call": nbytes},
             "cache_bytes_per_token": 2 * H * kv.kv_int8_row_bytes(d),
             "int4_cache_bytes_per_token": 2 * H * kv.kv_int4_row_bytes(d)}
 
 
 # ------------------------------------------------------------------------------- CPU oracle
 
-def _attention_only(torch, kv, wl, dev, reps, rows=None, segment_len=0):
-    """Write every token of ``wl`` (untimed), then time ``reps`` back-to-back attention calls
-    (captured in one CUDA graph) over the whole batch.  Returns ms per call."""
-    H, d = wl.num_kv_heads, wl.head_size
-    signs = torch.from_numpy(wl.signs).to(dev)
-    cache = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
-    step = 1 << 18
-    for r0 in range(0, wl.key.shape[0], step):
-        r1 = min(wl.key.shape[0], r0 + step)
-        kv.kv_int4_write(wl.key[r0:r1].to(dev), wl.value[r0:r1].to(dev),
-                         torch.from_numpy(wl.slot_mapping[r0:r1]).to(dev), signs, cache)
-    q = wl.query.to(dev)
-    tables, lens = torch.from_numpy(wl.block_tables).to(dev), torch.from_numpy(wl.seq_lens).to(dev)
-    qsl = torch.from_numpy(wl.query_start_loc).to(dev)
-    seg = kv.kv_int4_attention_segment_len(len(wl.seq_lens), wl.max_seq_len, segment_len)
-    ws = torch.empty(max(1, kv.kv_int4_attention_workspace_bytes(wl.num_q_heads, H, d, len(wl.seq_lens),
-                                                                 wl.max_seq_len, seg)), dtype=torch.uint8, device=dev)
-    out = torch.empty_like(q)
-
-    def call():
-        kv.kv_int4_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, signs,
-                                   max_query_len=wl.max_query_len, max_seq_len=wl.max_seq_len, out=out,
-                                   segment_len=seg, workspace=ws)
-    for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for _ in range(reps):
-            call()
-    g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    del cache
-    return e0.elapsed_time(e1) / reps, seg
-
-
-def _extra(torch, kv, workloads, dev, args):
-    """The long-context and mixed workloads, attention call only (their caches exceed L2)."""
-    peak, _ = _peaks()
-    res = {}
-    wl = workloads.long_context_decode(seed=args.seed)
-    ms, seg = _attention_only(torch, kv, wl, dev, reps=20)
-    rb = kv.kv_int4_row_bytes(wl.head_size)
-    kvb = int(wl.seq_lens.sum()) * 2 * wl.num_kv_heads * rb + 2 * wl.query.numel() * 2
-    res["long_context_decode"] = {"ms": round(ms, 4), "GB/s": round(kvb / ms / 1e6, 1),
-                                  "frac": round(kvb / ms / 1e6 / peak, 4), "bytes": kvb, "segment_len": seg}
-    del wl
-    wl = workloads.mixed_prefill_decode(seed=args.seed)
-    ms, seg = _attention_only(torch, kv, wl, dev, reps=10)
-    kvb = int(wl.seq_lens.sum()) * 2 * wl.num_kv_heads * rb + 2 * wl.query.numel() * 2
-    # dense-equivalent attention FLOPs of the prefill chunks: 4 d per visible (query, key) pair per q head
-    pairs = sum(int(q) * (int(L) - int(q)) + int(q) * (int(q) + 1) // 2
-                for L, q in zip(wl.seq_lens, wl.query_lens) if q > 1)
-    flops = 4 * wl.head_size * pairs * wl.num_q_heads
-    res["mixed_prefill_decode"] = {"ms": round(ms, 4), "GB/s_packed_kv": round(kvb / ms / 1e6, 1),
-                                   "prefill_TFLOP": round(flops / 1e12, 4), "bytes": kvb, "segment_len": seg}
-    pre = workloads.make_attention_workload("prefill_only", wl.seq_lens[:4], wl.query_lens[:4], 32, 8, 128,
-                                            seed=args.seed)
-    ms_p, _ = _attention_only(torch, kv, pre, dev, reps=10)
-    res["mixed_prefill_decode"]["prefill_part_ms"] = round(ms_p, 4)
-    res["mixed_prefill_decode"]["prefill_part_TFLOP/s"] = round(flops / ms_p / 1e9, 1)
-    res["int8_write_comparator"] = _int8_write_bench(torch, kv, workloads, dev, args)
-    return res
-
-
-def _only(args):
-    """One workload's attention call, timed as in --extra, on its own (no decode-batch steps)."""
-    import torch
-
-    import int4_token_head_kv_gb300 as kv
-    import workloads
-
-    dev = torch.device("cuda:0")
-    torch.cuda.set_device(dev)
-    peak, _ = _peaks()
-    wl = getattr(workloads, args.only)(seed=args.seed)
-    ms, seg = _attention_only(torch, kv, wl, dev, reps=10)
-    kvb = int(wl.seq_lens.sum()) * 2 * wl.num_kv_heads * kv.kv_int4_row_bytes(wl.head_size) + 2 * wl.query.numel() * 2
-    print(json.dumps({"only": args.only, "ms": round(ms, 4), "GB/s": round(kvb / ms / 1e6, 1),
-                      "frac": round(kvb / ms / 1e6 / peak, 4), "bytes": kvb, "segment_len": seg}))
-
-
-def _cpu_baseline(kind, args, nsample=None):
+def _oracle_timing(argv):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    n = nsample if nsample is not None else (2 if kind == "decode" else 2048)
-    res = subprocess.run([sys.executable, "-m", "oracle.timing", kind, str(n), str(args.seed)], cwd=ROOT, env=env,
-                         capture_output=True, text=True, timeout=900)
+    res = subprocess.run([sys.executable, "-m", "oracle.timing"] + argv, cwd=ROOT, env=env, capture_output=True,
+                         text=True, timeout=1200)
     if res.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": res.stderr[-400:]}
-    r = json.loads(res.stdout.strip().splitlines()[-1])
-    return {"value": round(r["bytes"] / r["seconds"] / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{r['what']} of the GQA decode workload (write their tokens + attention), "
-                      f"{r['seconds']:.2f} s single-threaded" if kind == "decode" else r["what"],
-            "seconds": round(r["seconds"], 3)}
+        raise RuntimeError(res.stderr[-600:])
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def _cpu_baseline(args):
+    """The oracle on a bounded sample of the headline workload: single-threaded (a few (sequence,
+    kv head) pairs) and on all host cores (one process per core, one pair each)."""
+    ncpu = os.cpu_count() or 1
+    try:
+        r = _oracle_timing(["long_decode", str(args.cpu_pairs), str(args.seed), "--procs", str(ncpu)])
+    except Exception as e:   # report, do not fail the GPU measurement
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": str(e)[-400:]}
+    one = r["single"]
+    out = {"value": round(one["bytes"] / one["seconds"] / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": one["what"] + f"; {one['seconds']:.1f} s", "nproc": ncpu}
+    if "all_cores" in r:
+        a = r["all_cores"]
+        out["all_cores"] = {"value": round(a["bytes"] / a["seconds"] / 1e9, 6), "unit": "GB/s", "cores": a["threads"],
+                            "kind": "oracle", "sample": a["what"] + f"; {a['seconds']:.1f} s wall"}
+    return out
 
 
 def _reference_arm(args):
-    """The CPU oracle, as it stands, on the GPU arm's workload and metric.  Each step is a bounded
-    sample: one (sequence, kv head) of the GQA decode batch, round-robin, truncated to the first n
-    tokens so that warm-up + steps take about two minutes whatever --steps is.  A step writes the
-    sample's tokens into the oracle's cache and runs the oracle attention for that kv head's query
-    heads; its bytes are the packed K/V rows (+ Q/O) it covers."""
+    """The CPU oracle, as it stands, on the GPU arm's headline workload and metric.  Each step is a
+    bounded sample: one (sequence, kv head) pair of the long-context decode batch, round-robin,
+    truncated to its first n tokens so that warm-up + steps take about ``--ref-budget-s`` seconds
+    whatever --steps is.  A step writes the sample's tokens into the oracle's cache and runs the oracle
+    attention for that kv head's query heads; its bytes are the packed K/V rows (+ Q/O) it covers."""
     world, rank, _ = _dist()
     if rank != 0:
         return
@@ -525,29 +575,30 @@ def _reference_arm(args):
     import oracle
     import workloads
 
-    wl = workloads.gqa_decode_batch(seed=args.seed)
+    t_start = time.perf_counter()
+    wl = workloads.long_context_decode(seed=args.seed)
     S, H, G, d = len(wl.seq_lens), wl.num_kv_heads, wl.num_q_heads // wl.num_kv_heads, wl.head_size
     rb = d // 2 + 4
 
     def one(i, ntok):
         b, h = i % S, (i // S) % H
         L = min(int(wl.seq_lens[b]), ntok)
-        rows = np.arange(wl.token_start[b], wl.token_start[b] + L)
+        rows = slice(int(wl.token_start[b]), int(wl.token_start[b]) + L)
         nb = (L + 15) // 16
         table = np.arange(nb, dtype=np.int32)[None]
         cache = np.zeros(oracle.cache_shape(nb, 16, 1, d), np.uint8)
+        k, v = wl.key[rows, h:h + 1], wl.value[rows, h:h + 1]
         q = wl.query[b:b + 1, h * G:(h + 1) * G]
         t0 = time.perf_counter()
-        oracle.write(wl.key[rows, h:h + 1], wl.value[rows, h:h + 1], np.arange(L, dtype=np.int64), wl.signs, cache)
+        oracle.write(k, v, np.arange(L, dtype=np.int64), wl.signs, cache)
         oracle.paged_attention(q, cache, table, np.array([L], np.int32), np.array([0, 1], np.int32),
                                wl.softmax_scale, wl.signs)
         return time.perf_counter() - t0, L * 2 * rb + 2 * G * d * 2
 
-    t_start = time.perf_counter()
     dt, _ = one(0, 4096)
-    per_tok = dt / min(int(wl.seq_lens[0]), 4096)
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    ntok = int(max(16, min(4096, budget / max(per_tok, 1e-9))))
+    per_tok = dt / 4096
+    budget = args.ref_budget_s / max(1, args.steps + args.warmup)
+    ntok = int(max(16, min(int(wl.seq_lens[0]), budget / max(per_tok, 1e-9))))
     for i in range(args.warmup):
         one(i, ntok)
     secs, nbytes = 0.0, 0
@@ -556,13 +607,13 @@ def _reference_arm(args):
         secs += s_
         nbytes += b_
     value = nbytes / secs / 1e9
-    sample = f"1 (sequence, kv head) of the GQA decode batch per step, first {ntok} tokens, round-robin"
+    sample = f"1 (sequence, kv head) pair of the long-context decode batch per step, first {ntok} tokens, round-robin"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 write / f64 attention",
             "data": "synthetic",
-            "config": {"workload": "gqa_decode_batch (the GPU arm's workload); oracle on a bounded sample per step",
-                       "sample_tokens": ntok},
+            "config": {"workload": "long_context_decode (the GPU arm's headline workload); oracle on a bounded "
+                                   "sample per step", "sample_tokens": ntok},
             "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -570,24 +621,57 @@ def _reference_arm(args):
     print(json.dumps(line))
 
 
-def main():
+def _only(args):
+    """One workload's attention call (or the write), timed as in the sub-objects, on its own: a small
+    program for profiling one kernel."""
+    import torch
+
+    import int4_token_head_kv_gb300 as kv
+    import workloads
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    hbm, _, _ = _peaks()
+    if args.only == "write_throughput":
+        r = _write_bench(torch, kv, workloads, dev, args, hbm, "measured")
+        print(json.dumps({"only": args.only, "ms": r["ms_per_call"], "GB/s": r["GB/s"]}))
+        return
+    wl = getattr(workloads, args.only)(seed=args.seed)
+    res = _attention_calls(torch, kv, wl, dev, reps=args.steps, segment_len=args.segment_len)["all"]
+    print(json.dumps({"only": args.only, "ms": round(res["ms"], 4), "GB/s": round(_gbs(res["bytes"], res["ms"]), 1),
+                      "frac": round(_gbs(res["bytes"], res["ms"]) / hbm, 4), "bytes": res["bytes"],
+                      "segment_len": res["seg"]}))
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--segment-len", type=int, default=0,
                     help="split-KV segment length in tokens (multiple of 16); 0 = the library's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--extra", action="store_true",
-                    help="also time the long-context and mixed prefill+decode workloads (attention call only)")
-    ap.add_argument("--only", choices=["long_context_decode", "mixed_prefill_decode"],
-                    help="time just this workload's attention call and print its own JSON line (for profiling)")
-    args = ap.parse_args()
+    ap.add_argument("--headline-only", action="store_true", help="skip the sub-object workloads")
+    ap.add_argument("--cpu-pairs", type=int, default=8,
+                    help="(sequence, kv head) pairs in the single-threaded oracle sample")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="reference arm: seconds of oracle work over warm-up + steps")
+    ap.add_argument("--only", choices=["long_context_decode", "mixed_prefill_decode", "gqa_decode_batch",
+                                       "write_throughput"],
+                    help="time just this workload's attention call (or the write) and print its own line")
+    args = ap.parse_args(argv)
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        return launch_local_ranks(args.gpus, argv)
+    if world is not None and int(world) != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        return 2
     if args.only:
         _only(args)
-        return
+        return 0
     if args.impl == "reference":
         # the oracle runs single-threaded; fix BLAS threads before numpy loads
         for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -598,7 +682,8 @@ def main():
         _reference_arm(args)
     else:
         _gpu_arm(args)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -206,10 +206,15 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
  * when the library is loaded, held by every GPU that loads it until the process exits).  It calls
  * no cudaMalloc, cudaFree or allocating library routine.
  *
- * Returns KV_INT4_EWORKSPACE, launching nothing, when kv_int4_attention_workspace_bytes() for
- * these sizes exceeds KV_INT4_NOALLOC_SCRATCH_BYTES (use a larger segment_len, or the regular
- * entry point).  The first call on a device looks up the scratch array's device address (a
- * runtime call that does not touch any stream); make that first call before any stream capture.
+ * Segment length: an explicit segment_len is used as given.  With segment_len 0 the call takes the
+ * library's usual choice (kv_int4_attention_segment_len) when its workspace fits the scratch array;
+ * otherwise it raises the segment length in steps of 32 tokens, up to 4096, to the first value whose
+ * kv_int4_attention_workspace_bytes() fits, and computes exactly what kv_int4_paged_attention computes
+ * with that segment_len.  Returns KV_INT4_EWORKSPACE, launching nothing, when the workspace for an
+ * explicit segment_len, or for 4096, exceeds KV_INT4_NOALLOC_SCRATCH_BYTES (use a larger
+ * segment_len, or the regular entry point).  The first call on a device looks up the scratch
+ * array's device address (a runtime call that does not touch any stream); make that first call
+ * before any stream capture.
  * Every call shares the one array and it keeps the last call's contents; nothing in it needs to
  * start at zero, because each call writes every partial it later reads.  Calls that overlap on the
  * GPU (different streams, or different host threads on one device) race on the array: serialise

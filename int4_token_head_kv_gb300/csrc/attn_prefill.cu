@@ -78,9 +78,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     if (qt0 >= qlen) return;
     int L = __ldg(p.seq_lens + seq);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (L > p.max_blocks_per_seq * kBlockSize || qlen > L) {
+    // the same context cap as the decode path (max_seq_len and the block table), counted as bad metadata
+    if (L > p.len_cap || qlen > L) {
         if (qtile == 0 && h == 0 && threadIdx.x == 0) count_status(p.status, 2);
-        L = min(L, p.max_blocks_per_seq * kBlockSize);
+        L = min(L, p.len_cap);
     }
     const int pos0 = L - qlen;   // position of query token 0
 

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace kvi4 {
 
 constexpr int kBlockSize = 16;   // tokens per cache block
@@ -91,18 +93,24 @@ inline uint32_t div_rcp(uint32_t d) { return d <= 1 ? 0xFFFFFFFFu : (uint32_t)((
 
 // Opt a kernel in to `bytes` of dynamic shared memory, once per device (so that launches issued
 // under stream capture contain nothing but the launch itself).
+// Host threads may launch concurrently: the per-device record is atomic (two threads that both see
+// it short set the same attributes, which is harmless).
 template <auto Kern>
 cudaError_t opt_in_smem(size_t bytes) {
-    static size_t done[64] = {};
+    static std::atomic<size_t> done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (done[dev] >= bytes) return cudaSuccess;
+    if (done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     // prefer the largest shared-memory carve-out, so that several CTAs fit on an SM
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(Kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess) done[dev] = bytes;
+    if (e == cudaSuccess) {
+        size_t prev = done[dev].load(std::memory_order_relaxed);
+        while (prev < bytes && !done[dev].compare_exchange_weak(prev, bytes, std::memory_order_release)) {
+        }
+    }
     return e;
 }
 

@@ -85,9 +85,11 @@ def test_long_context_decode_scaled():
     _run_case(wl)
 
 
-def test_long_context_decode_full_size_sampled():
+@pytest.mark.parametrize("segment_len", [4096, 0])
+def test_long_context_decode_full_size_sampled(segment_len):
+    # the workload's own segments of 4096, and the library's choice (what the benchmark times)
     wl = workloads.long_context_decode()
-    _run_case(wl, seqs=[0, 7], kv_heads=[0, 5])
+    _run_case(wl, segment_len=segment_len, seqs=[0, 7], kv_heads=[0, 5])
 
 
 def test_mixed_prefill_decode_scaled():
@@ -97,8 +99,13 @@ def test_mixed_prefill_decode_scaled():
 
 
 def test_mixed_prefill_decode_full_size_sampled():
+    # at the library's segment length (what the benchmark times): every prefill sequence, the
+    # longest and shortest decode contexts and a few others
     wl = workloads.mixed_prefill_decode()
-    _run_case(wl, seqs=[0, 3, 4, 30, 63], kv_heads=[0, 7])
+    assert wl.segment_len == 0
+    dec = np.arange(4, len(wl.seq_lens))
+    pick = [int(dec[np.argmax(wl.seq_lens[dec])]), int(dec[np.argmin(wl.seq_lens[dec])]), 4, 30, 63]
+    _run_case(wl, seqs=sorted(set([0, 1, 2, 3] + pick)), kv_heads=[0, 3, 7])
 
 
 @pytest.mark.parametrize("H,G,d", [(1, 1, 64), (2, 4, 128), (4, 2, 64), (8, 8, 128), (1, 8, 128), (8, 1, 64),
@@ -125,14 +132,15 @@ def test_segment_longer_than_the_staged_block_table():
 
 def test_units_longer_than_a_cta_share():
     # 6 x 5000 tokens in segments of 2048: 18 units of up to 128 blocks over 18 CTAs whose shares
-    # are about 104 blocks, so most units straddle a boundary (some two) and are taken at run time
+    # are about 104 blocks, so most units straddle a share boundary (some two); each unit belongs to
+    # the share its first block falls in
     wl = workloads.make_attention_workload("strad", [5000, 4999, 4097, 5000, 2049, 5000], [1] * 6, 32, 8, 128,
                                            seed=14)
     out, _ = _run_case(wl, segment_len=2048)
     from gpu_helpers import gpu_attention, gpu_cache, gpu_write
     cache = gpu_cache(wl.num_blocks, 16, 8, 128)
     gpu_write(wl.key, wl.value, wl.slot_mapping, wl.signs, cache)
-    for _ in range(3):   # whichever CTA takes a shared unit, its arithmetic is the same
+    for _ in range(3):   # repeated calls give the same bits
         assert torch.equal(gpu_attention(wl, cache, segment_len=2048), out)
 
 
@@ -216,3 +224,26 @@ def test_invalid_block_ids_are_counted():
     wl.block_tables = tables
     ref = oracle_attention(wl, oracle_cache(wl), seqs=[1])   # the other sequence is unaffected
     assert_attention_close(out, ref, "unaffected sequence")
+
+
+def test_contexts_longer_than_max_seq_len_are_clamped_alike():
+    # one decode and one prefill sequence both longer than the max_seq_len the caller passes: both
+    # paths cap the context at max_seq_len (counted as bad metadata), so each sees the first 150
+    # tokens with its queries at the last positions of that window
+    import int4_token_head_kv_gb300 as kv
+    from gpu_helpers import assert_attention_close, dev, gpu_cache, gpu_write, oracle_attention, oracle_cache, \
+        status
+    wl = workloads.make_attention_workload("overlong", [300, 200], [1, 40], 16, 4, 128, seed=15)
+    cache = gpu_cache(wl.num_blocks, 16, 4, 128)
+    gpu_write(wl.key, wl.value, wl.slot_mapping, wl.signs, cache)
+    cap = 150
+    out = kv.kv_int4_paged_attention(wl.query.to(dev()), cache, torch.from_numpy(wl.block_tables).to(dev()),
+                                     torch.from_numpy(wl.seq_lens).to(dev()),
+                                     torch.from_numpy(wl.query_start_loc).to(dev()), wl.softmax_scale,
+                                     torch.from_numpy(wl.signs).to(dev()), max_query_len=wl.max_query_len,
+                                     max_seq_len=cap, out_dtype=torch.float32, segment_len=64)
+    torch.cuda.synchronize()
+    assert status()["bad_sequence"] >= 2
+    ref_cache = oracle_cache(wl)
+    wl.seq_lens = np.minimum(wl.seq_lens, cap).astype(np.int32)
+    assert_attention_close(out, oracle_attention(wl, ref_cache), "clamped contexts")

@@ -49,3 +49,37 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(4.5, "cpu") == 4.5
     assert bench.whole_job_gbs(2_000_000, 1, 2.0) == pytest.approx(1.0)
+
+
+def _bench_env():
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR",
+                                                            "MASTER_PORT")}
+    env["OPENBLAS_NUM_THREADS"] = "1"
+    return env
+
+
+def test_gpus_flag_starts_local_ranks():
+    # `bench.py --gpus 2` without an outer launcher starts two local ranks itself; the reference arm
+    # runs on CPU (rank 0 times the oracle and prints the line, rank 1 exits 0)
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                          "--warmup", "3", "--ref-budget-s", "2"], cwd=root, env=_bench_env(), capture_output=True,
+                         text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_gpus_flag_must_match_an_outer_launcher():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(_bench_env(), WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, "bench.py", "--gpus", "2"], cwd=root, env=env, capture_output=True,
+                         text=True, timeout=120)
+    assert res.returncode == 2 and "WORLD_SIZE" in res.stderr

@@ -22,6 +22,31 @@ def test_hand_examples():
     assert s[0] == np.float32(1e-6) and not q.any()
 
 
+def test_pages_raw_cache_vector():
+    # "tests/quantization/test_per_token_kv_cache.py", test_int8_per_token_head_raw_cache_matches_
+    # round_reference: one bf16 vector of 8 elements, V = -K, a cache of one block of 4 slots, slot 2.
+    # bf16 (8 significant bits) holds 127 exactly and rounds the others to the nearest multiple of
+    # 2^-6 (for 2 <= |x| < 4), 2^-7 (1 <= |x| < 2), 2^-8 (0.5 <= |x| < 1) or 2^-9 (0.25 <= |x| < 0.5):
+    #   2.6 -> 166/64 = 2.59375, 2.4 -> 154/64 = 2.40625, 1.6 -> 205/128 = 1.6015625,
+    #   1.4 -> 179/128 = 1.3984375, 0.6 -> 154/256 = 0.6015625, 0.4 -> 205/512 = 0.400390625.
+    # absmax = 127, so s = 127 / 127 = 1 and r = 1: the codes are the values rounded to the nearest
+    # integer (no ties here), -127 -3 -2 -2 -1 -1 0 127, where truncation toward zero -- the bug the
+    # page's INT8 reshape-kernel fix removes -- would give -127 -2 -2 -1 -1 0 0 127.
+    import torch
+    key = torch.tensor([[[-127.0, -2.6, -2.4, -1.6, -1.4, -0.6, -0.4, 127.0]]], dtype=torch.bfloat16)
+    assert key.float().flatten().tolist() == [-127.0, -2.59375, -2.40625, -1.6015625, -1.3984375, -0.6015625,
+                                              -0.400390625, 127.0]
+    cache = np.zeros(o8.cache_shape(1, 4, 1, 8), np.uint8)
+    assert o8.write(key, -key, np.array([2]), cache) == 0
+    k_codes = cache[0, 0, 2, 0, :8].view(np.int8).tolist()
+    v_codes = cache[0, 1, 2, 0, :8].view(np.int8).tolist()
+    assert k_codes == [-127, -3, -2, -2, -1, -1, 0, 127]
+    assert v_codes == [127, 3, 2, 2, 1, 1, 0, -127]
+    for p in (0, 1):
+        assert struct.unpack("<f", bytes(cache[0, p, 2, 0, 8:12]))[0] == 1.0
+    assert not cache[0, :, [0, 1, 3]].any()   # the other slots of the block are untouched
+
+
 def test_quantizer_invariants():
     r = np.random.default_rng(1)
     x = (r.standard_normal((512, 128)) * 10.0 ** r.uniform(-3, 3, (512, 1))).astype(np.float32)

@@ -9,7 +9,9 @@ what it returns, so both sides see identical input bits.
 Recipe (all draws from numpy's PCG64 through ``np.random.SeedSequence``):
 
 * Each component (structure, K, V, Q) gets its own child stream spawned from the workload seed,
-  so that the draw of one never depends on the size of another.
+  so that the draw of one never depends on the size of another.  Large tensors are drawn in
+  chunks of about 4 M elements, chunk i from the i-th child of the component's stream, in
+  parallel threads (the bits do not depend on the thread count).
 * Gaussian draws are float32 ``standard_normal``; Student-t draws are ``Z * sqrt(nu / (2 G))``
   with ``G ~ Gamma(nu/2)`` (the textbook construction t = Z / sqrt(chi2_nu / nu)).
 * The float32 draws are rounded to fp16 / bf16 with round-to-nearest-even (torch ``.to``).
@@ -19,6 +21,8 @@ Recipe (all draws from numpy's PCG64 through ``np.random.SeedSequence``):
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -47,22 +51,38 @@ def _to_half(x: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dtype)
 
 
-def _children(seed: int, n: int) -> list[np.random.Generator]:
-    return [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(n)]
+def _children(seed: int, n: int) -> list[np.random.SeedSequence]:
+    return np.random.SeedSequence(seed).spawn(n)
 
 
-def _fill_random(shape, dtype, rng, dist, chunk_rows=65536, row_scale=None):
-    """Draw ``shape`` (rows first) into a torch CPU tensor of ``dtype`` chunk by chunk.
+def _rng(seq: np.random.SeedSequence) -> np.random.Generator:
+    return np.random.default_rng(seq)
 
+
+_CHUNK_ELEMS = 1 << 22
+
+
+def _fill_random(shape, dtype, seq, dist, row_scale=None):
+    """Draw ``shape`` (rows first) into a torch CPU tensor of ``dtype``.
+
+    The rows are cut into chunks of about 4 M elements; chunk i draws from the i-th child of ``seq``,
+    so the result does not depend on how many threads draw the chunks (they run in parallel).
     ``row_scale`` (float32 [rows]) multiplies each row: it carries the per-token magnitudes of the
     write-throughput workload.  The multiplication is part of drawing the input, not of the method.
     """
     out = torch.empty(shape, dtype=dtype)
     rows = shape[0]
-    inner = shape[1:]
-    for r0 in range(0, rows, chunk_rows):
+    inner = tuple(shape[1:])
+    per_row = int(np.prod(inner)) if inner else 1
+    chunk_rows = max(1, _CHUNK_ELEMS // max(1, per_row))
+    starts = list(range(0, rows, chunk_rows))
+    seqs = seq.spawn(len(starts))
+
+    def one(i):
+        r0 = starts[i]
         r1 = min(rows, r0 + chunk_rows)
-        sub = (r1 - r0,) + tuple(inner)
+        rng = np.random.default_rng(seqs[i])
+        sub = (r1 - r0,) + inner
         if dist == "normal":
             x = rng.standard_normal(sub, dtype=np.float32)
         elif dist == "student_t3":
@@ -75,6 +95,14 @@ def _fill_random(shape, dtype, rng, dist, chunk_rows=65536, row_scale=None):
         if row_scale is not None:
             x *= row_scale[r0:r1].reshape((-1,) + (1,) * len(inner))
         out[r0:r1] = _to_half(x, dtype)
+
+    workers = min(len(starts), os.cpu_count() or 1, 16)
+    if workers <= 1:
+        for i in range(len(starts)):
+            one(i)
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, range(len(starts))))
     return out
 
 
@@ -179,7 +207,8 @@ def make_attention_workload(name, seq_lens, query_lens, num_q_heads, num_kv_head
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     query_lens = np.asarray(query_lens, dtype=np.int32)
     assert np.all(query_lens <= seq_lens)
-    r_struct, r_k, r_v, r_q = _children(seed, 4)
+    s_struct, r_k, r_v, r_q = _children(seed, 4)
+    r_struct = _rng(s_struct)
     nblk = [(int(L) + block_size - 1) // block_size for L in seq_lens]
     total_blocks = sum(nblk) + extra_blocks
     maxb = max(nblk) if nblk else 1
@@ -232,7 +261,7 @@ def gqa_decode_batch(seed=0, num_seqs=32, len_range=(512, 4096)) -> AttentionWor
 
     Per kv head, 4 random K channels are 10x louder for every token; blocks are randomly permuted.
     """
-    rng = _children(seed + 1000, 1)[0]
+    rng = _rng(_children(seed + 1000, 1)[0])
     lens = rng.integers(len_range[0], len_range[1] + 1, size=num_seqs)
     return make_attention_workload("gqa_decode_batch", lens, np.ones(num_seqs, np.int32), 32, 8, 128,
                                    dtype=torch.bfloat16, k_outlier_channels=4, seed=seed)
@@ -253,7 +282,8 @@ def write_throughput(seed=0, num_tokens=65536, num_kv_heads=8, head_size=128,
     """65536 new tokens, 8 kv heads, d 128, bf16: K, V = N(0,1) x m_t with m_t = 10^U(-2, 2) drawn
     per token (independently for K and V); slots are the first 65536 entries of a random
     permutation of the 8192 x 16 cache slots."""
-    r_struct, r_k, r_v, r_mk, r_mv = _children(seed, 5)
+    s_struct, r_k, r_v, s_mk, s_mv = _children(seed, 5)
+    r_struct, r_mk, r_mv = _rng(s_struct), _rng(s_mk), _rng(s_mv)
     slots = r_struct.permutation(num_blocks * block_size)[:num_tokens].astype(np.int64)
     mk = np.power(np.float32(10.0), r_mk.uniform(-2.0, 2.0, num_tokens).astype(np.float32))
     mv = np.power(np.float32(10.0), r_mv.uniform(-2.0, 2.0, num_tokens).astype(np.float32))
@@ -269,7 +299,7 @@ def mixed_prefill_decode(seed=0, num_prefill=4, prefill_cached=2048, prefill_chu
     """4 prefill sequences (2048 cached tokens + a 2048-token causal chunk, so seq_len 4096) and
     60 decode sequences with lengths uniform in [1, 32768]; 32 q / 8 kv heads, d 128, bf16 N(0,1).
     Prefill sequences come first in the batch."""
-    rng = _children(seed + 2000, 1)[0]
+    rng = _rng(_children(seed + 2000, 1)[0])
     dec = rng.integers(1, decode_len_max + 1, size=num_decode)
     lens = [prefill_cached + prefill_chunk] * num_prefill + dec.tolist()
     qlens = [prefill_chunk] * num_prefill + [1] * num_decode
@@ -281,7 +311,8 @@ def random_write(num_tokens, num_kv_heads, head_size, dtype=torch.bfloat16, seed
                  num_blocks=None, block_size=BLOCK_SIZE, scale=1.0, negative_every=0):
     """Small write cases in the shape of the pages' cache-write tests: N(0,1) x ``scale`` K/V and
     slots sampled without replacement; optionally every ``negative_every``-th slot is -1."""
-    r_struct, r_k, r_v = _children(seed, 3)
+    s_struct, r_k, r_v = _children(seed, 3)
+    r_struct = _rng(s_struct)
     if num_blocks is None:
         num_blocks = (num_tokens + block_size - 1) // block_size + 4
     slots = r_struct.permutation(num_blocks * block_size)[:num_tokens].astype(np.int64)
