@@ -150,6 +150,14 @@ __device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint
     lo = pack_f16x2(a - hf.x, b - hf.y);
 }
 
+// fp32 -> (hi, lo) fp16 halves of one value in one register (hi in the low 16 bits), hi + lo ~ x
+// to about 22 bits.
+__device__ __forceinline__ uint32_t hi_lo_f16x2(float x) {
+    const __half hi = __float2half_rn(x);
+    const __half lo = __float2half_rn(x - __half2float(hi));
+    return (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+}
+
 // Un-rotate an accumulated output vector held by a warp (lane l: x[k] = o[l + 32 k]) and store it:
 // out = c * D * H_d * (o * inv_l).
 template <int D, typename OT>

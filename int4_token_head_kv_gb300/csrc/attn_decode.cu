@@ -56,6 +56,8 @@ constexpr uint32_t kSmemPerSm = 233472;               // 228 KB of shared memory
 constexpr uint32_t kSmemPerCtaReserved = 1024;
 
 constexpr int kMaxHead = 128;
+constexpr float kLazyMax = 8.0f;     // log2 units the running maximum may fall behind a block's
+constexpr uint32_t kLazyExp = 4;     // binades the V exponent reference may fall behind a V scale
 // unpack_word operands that turn codes into exact fp16 integers: lo nibbles 1024 + e - 1024,
 // hi nibbles (1024 + 16 e) / 16 - 64
 constexpr uint32_t kCodeLo = 0x64006400u;   // (1024, 1024)
@@ -212,16 +214,16 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
         // Score-mma B fragments.  Lane (g, t) of kv head h's warp feeds, for code word W = t + 4 j
         // of a key row (dims 8W .. 8W+7), the pairs (8W+2hh, 8W+2hh+4) and (8W+2hh+1, 8W+2hh+5)
         // of its column's vector, hh = 0, 1.  Columns: G == 8, head g (high halves; the low
-        // halves follow as a second tile); otherwise head g & 3, high halves for g < 4 and low
-        // halves for g >= 4.
+        // halves follow as a second tile); otherwise head g >> 1, the high half for even g and the
+        // low half for odd g.
         uint32_t* rec = p.ws_q + (size_t)seq * p.qrec_words;
         for (int idx = threadIdx.x; idx < H * KWPT * 32; idx += blockDim.x) {
             const int ln = idx & 31, j = (idx >> 5) % KWPT, h = idx / (32 * KWPT);
             const int g = ln >> 2, t = ln & 3;
-            const int head = WIDE ? g : (g & 3);
+            const int head = WIDE ? g : (g >> 1);
             const bool live = head < G;
             const int vrow = (h * G + (live ? head : 0)) * D;
-            const __half* qv = (WIDE || g < 4 ? qh : ql) + vrow;
+            const __half* qv = (WIDE || (g & 1) == 0 ? qh : ql) + vrow;
             const __half* qv2 = ql + vrow;
             const int W = t + 4 * j;
             uint32_t w[QW];
@@ -514,15 +516,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     const int sub = warp >> (3 - p.wph_shift);
     const int tk0 = block_token(g), tk1 = block_token(g + 8);
     // Score columns (the mma N dimension, 8 wide).  WIDE (8 query heads per kv head): column n is
-    // head n, with a second 8-wide tile carrying the low halves.  Otherwise columns 0-3 carry the
-    // high halves of heads 0-3 and columns 4-7 their low halves, so the split costs no extra mma:
-    // lane quad t then holds heads hb, hb+1 with hb = 2 (t & 1).
-    const int hb = WIDE ? 2 * t : 2 * (t & 1);
-    const bool lo_lane = !WIDE && t >= 2;   // this lane's P columns carry low halves
+    // head n, with a second 8-wide tile carrying the low halves; lane quad t holds heads 2t, 2t+1.
+    // Otherwise column 2n carries the high half of head n and column 2n + 1 its low half, so the
+    // split costs no extra mma, and lane quad t holds head t with both halves (their sum is local;
+    // m1, l1, al1, qs1 and WZ1 are then unused).  The weights of P.V take the same columns.
+    const int hb = WIDE ? 2 * t : t;
     uint32_t qb[Gm::KSTEPS][WIDE ? 4 : 2];
-    float al0 = 0.0f, al1 = 0.0f;     // logit factor of columns hb, hb + 1
-    float qs0 = 0.0f, qs1 = 0.0f;     // sum(Q') of those columns (high + low halves as stored)
-    float WZ0 = 0.0f, WZ1 = 0.0f;     // sum(w zp) per column
+    float al0 = 0.0f, al1 = 0.0f;     // logit factor of heads hb, hb + 1
+    float qs0 = 0.0f, qs1 = 0.0f;     // sum(Q') of those heads (high + low halves as stored)
+    float WZ0 = 0.0f, WZ1 = 0.0f;     // sum(w zp) per head
     int run = -1, prev_seq = -1;
     bool stop = false;
 
@@ -560,9 +562,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             const float* alpha = reinterpret_cast<const float*>(rec) + (size_t)H * D * QW;
             const float* qsum = alpha + ((p.Hq + 3) & ~3);
             al0 = (hb < G) ? alpha[h * G + hb] : 0.0f;
-            al1 = (hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
+            al1 = (WIDE && hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
             qs0 = (hb < G) ? qsum[h * G + hb] : 0.0f;
-            qs1 = (hb + 1 < G) ? qsum[h * G + hb + 1] : 0.0f;
+            qs1 = (WIDE && hb + 1 < G) ? qsum[h * G + hb + 1] : 0.0f;
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();   // this warp's reads of the buffer come before the count
@@ -647,57 +649,67 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         }
                     }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        c[e] += c2[e];
-                        if constexpr (!WIDE) c[e] += __shfl_xor_sync(0xffffffffu, c[e], 2);   // high + low columns
-                    }
+                    for (int e = 0; e < 4; ++e) c[e] += c2[e];
                     const int tb = (k + b) * kBlockSize;   // token offset of this block in the unit
                     const bool v0 = ok[b] && tb + tk0 < u.w, v1 = ok[b] && tb + tk1 < u.w;
                     const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
                     // score = S - zp sum(Q'), then the key's scale and the logit factor
                     const float zk0 = (float)(ks0 & 15u), zk1 = (float)(ks1 & 15u);
-                    x[b][0] = v0 ? fmaf(-zk0, qs0, c[0]) * sk0 * al0 : -INFINITY;
-                    x[b][1] = v0 ? fmaf(-zk0, qs1, c[1]) * sk0 * al1 : -INFINITY;
-                    x[b][2] = v1 ? fmaf(-zk1, qs0, c[2]) * sk1 * al0 : -INFINITY;
-                    x[b][3] = v1 ? fmaf(-zk1, qs1, c[3]) * sk1 * al1 : -INFINITY;
+                    if constexpr (WIDE) {   // x = (token tk0: heads hb, hb+1; token tk1: heads hb, hb+1)
+                        x[b][0] = v0 ? fmaf(-zk0, qs0, c[0]) * sk0 * al0 : -INFINITY;
+                        x[b][1] = v0 ? fmaf(-zk0, qs1, c[1]) * sk0 * al1 : -INFINITY;
+                        x[b][2] = v1 ? fmaf(-zk1, qs0, c[2]) * sk1 * al0 : -INFINITY;
+                        x[b][3] = v1 ? fmaf(-zk1, qs1, c[3]) * sk1 * al1 : -INFINITY;
+                    } else {   // x[0] = token tk0, x[2] = token tk1 (head hb; high + low columns)
+                        x[b][0] = v0 ? fmaf(-zk0, qs0, c[0] + c[1]) * sk0 * al0 : -INFINITY;
+                        x[b][2] = v1 ? fmaf(-zk1, qs0, c[2] + c[3]) * sk1 * al0 : -INFINITY;
+                        x[b][1] = x[b][3] = -INFINITY;
+                    }
                     const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp[b] + (tk0 * H + h) * Gm::RB);
                     const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp[b] + (tk1 * H + h) * Gm::RB);
                     vs0[b] = v0 ? vg0[Gm::KW] : 0u;   // invisible tokens: scale word 0 (exponent 0, weight 0)
                     vs1[b] = v1 ? vg1[Gm::KW] : 0u;
                 }
-                // ---- one online-softmax update for heads hb, hb+1 over the 32 tokens
+                // ---- one online-softmax update for heads hb (, hb+1) over the 32 tokens
                 float bm0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
-                float bm1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+                float bm1 = WIDE ? fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3])) : kNegBig;
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                    if constexpr (WIDE) bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
                 }
-                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-                const float r0 = fast_exp2(m0 - mn0), r1 = fast_exp2(m1 - mn1);
+                // The reference maximum moves only when a block's maximum passes it by more than
+                // kLazyMax (log2 units): the weights then stay below 2^kLazyMax and most updates need
+                // no rescaling of O (the softmax is the same for any reference).
+                const bool up0 = bm0 > m0 + kLazyMax, up1 = bm1 > m1 + kLazyMax;
+                const float mn0 = up0 ? bm0 : m0, mn1 = up1 ? bm1 : m1;
+                const float r0 = up0 ? fast_exp2(m0 - mn0) : 1.0f, r1 = up1 ? fast_exp2(m1 - mn1) : 1.0f;
                 float pr[2][4];
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     pr[b][0] = fast_exp2(x[b][0] - mn0);
-                    pr[b][1] = fast_exp2(x[b][1] - mn1);
                     pr[b][2] = fast_exp2(x[b][2] - mn0);
-                    pr[b][3] = fast_exp2(x[b][3] - mn1);
+                    pr[b][1] = WIDE ? fast_exp2(x[b][1] - mn1) : 0.0f;
+                    pr[b][3] = WIDE ? fast_exp2(x[b][3] - mn1) : 0.0f;
                 }
                 m0 = mn0;
                 m1 = mn1;
                 l0 = l0 * r0 + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
-                l1 = l1 * r1 + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
+                if constexpr (WIDE) l1 = l1 * r1 + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
                 // ---- V scales: exponent reference so the fp16 weights stay in range
                 const uint32_t emax = max(max((vs0[0] >> 23) & 0xFFu, (vs1[0] >> 23) & 0xFFu),
                                           max((vs0[1] >> 23) & 0xFFu, (vs1[1] >> 23) & 0xFFu));
                 const uint32_t eblk = __reduce_max_sync(0xffffffffu, emax);
+                // The exponent reference moves only when a V scale passes it by more than kLazyExp
+                // binades (the fp16 weights then stay below 2^(kLazyMax + kLazyExp + 1)).
                 float escale = 1.0f;
-                if (eblk > eref) {
+                if (eblk > eref + kLazyExp || (eref == 0u && eblk > 0u)) {
                     // 2^(eref - eblk); 0 when nothing was accumulated yet or the jump underflows
                     escale = (eref == 0u || eblk - eref > 126u) ? 0.0f : __uint_as_float((127u + eref - eblk) << 23);
                     eref = eblk;
                 }
-                const float f0 = r0 * escale, f1 = r1 * escale;
+                // (one head per lane when !WIDE: its high- and low-weight columns scale alike)
+                const float f0 = r0 * escale, f1 = (WIDE ? r1 : r0) * escale;
                 if (__any_sync(0xffffffffu, f0 != 1.0f || f1 != 1.0f)) {
 #pragma unroll
                     for (int mt = 0; mt < Gm::MT; ++mt) {
@@ -716,24 +728,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     if (!ok[b]) continue;
                     const float sv0 = __uint_as_float(vs0[b] & 0xFFFFFFF0u) * wsc;
                     const float sv1 = __uint_as_float(vs1[b] & 0xFFFFFFF0u) * wsc;
-                    // weights w = p * s'_V * 2^-E as fp16 high + low halves (invisible tokens: 0)
+                    // weights w = p * s'_V * 2^-E (invisible tokens: 0)
                     const float wa0 = pr[b][0] * sv0, wa1 = pr[b][1] * sv0;   // token tk0
                     const float wb0 = pr[b][2] * sv1, wb1 = pr[b][3] * sv1;   // token tk1
                     const float zv0 = (float)(vs0[b] & 15u), zv1 = (float)(vs1[b] & 15u);
-                    WZ0 = fmaf(wa0, zv0, fmaf(wb0, zv1, WZ0));
-                    WZ1 = fmaf(wa1, zv0, fmaf(wb1, zv1, WZ1));
-                    uint32_t xlo_h, xlo_l, xhi_h, xhi_l;
-                    split_f16x2(wa0, wa1, xlo_h, xlo_l);
-                    split_f16x2(wb0, wb1, xhi_h, xhi_l);
-                    uint32_t bb0, bb1, bb0l = 0, bb1l = 0;
+                    uint32_t bb0, bb1;
                     if constexpr (WIDE) {
-                        bb0 = movmatrix_trans(xlo_h);
-                        bb1 = movmatrix_trans(xhi_h);
-                        bb0l = movmatrix_trans(xlo_l);
-                        bb1l = movmatrix_trans(xhi_l);
+                        // All eight columns are heads: plain fp16 weights (they are not exponentiated
+                        // again, so their 11 bits cost each term at most 2^-11 relative).  sum(w zp)
+                        // takes the same rounded weights: the codes' mean is far from zero, so the
+                        // rounding errors cancel only against the zero-points they were made with.
+                        const uint32_t pa = pack_f16x2(wa0, wa1), pb = pack_f16x2(wb0, wb1);
+                        const float2 ra = __half22float2(*reinterpret_cast<const __half2*>(&pa));
+                        const float2 rb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
+                        WZ0 = fmaf(ra.x, zv0, fmaf(rb.x, zv1, WZ0));
+                        WZ1 = fmaf(ra.y, zv0, fmaf(rb.y, zv1, WZ1));
+                        bb0 = movmatrix_trans(pa);
+                        bb1 = movmatrix_trans(pb);
                     } else {
-                        bb0 = movmatrix_trans(lo_lane ? xlo_l : xlo_h);
-                        bb1 = movmatrix_trans(lo_lane ? xhi_l : xhi_h);
+                        // head hb's weight as fp16 high (column 2t) + low (column 2t + 1) halves
+                        WZ0 = fmaf(wa0, zv0, fmaf(wb0, zv1, WZ0));
+                        bb0 = movmatrix_trans(hi_lo_f16x2(wa0));
+                        bb1 = movmatrix_trans(hi_lo_f16x2(wb0));
                     }
                     const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp[b] + ((t)*H + h) * Gm::RB);
                     const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 4) * H + h) * Gm::RB);
@@ -748,7 +764,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 #pragma unroll
                         for (int mt = 0; mt < 8; ++mt) {
                             mma_f16_16816(o[mt], ua[mt], ubv[mt], uc[mt], ud[mt], bb0, bb1);
-                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ubv[mt], uc[mt], ud[mt], bb0l, bb1l);
                         }
                     } else {
                         uint32_t ua[8], uc[8];
@@ -757,7 +772,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 #pragma unroll
                         for (int mt = 0; mt < 4; ++mt) {
                             mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], bb0, bb1);
-                            if constexpr (WIDE) mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], bb0l, bb1l);
                         }
                     }
                 }
@@ -777,45 +791,51 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         }
         if (stop) break;
 
-        // ---- this warp's partial of unit j: (m, l) per column and O in fragment order, O scaled
-        // back by 2^(E - 127).  Lanes t < 2 hold the finished columns when the low halves ride in
-        // columns 4-7 (their sums are added in first).
+        // ---- this warp's partial of unit j: (m, l) per head and O in fragment order, O scaled back
+        // by 2^(E - 127).  Record slot (mt, ls) holds (row g: heads 2t', 2t'+1; row g + 8: the same
+        // heads) for ls = 2g + t' (t' < 2) when !WIDE, (row g: heads 2t, 2t+1; row g+8: ...) for
+        // ls = lane when WIDE; the (m, l) record of heads 2t', 2t'+1 sits at floats 4t' .. 4t'+3.
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
             WZ0 += __shfl_xor_sync(0xffffffffu, WZ0, off);
-            WZ1 += __shfl_xor_sync(0xffffffffu, WZ1, off);
-        }
-        if constexpr (!WIDE) {
-#pragma unroll
-            for (int mt = 0; mt < Gm::MT; ++mt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
+            if constexpr (WIDE) {
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+                WZ1 += __shfl_xor_sync(0xffffffffu, WZ1, off);
             }
-        }
-        // O = sum(w code) - sum(w zp)
-#pragma unroll
-        for (int mt = 0; mt < Gm::MT; ++mt) {
-            o[mt][0] -= WZ0;
-            o[mt][1] -= WZ1;
-            o[mt][2] -= WZ0;
-            o[mt][3] -= WZ1;
         }
         const float es = eref ? __uint_as_float(eref << 23) : 0.0f;   // 2^(eref - 127)
         const size_t recn = (size_t)u.z * kConsumerWarps + warp;
-        if (WIDE || t < 2) {
-            const int ls = WIDE ? lane : (g * 2 + t);
-            float4* po = reinterpret_cast<float4*>(p.ws_po + recn * PO) + ls;
+        if constexpr (WIDE) {
+            // O = sum(w code) - sum(w zp)
+            float4* po = reinterpret_cast<float4*>(p.ws_po + recn * PO) + lane;
 #pragma unroll
             for (int mt = 0; mt < Gm::MT; ++mt)
-                po[mt * NLS] = make_float4(o[mt][0] * es, o[mt][1] * es, o[mt][2] * es, o[mt][3] * es);
+                po[mt * NLS] = make_float4((o[mt][0] - WZ0) * es, (o[mt][1] - WZ1) * es, (o[mt][2] - WZ0) * es,
+                                           (o[mt][3] - WZ1) * es);
             if (g == 0) {
-                float* ml = p.ws_pml + recn * 16 + 2 * (2 * t);
+                float* ml = p.ws_pml + recn * 16 + 4 * t;
                 ml[0] = m0;
                 ml[1] = l0;
                 ml[2] = m1;
                 ml[3] = l1;
+            }
+        } else {
+            // head t = high + low weight columns; lanes with even t take their neighbour's head
+            float4* po = reinterpret_cast<float4*>(p.ws_po + recn * PO) + (g * 2 + (t >> 1));
+#pragma unroll
+            for (int mt = 0; mt < Gm::MT; ++mt) {
+                const float a = (o[mt][0] + o[mt][1] - WZ0) * es, b = (o[mt][2] + o[mt][3] - WZ0) * es;
+                const float a1 = __shfl_xor_sync(0xffffffffu, a, 1), b1 = __shfl_xor_sync(0xffffffffu, b, 1);
+                if ((t & 1) == 0) po[mt * NLS] = make_float4(a, a1, b, b1);
+            }
+            const float m_n = __shfl_xor_sync(0xffffffffu, m0, 1), l_n = __shfl_xor_sync(0xffffffffu, l0, 1);
+            if (g == 0 && (t & 1) == 0) {
+                float* ml = p.ws_pml + recn * 16 + 2 * t;
+                ml[0] = m0;
+                ml[1] = l0;
+                ml[2] = m_n;
+                ml[3] = l_n;
             }
         }
     }

@@ -126,48 +126,17 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // -------------------------------------------------------------------- packed fp32 (sm_100+)
 // Each lane of the pair is an independent IEEE round-to-nearest-even operation, so results are
-// bit-identical to two scalar operations.
+// bit-identical to two scalar operations.  The compiler builtins keep the pair in a register pair
+// (no packing moves around each operation).  a - b is fma(b, -1, a): the product is exact, so the
+// one rounding is that of a - b.
 
-__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
-    uint64_t ua, ub, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ua), "l"(ub));
-    float2 o;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
-    return o;
-}
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
-__device__ __forceinline__ float2 sub_f32x2(float2 a, float2 b) {
-    uint64_t ua, ub, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ua), "l"(ub));
-    float2 o;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
-    return o;
-}
+__device__ __forceinline__ float2 sub_f32x2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
 
-__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
-    uint64_t ua, ub, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ua), "l"(ub));
-    float2 o;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
-    return o;
-}
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
-__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
-    uint64_t ua, ub, uc, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ua), "l"(ub), "l"(uc));
-    float2 o;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
-    return o;
-}
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;

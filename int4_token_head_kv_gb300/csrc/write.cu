@@ -3,17 +3,25 @@
 // paged store ("[Feature] Triton INT4 / INT2 per-token-head KV cache quantization", description;
 // "PR #40835 report", get_kv_cache_shape).
 //
-// One thread encodes one (token, head, plane) vector entirely in registers.  Every arithmetic step
-// is an explicit round-to-nearest-even operation (intrinsics or packed fp32x2 PTX), so the bytes
-// are bit-exact with the definition in kv_int4.h regardless of how the compiler schedules them:
+// Two threads (a lane pair) encode one (token, head, plane) vector in registers.  Every arithmetic
+// step is an explicit round-to-nearest-even operation (intrinsics or packed fp32x2 builtins), so the
+// bytes are bit-exact with the definition in kv_int4.h regardless of how the compiler schedules them:
 //   butterflies at strides 1, 2, ..., D/2 (fixed order) -> multiply by c -> min/max ->
 //   s = (max - min) / 15 floored at 1e-6 -> s' = s with the low 4 mantissa bits cleared ->
 //   zp = clamp(rint(-min / s'), 0, 15) -> code = clamp(N(y * (1/s') + zp), 0, 15).
 // The last step uses one fused multiply-add against 1.5 * 2^23 + zp: the sum lands in
 // [2^23, 2^24) where the fp32 spacing is 1, so the single rounding of the FMA is exactly the
 // nearest-even integer of the real value y * r + zp, and the code sits in the low mantissa bits.
+//
+// The lane pair splits the vector by the parity of the element index after the stride-1
+// butterflies: thread t keeps elements 2m + t.  Each thread forms its own stride-1 outputs straight
+// from the inputs (a + b for t = 0, a - b for t = 1), and every later stride pairs two elements of
+// the same parity, so the rest of the rotation needs no exchange.  Only the min/max and the code
+// bytes (whose two nibbles come from the two threads) cross the pair.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "device.cuh"
 
@@ -39,65 +47,86 @@ __device__ __forceinline__ float2 upcast_pair<__half>(uint32_t w) {
     return __half22float2(h);
 }
 
-// load_vector: D 16-bit inputs (D/2 little-endian pairs) -> fp32 after the sign flips (XOR masks on
-// the pairs: bit 15 of each half is the sign in fp16 and bf16) and the stride-1 butterflies.
-// encode_vector: the remaining butterflies, normalisation, scale / zero-point and codes; output
-// the D/8 code words and the scale word of the cache row.
-template <int D, typename T>
-__device__ __forceinline__ void load_vector(const uint4* src, const uint32_t* sign_mask, float (&u)[D]) {
-#pragma unroll
-    for (int cc = 0; cc < D / 8; ++cc) {
-        const uint4 q = src[cc];
-        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int j = cc * 4 + e;
-            const float2 x = upcast_pair<T>(w4[e] ^ sign_mask[j]);
-            // stride-1 butterfly straight from the pair
-            u[2 * j] = __fadd_rn(x.x, x.y);
-            u[2 * j + 1] = __fsub_rn(x.x, x.y);
-        }
-    }
-}
-
+// Sign tables of the half-vector encoder, per element parity t (shared memory, built once per CTA):
+//   xmask[t][m]  XOR mask for input pair m: bit 31 = sign of element 2m + 1 times (t ? -1 : +1);
+//                bit 15 = sign of element 2m for fp16 inputs (bf16 inputs take it from even[]);
+//   even[k]      (sign of element 2k, sign of element 2(k + D/4)) as +-1.0f.
 template <int D>
-__device__ __forceinline__ void encode_vector(float (&u)[D], float c, uint32_t (&words)[Geo<D>::KW + 1]) {
-    using Gm = Geo<D>;
-    // strides 2 .. D/2, two lanes at a time
+struct WriteSigns {
+    uint32_t xmask[2][D / 2];
+    float2 even[D / 4];
+};
+
+// One thread's half of an INT4 vector.  row: the vector's D/2 input pairs (pair m = elements 2m,
+// 2m + 1, low half first) in shared memory; t: this thread's element parity.  With Q = D/4, thread t
+// holds P[k] = (u_{2k+t}, u_{2(k+Q)+t}) in a register pair.  A butterfly at stride 2s (s < Q) of the
+// element index pairs local m with m + s, i.e. P[k] with P[k + s] lane by lane; the stride D/2
+// pairs the two lanes of P[k].  The output: the Q/4 code words this thread stores (t = 0: words
+// 0 .. Q/4 - 1; t = 1: words Q/4 .. Q/2 - 1) and the scale word.
+template <int D, typename T>
+__device__ __forceinline__ void encode_half(const uint32_t* row, const WriteSigns<D>& sg, int t, float c,
+                                            uint32_t (&out)[D / 16 + 1]) {
+    constexpr int Q = D / 4;
+    float2 P[Q];
+    const uint32_t* xm = sg.xmask[t];
+    // stride 1: u_{2m+t} = a_m + (t ? -1 : 1) b_m, (a_m, b_m) = the sign-flipped input pair m
 #pragma unroll
-    for (int hs = 2; hs < D; hs <<= 1) {
+    for (int k = 0; k < Q; k += 4) {
+        const uint4 lo = *reinterpret_cast<const uint4*>(row + k);
+        const uint4 hi = *reinterpret_cast<const uint4*>(row + k + Q);
+        const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
+        const uint32_t ml[4] = {xm[k], xm[k + 1], xm[k + 2], xm[k + 3]};
+        const uint32_t mh[4] = {xm[k + Q], xm[k + Q + 1], xm[k + Q + 2], xm[k + Q + 3]};
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+            // odd element: its sign (and the parity's -1) by XOR while masking out the even half (one
+            // logic op); even element: its bits moved up, the sign applied by the (exact) product of
+            // the FMA
 #pragma unroll
-        for (int i = 0; i < D; i += 2) {
-            if (i & hs) continue;
-            const float2 a = make_float2(u[i], u[i + 1]);
-            const float2 b = make_float2(u[i + hs], u[i + hs + 1]);
-            const float2 s = add_f32x2(a, b);
-            const float2 d = sub_f32x2(a, b);
-            u[i] = s.x;
-            u[i + 1] = s.y;
-            u[i + hs] = d.x;
-            u[i + hs + 1] = d.y;
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = make_float2(__uint_as_float(wl[e] * 65536u), __uint_as_float(wh[e] * 65536u));
+                const float2 b = make_float2(__uint_as_float((wl[e] ^ ml[e]) & 0xFFFF0000u),
+                                             __uint_as_float((wh[e] ^ mh[e]) & 0xFFFF0000u));
+                P[k + e] = fma_f32x2(a, sg.even[k + e], b);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 xa = upcast_pair<T>(wl[e] ^ ml[e]);
+                const float2 xb = upcast_pair<T>(wh[e] ^ mh[e]);
+                P[k + e] = add_f32x2(make_float2(xa.x, xb.x), make_float2(xa.y, xb.y));
+            }
         }
     }
+    // strides 2, 4, ..., D/4 of the element index
+#pragma unroll
+    for (int st = 1; st < Q; st <<= 1) {
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            if (k & st) continue;
+            const float2 a = P[k], b = P[k + st];
+            P[k] = add_f32x2(a, b);
+            P[k + st] = sub_f32x2(a, b);
+        }
+    }
+    // stride D/2, then the normalisation
     const float2 c2 = make_float2(c, c);
 #pragma unroll
-    for (int i = 0; i < D; i += 2) {
-        const float2 y = mul_f32x2(make_float2(u[i], u[i + 1]), c2);
-        u[i] = y.x;
-        u[i + 1] = y.y;
-    }
-    // min / max over the rotated vector (exact)
-    float mx0 = u[0], mx1 = u[1], mn0 = u[0], mn1 = u[1];
+    for (int k = 0; k < Q; ++k)
+        P[k] = mul_f32x2(make_float2(__fadd_rn(P[k].x, P[k].y), __fsub_rn(P[k].x, P[k].y)), c2);
+    // min / max over the rotated vector (exact): this half, then the other
+    float mx0 = P[0].x, mx1 = P[0].y, mn0 = P[0].x, mn1 = P[0].y;
 #pragma unroll
-    for (int i = 2; i < D; i += 4) {
-        mx0 = max3(mx0, u[i], u[i + 1]);
-        mn0 = min3(mn0, u[i], u[i + 1]);
-        if (i + 3 < D) {
-            mx1 = max3(mx1, u[i + 2], u[i + 3]);
-            mn1 = min3(mn1, u[i + 2], u[i + 3]);
+    for (int k = 1; k < Q; k += 2) {
+        mx0 = max3(mx0, P[k].x, P[k].y);
+        mn0 = min3(mn0, P[k].x, P[k].y);
+        if (k + 1 < Q) {
+            mx1 = max3(mx1, P[k + 1].x, P[k + 1].y);
+            mn1 = min3(mn1, P[k + 1].x, P[k + 1].y);
         }
     }
-    const float mx = fmaxf(mx0, mx1), mn = fminf(mn0, mn1);
+    float mx = fmaxf(mx0, mx1), mn = fminf(mn0, mn1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
     float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
     if (!(s >= 1e-6f)) s = 1e-6f;
     const uint32_t sb = __float_as_uint(s) & 0xFFFFFFF0u;
@@ -107,26 +136,46 @@ __device__ __forceinline__ void encode_vector(float (&u)[D], float c, uint32_t (
     const float r = __frcp_rn(sp);
     const float zpm = kRoundMagic + (float)zp;   // exact
     // The map y -> RN(y * r + zpm) is monotone, so the codes of min and max bound all codes:
-    // clamping is needed only when one of them falls outside [0, 15].
+    // clamping is needed only when one of them falls outside [0, 15] (rare: a one-signed vector),
+    // and clamping codes already in range changes nothing, so the warp clamps all or none.
     const float lo = __fmaf_rn(mn, r, zpm), hi = __fmaf_rn(mx, r, zpm);
-    const bool clamp = !(lo >= kRoundMagic && hi <= kRoundMagic + 15.0f);
+    const bool clamp = __any_sync(0xffffffffu, !(lo >= kRoundMagic && hi <= kRoundMagic + 15.0f));
     const float2 r2 = make_float2(r, r), z2 = make_float2(zpm, zpm);
+    float2 f[Q];
 #pragma unroll
-    for (int wi = 0; wi < Gm::KW; ++wi) {
-        uint32_t acc = 0;
+    for (int k = 0; k < Q; ++k) f[k] = fma_f32x2(P[k], r2, z2);
+    if (clamp) {
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-            float2 f = fma_f32x2(make_float2(u[wi * 8 + k], u[wi * 8 + k + 1]), r2, z2);
-            if (clamp) {
-                f.x = fminf(fmaxf(f.x, kRoundMagic), kRoundMagic + 15.0f);
-                f.y = fminf(fmaxf(f.y, kRoundMagic), kRoundMagic + 15.0f);
-            }
-            acc += (__float_as_uint(f.x) << (4 * k)) + (__float_as_uint(f.y) << (4 * k + 4));
+        for (int k = 0; k < Q; ++k) {
+            f[k].x = fminf(fmaxf(f[k].x, kRoundMagic), kRoundMagic + 15.0f);
+            f[k].y = fminf(fmaxf(f[k].y, kRoundMagic), kRoundMagic + 15.0f);
         }
-        // each term carried kRoundMagicBits << 4k; their sum modulo 2^32 is 0x3F400000
-        words[wi] = acc - 0x3F400000u;
     }
-    words[Gm::KW] = sb | zp;
+    // Element 2m + t is the nibble 4t of row byte m, byte m % 4 of word m / 4: f[k].x (m = k) goes
+    // to word k / 4, f[k].y (m = k + Q) to word Q / 4 + k / 4.  A code's float has bits
+    // 0x4B400000 + code; four of them at bytes 0..3 (multiply-adds) sum to 0x8B400000 + the codes
+    // (mod 2^32), and the word is then moved up by 4t nibble bits: (sum - 0x8B400000) * 16^t.
+    const uint32_t mul = t ? 16u : 1u;
+    const uint32_t cst = t ? 0x4C000000u : 0x74C00000u;   // -(0x8B400000 * 16^t) mod 2^32
+    uint32_t xw[Q / 4], yw[Q / 4];
+#pragma unroll
+    for (int w = 0; w < Q / 4; ++w) {
+        const float2* g = f + 4 * w;
+        const uint32_t ax = __float_as_uint(g[0].x) + __float_as_uint(g[1].x) * 256u +
+                            __float_as_uint(g[2].x) * 65536u + __float_as_uint(g[3].x) * 16777216u;
+        const uint32_t ay = __float_as_uint(g[0].y) + __float_as_uint(g[1].y) * 256u +
+                            __float_as_uint(g[2].y) * 65536u + __float_as_uint(g[3].y) * 16777216u;
+        xw[w] = ax * mul + cst;
+        yw[w] = ay * mul + cst;
+    }
+    // thread 0 finishes the first half of the row's words, thread 1 the second: each sends the
+    // other the nibbles it holds of the other's words
+#pragma unroll
+    for (int w = 0; w < Q / 4; ++w) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, t ? xw[w] : yw[w], 1);
+        out[w] = (t ? yw[w] : xw[w]) | other;
+    }
+    out[Q / 4] = sb | zp;
 }
 
 // INT8 per-(token, head) comparator ("tests/quantization/test_per_token_kv_cache.py",
@@ -177,24 +226,23 @@ __device__ __forceinline__ void encode_vector_int8(const float (&u)[D], uint32_t
 }
 
 // Work split: vectors are numbered v = (t * 2 + plane) * H + h, so H consecutive vectors are one
-// (token, plane) row group, contiguous in the cache.  Each warp owns tiles of 32 consecutive
-// vectors and works through them on its own (no CTA-wide barriers): it prefetches the next tile's
-// inputs, one bulk async copy of 2D bytes per lane (its vector) completing on the buffer's
-// mbarrier, into one of two padded shared-memory buffers
-// (row stride 2D + 16 bytes, so the 16-byte reads of 8 neighbouring rows hit distinct banks),
-// encodes the current tile with one vector per lane, stages the encoded rows in the buffer it just
-// read, and writes each row group with one bulk async store (when H divides 32 and a group is a
-// multiple of 16 bytes; otherwise each lane stores its own row).
-constexpr int kWarpVecs = 32;
+// (token, plane) row group, contiguous in the cache.  Each warp owns tiles of TV consecutive vectors
+// (TV = 32 / threads per vector: 16 for INT4, 32 for INT8) and works through them on its own (no
+// CTA-wide barriers): it prefetches the next tile's inputs, one bulk async copy of 2D bytes per
+// vector completing on the buffer's mbarrier, into one of two padded shared-memory buffers (row
+// stride 2D + 16 bytes, so the 16-byte reads of 8 neighbouring rows hit distinct banks), encodes the
+// current tile, stages the encoded rows in the buffer it just read, and writes each row group with
+// one bulk async store (when H divides TV and a group is a multiple of 16 bytes; otherwise each
+// thread stores its own words).
 constexpr int kWriteWarps = kWriteThreads / 32;
 
-template <int D>
+template <int D, int TV>
 struct WriteSmem {
     static constexpr int kRowPad = 2 * D + 16;
-    static constexpr int kBuf = kWarpVecs * kRowPad;            // one tile of inputs
+    static constexpr int kBuf = TV * kRowPad;                   // one tile of inputs
     static constexpr int kPerWarp = 2 * kBuf;
     static constexpr int kBars = kWriteWarps * kPerWarp;        // two mbarriers per warp
-    static constexpr int kBytes = kBars + kWriteWarps * 2 * 8 + (D / 2) * 4;
+    static constexpr int kBytes = kBars + kWriteWarps * 2 * 8 + (int)sizeof(WriteSigns<D>);
 };
 
 
@@ -223,21 +271,33 @@ struct VecIndex {
     }
 };
 
+template <bool INT8>
+struct WriteShape {
+    static constexpr int kTpv = INT8 ? 1 : 2;          // threads per vector
+    static constexpr int kTileVecs = 32 / kTpv;        // vectors per warp tile
+    static constexpr int kMinBlocks = INT8 ? 3 : 5;    // resident CTAs per SM (register budget)
+};
+
 template <int D, typename T, bool INT8>
-__global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_constant__ WriteParams p) {
+__global__ void __launch_bounds__(kWriteThreads, WriteShape<INT8>::kMinBlocks)
+    write_kernel(const __grid_constant__ WriteParams p) {
     using Gm = Geo<D>;
+    using Sh = WriteShape<INT8>;
+    constexpr int TPV = Sh::kTpv, TV = Sh::kTileVecs;
     constexpr int RB = INT8 ? D + 4 : Gm::RB;       // cache row bytes
     constexpr int NW = INT8 ? D / 4 : Gm::KW;       // code words per row (then the scale word)
-    using Sm = WriteSmem<D>;
+    constexpr int OW = INT8 ? NW + 1 : D / 16 + 1;  // words one thread stores (the last: the scale word)
+    using Sm = WriteSmem<D, TV>;
     extern __shared__ __align__(128) uint8_t smem[];
     // Launched as a programmatic dependent: wait for the previous kernel of the stream (it may
     // produce K, V or the slots), then let the next kernel start its own set-up.
     griddep_wait();
     griddep_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int vl = lane / TPV, part = lane % TPV;   // this thread's vector of the tile and its part
     uint8_t* wbuf = smem + warp * Sm::kPerWarp;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sm::kBars) + warp * 2;   // this warp's [buffer]
-    uint32_t* sign_mask = reinterpret_cast<uint32_t*>(smem + Sm::kBars + kWriteWarps * 2 * 8);
+    WriteSigns<D>& sgn = *reinterpret_cast<WriteSigns<D>*>(smem + Sm::kBars + kWriteWarps * 2 * 8);
     if (lane == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
@@ -245,7 +305,13 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
     }
     for (int j = tid; j < (INT8 ? 0 : D / 2); j += kWriteThreads) {   // INT8 rows take no signs
         const float s0 = p.signs[2 * j], s1 = p.signs[2 * j + 1];
-        sign_mask[j] = ((__float_as_uint(s0) >> 31) << 15) | ((__float_as_uint(s1) >> 31) << 31);
+        // bf16 takes the even sign in the FMA (its mask flips only the odd element); fp16 in the XOR
+        const uint32_t m = ((std::is_same<T, __nv_bfloat16>::value ? 0u : (__float_as_uint(s0) >> 31)) << 15) |
+                           ((__float_as_uint(s1) >> 31) << 31);
+        sgn.xmask[0][j] = m;
+        sgn.xmask[1][j] = m ^ 0x80000000u;
+        float* ev = reinterpret_cast<float*>(sgn.even);   // element 2j: lane j / Q of pair j % Q
+        ev[2 * (j % (D / 4)) + j / (D / 4)] = s0 < 0.0f ? -1.0f : 1.0f;
         if (blockIdx.x == 0 && ((fabsf(s0) != 1.0f) || (fabsf(s1) != 1.0f))) count_status(p.status, 4);
     }
     __syncthreads();
@@ -256,17 +322,17 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
     vx.hmask = H - 1;
     vx.hshift = (H & (H - 1)) == 0 ? __ffs(H) - 1 : -1;
     const uint32_t nvec = (uint32_t)(p.num_tokens * H * 2);
-    const uint32_t ntiles = (nvec + kWarpVecs - 1) / kWarpVecs;
+    const uint32_t ntiles = (nvec + TV - 1) / TV;
     const uint32_t gwarp = blockIdx.x * kWriteWarps + warp, nwarps = gridDim.x * kWriteWarps;
     const uint32_t group_bytes = H * RB;
-    const bool grouped = vx.hshift >= 0 && H <= (uint32_t)kWarpVecs && (group_bytes % 16) == 0;
+    const bool grouped = vx.hshift >= 0 && H <= (uint32_t)TV && (group_bytes % 16) == 0;
     const uint8_t* kin = static_cast<const uint8_t*>(p.k);
     const uint8_t* vin = static_cast<const uint8_t*>(p.v);
 
-    // lane copies its vector of the tile (2D bytes) into row lane of the buffer
+    // lane i < TV copies vector i of the tile (2D bytes) into row i of the buffer
     auto prefetch = [&](uint32_t tile, uint8_t* buf, uint64_t* bar) {
-        const uint32_t v0 = tile * kWarpVecs;
-        const uint32_t live_vecs = min((uint32_t)kWarpVecs, nvec - v0);
+        const uint32_t v0 = tile * TV;
+        const uint32_t live_vecs = min((uint32_t)TV, nvec - v0);
         if (lane == 0) mbar_arrive_expect_tx(bar, live_vecs * (uint32_t)(D * 2));
         __syncwarp();
         if ((uint32_t)lane < live_vecs) {
@@ -294,49 +360,58 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
             waited_out = true;
             break;
         }
-        const uint32_t v = tile * kWarpVecs + lane;
+        const uint32_t v = tile * TV + vl;
         const bool live = v < nvec;
-        float u[D];
-        uint32_t words[NW + 1];
+        uint32_t words[OW];
         if constexpr (INT8) {
-            if (live) load_vector_raw<D, T>(reinterpret_cast<const uint4*>(cur + lane * Sm::kRowPad), u);
+            float u[D];
+            if (live) load_vector_raw<D, T>(reinterpret_cast<const uint4*>(cur + vl * Sm::kRowPad), u);
             __syncwarp();   // the tile's inputs are in registers; its buffer becomes the output stage
             if (live) encode_vector_int8<D>(u, words);
         } else {
-            if (live) load_vector<D, T>(reinterpret_cast<const uint4*>(cur + lane * Sm::kRowPad), sign_mask, u);
-            __syncwarp();   // the tile's inputs are in registers; its buffer becomes the output stage
-            if (live) encode_vector<D>(u, p.c, words);
+            // every lane runs the encoder (it exchanges values within the lane pair); a vector past
+            // the end reads row 0, which every tile holds, and its words are discarded
+            encode_half<D, T>(reinterpret_cast<const uint32_t*>(cur + (live ? vl : 0) * Sm::kRowPad), sgn, part,
+                              p.c, words);
+            __syncwarp();   // the tile's inputs are consumed; its buffer becomes the output stage
         }
+        // this thread's words of the row: all of them (INT8), or the first / second half of the code
+        // words (INT4 parts 0 / 1; part 1 also the scale word)
+        const int w0 = INT8 ? 0 : part * (D / 16);
+        const int nw = INT8 ? OW : (part ? OW : OW - 1);
         uint32_t tok = 0, h = 0, pl = 0;
         if (live) vx.split(v, tok, h, pl);
         if (grouped) {
-            uint32_t* orow = reinterpret_cast<uint32_t*>(cur + lane * RB);
+            uint32_t* orow = reinterpret_cast<uint32_t*>(cur + vl * RB) + w0;
             if (live) {
 #pragma unroll
-                for (int wi = 0; wi <= NW; ++wi) orow[wi] = words[wi];
+                for (int wi = 0; wi < OW; ++wi)
+                    if (wi < nw) orow[wi] = words[wi];
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staged rows -> bulk store
             __syncwarp();
-            // the first lane of each row group stores the whole group
-            if (live && h == 0) {
+            // the first thread of each row group stores the whole group
+            if (live && h == 0 && part == 0) {
                 const int64_t slot = __ldg(p.slots + tok);
                 if (slot >= p.num_slots) {
                     if (pl == 0) count_status(p.status, 0);
                 } else if (slot >= 0) {
                     const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
                     bulk_store_s2g(p.cache + ((blk * 2 + pl) * kBlockSize + off) * (int64_t)group_bytes,
-                                   cur + lane * RB, group_bytes);
+                                   cur + vl * RB, group_bytes);
                 }
             }
         } else if (live) {
             const int64_t slot = __ldg(p.slots + tok);
             if (slot >= p.num_slots) {
-                if (pl == 0 && h == 0) count_status(p.status, 0);
+                if (pl == 0 && h == 0 && part == 0) count_status(p.status, 0);
             } else if (slot >= 0) {
                 const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-                uint32_t* row = reinterpret_cast<uint32_t*>(p.cache + (((blk * 2 + pl) * kBlockSize + off) * H + h) * RB);
+                uint32_t* row =
+                    reinterpret_cast<uint32_t*>(p.cache + (((blk * 2 + pl) * kBlockSize + off) * H + h) * RB) + w0;
 #pragma unroll
-                for (int wi = 0; wi <= NW; ++wi) row[wi] = words[wi];
+                for (int wi = 0; wi < OW; ++wi)
+                    if (wi < nw) row[wi] = words[wi];
             }
         }
     }
@@ -349,10 +424,11 @@ __global__ void __launch_bounds__(kWriteThreads, 3) write_kernel(const __grid_co
 
 template <int D, typename T, bool INT8>
 cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
-    using Sm = WriteSmem<D>;
-    const int64_t ntiles = (p.num_tokens * p.H * 2 + kWarpVecs - 1) / kWarpVecs;
+    using Sh = WriteShape<INT8>;
+    using Sm = WriteSmem<D, Sh::kTileVecs>;
+    const int64_t ntiles = (p.num_tokens * p.H * 2 + Sh::kTileVecs - 1) / Sh::kTileVecs;
     int64_t blocks = (ntiles + kWriteWarps - 1) / kWriteWarps;
-    const int64_t cap = (int64_t)num_sms() * 3;
+    const int64_t cap = (int64_t)num_sms() * Sh::kMinBlocks;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     cudaError_t err = opt_in_smem<write_kernel<D, T, INT8>>(Sm::kBytes);
