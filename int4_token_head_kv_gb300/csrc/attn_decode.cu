@@ -128,6 +128,11 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long
     return before + x - v;
 }
 
+// The low nibble of a word as an exact float: 2^23 + n - 2^23 (one logic op and one add).
+__device__ __forceinline__ float nibble_to_float(uint32_t w) {
+    return __uint_as_float(0x4B000000u | (w & 15u)) - 8388608.0f;
+}
+
 __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
@@ -568,8 +573,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();   // this warp's reads of the buffer come before the count
-                if (atomicAdd(&qreleased[qs], 1) == kConsumerWarps - 1) {
-                    qreleased[qs] = 0;
+                // the counter wraps to 0 on the last warp's increment
+                if (atomicInc(reinterpret_cast<unsigned*>(&qreleased[qs]), kConsumerWarps - 1) == kConsumerWarps - 1) {
                     __threadfence_block();
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     if (run + nq < nruns && !*(volatile int*)flags) produce_q(run + nq);
@@ -654,7 +659,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     const bool v0 = ok[b] && tb + tk0 < u.w, v1 = ok[b] && tb + tk1 < u.w;
                     const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
                     // score = S - zp sum(Q'), then the key's scale and the logit factor
-                    const float zk0 = (float)(ks0 & 15u), zk1 = (float)(ks1 & 15u);
+                    const float zk0 = nibble_to_float(ks0), zk1 = nibble_to_float(ks1);
                     if constexpr (WIDE) {   // x = (token tk0: heads hb, hb+1; token tk1: heads hb, hb+1)
                         x[b][0] = v0 ? fmaf(-zk0, qs0, c[0]) * sk0 * al0 : -INFINITY;
                         x[b][1] = v0 ? fmaf(-zk0, qs1, c[1]) * sk0 * al1 : -INFINITY;
@@ -697,9 +702,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 l0 = l0 * r0 + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
                 if constexpr (WIDE) l1 = l1 * r1 + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
                 // ---- V scales: exponent reference so the fp16 weights stay in range
-                const uint32_t emax = max(max((vs0[0] >> 23) & 0xFFu, (vs1[0] >> 23) & 0xFFu),
-                                          max((vs0[1] >> 23) & 0xFFu, (vs1[1] >> 23) & 0xFFu));
-                const uint32_t eblk = __reduce_max_sync(0xffffffffu, emax);
+                // scale words are positive floats (zero for invisible tokens): their bit patterns order
+                // like the values, so the largest word carries the largest exponent
+                const uint32_t wmax = max(max(vs0[0], vs1[0]), max(vs0[1], vs1[1]));
+                const uint32_t eblk = (__reduce_max_sync(0xffffffffu, wmax) >> 23) & 0xFFu;
                 // The exponent reference moves only when a V scale passes it by more than kLazyExp
                 // binades (the fp16 weights then stay below 2^(kLazyMax + kLazyExp + 1)).
                 float escale = 1.0f;
@@ -731,7 +737,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     // weights w = p * s'_V * 2^-E (invisible tokens: 0)
                     const float wa0 = pr[b][0] * sv0, wa1 = pr[b][1] * sv0;   // token tk0
                     const float wb0 = pr[b][2] * sv1, wb1 = pr[b][3] * sv1;   // token tk1
-                    const float zv0 = (float)(vs0[b] & 15u), zv1 = (float)(vs1[b] & 15u);
+                    const float zv0 = nibble_to_float(vs0[b]), zv1 = nibble_to_float(vs1[b]);
                     uint32_t bb0, bb1;
                     if constexpr (WIDE) {
                         // All eight columns are heads: plain fp16 weights (they are not exponentiated
@@ -780,8 +786,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             if (lane == 0) {
                 __threadfence_block();   // this warp's reads of the stages come before the counts
                 for (int b = 0; b < npair; ++b) {
-                    if (atomicAdd(&released[st[b]], 1) == kConsumerWarps - 1) {
-                        released[st[b]] = 0;
+                    // the counter wraps to 0 on the last warp's increment
+                    if (atomicInc(reinterpret_cast<unsigned*>(&released[st[b]]), kConsumerWarps - 1) ==
+                        kConsumerWarps - 1) {
                         __threadfence_block();
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         if (i + b + kStages < nb_cta && !*(volatile int*)flags) produce(i + b + kStages);
