@@ -79,37 +79,6 @@ __device__ __forceinline__ int prescale_exponent(float maxabs) {
 
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
-// Rotate one query vector q (original domain) for the packed read path:
-//   v = H_d (D q) (unnormalised), e = prescale exponent, qh = fp16(v * 2^e),
-//   alpha = c * 2^-e * softmax_scale * log2(e)  (raw score -> log2-domain logit, before the
-//   key's scale s' is applied).
-// The warp writes qh and ql (D halves each) to shared memory and returns alpha (all lanes).
-// The scaled vector is kept as two fp16 halves, qh = fp16(v 2^e) and ql = fp16(v 2^e - qh) (the
-// difference is exact in fp32), so that qh + ql carries about 22 significant bits: a plain fp16
-// copy (11 bits) turns large keys into logit errors that a heavy-tailed cache makes visible.
-template <int D, typename QT>
-__device__ __forceinline__ float rotate_query(const void* q, int64_t qoff, const float* sgn, __half* qh, __half* ql,
-                                              float c, float softmax_scale) {
-    const int lane = threadIdx.x & 31;
-    float x[D / 32];
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) x[k] = load_elem<QT>(q, qoff + lane + 32 * k) * sgn[lane + 32 * k];
-    warp_fwht<D>(x);
-    float m = 0.0f;
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) m = fmaxf(m, fabsf(x[k]));
-    const int e = prescale_exponent(warp_max(m));
-    const float sc = exp2i(e);
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
-        const float y = x[k] * sc;
-        const __half hi = __float2half_rn(y);
-        qh[lane + 32 * k] = hi;
-        ql[lane + 32 * k] = __float2half_rn(y - __half2float(hi));
-    }
-    return c * exp2i(-e) * softmax_scale * kLog2e;
-}
-
 // Walsh-Hadamard transform of NB vectors of one warp at once (vector k: lane l holds
 // x[k][j] = v_k[l + 32 j]).  The butterfly stages of the NB vectors interleave, so the warp pays
 // one chain of shuffle latencies instead of NB.

@@ -9,25 +9,32 @@
 //                       high + low halves (two MMAs per k-step) held in tensor memory, B = the
 //                       tile's keys dequantised to exact fp16 (code - zp) in shared memory
 //                       (K-major, 128-byte swizzle); S accumulates in fp32 in tensor memory
-//   online softmax     per row: logit = S * s'_K * alpha, causal mask, a reference maximum that
-//                       moves only on jumps of more than 2^8; P_w = p * s'_V * 2^-E as fp16
-//                       written back over S (E: a reference exponent of the V scales)
+//   online softmax     per row: logit = S * s'_K * k0 * 2^-e (k0 = c * scale * log2(e), e the
+//                       row's query prescale), causal mask on the diagonal tiles, a reference
+//                       maximum m that moves only on jumps of more than 2^8; the weights
+//                       P_w = 2^(logit - m + 127 - E) * s'_V (one FMA before exp2; E a reference
+//                       exponent of the V scales) as fp16 written back over S, and their sum l'
+//                       carries the same 2^(127 - E), so out = O / l' without it
 //   O += P_w (V - zp)  tcgen05.mma, A = P_w from tensor memory, B = the values dequantised to
 //                       fp16 in shared memory (the same row layout as K, read MN-major); O stays
 //                       in tensor memory for the whole key range
 // and un-rotates its rows at the end.
 //
-// Warp roles (384 threads): warps 0-7 own the rows (warp w reads tensor-memory lanes
-// 32 (w % 4) .. + 31, the lower or upper half of the key columns for w < 4 or w >= 4), rotate the
-// queries and run the softmax and the epilogue; warps 8-11 load the packed codes of the next key
-// tile (one key per thread, registers double-buffered) and dequantise them into the shared-memory
-// tile pair of its parity.  Warp 8 also allocates tensor memory, and its first thread issues every
-// MMA after dequantising its key of each tile: S of tile j once the tile is in shared memory, then
-// P.V of tile j - 1 once its weights are in tensor memory (the double-buffered hand-offs impose
-// that order anyway).
+// Warp roles (416 threads): warps 0-7 own the rows (warp w reads tensor-memory lanes
+// 32 (w % 4) .. + 31, the lower or upper half of the key columns for w < 4 or w >= 4; warps w and
+// w + 4 exchange their halves' maxima), rotate the queries and run the softmax and the epilogue;
+// warps 8-11 load the packed codes of the next key tile (one key per thread, registers
+// double-buffered) and dequantise them into the shared-memory tile pair of its parity; warp 12
+// allocates tensor memory and one of its threads issues every MMA.
+// Dimension order: a tile row holds each code word's eight dimensions in the order the nibble
+// unpacking yields them (8w + 0, 4, 1, 5, 2, 6, 3, 7), so the dequantisation needs no permutes;
+// Q' is stored in tensor memory in the same order (the contraction over dimensions does not care),
+// and the epilogue puts O's columns back in dimension order.
 // Tensor memory (512 columns): Q' high, Q' low, two S buffers (S of tile j + 1 is computed while
 // the softmax of tile j runs), O.  Hand-offs go through mbarriers (tcgen05.commit for the MMAs);
 // every wait is bounded and a wait that gives up is counted and winds the CTA down.
+#include <type_traits>
+
 #include "attn_common.cuh"
 
 namespace kvi4 {
@@ -35,39 +42,53 @@ namespace {
 
 constexpr int kPfRows = 128;                  // query rows per CTA (the MMA M)
 constexpr int kPfKeys = 128;                  // keys per tile (the S MMA N, the P.V MMA K)
+constexpr int kPfPairs = 2;                   // fp16 K/V tile pairs in shared memory
+constexpr int kPfKRing = 4;                   // key-tile records (K scales, "K converted") in flight
+constexpr int kPfRawStages = 4;               // packed key tiles staged ahead of their conversion
 constexpr int kPfSoftmaxWarps = 8;
 constexpr int kPfDequantWarps = 4;
-constexpr int kPfMmaWarp = kPfSoftmaxWarps;   // the first dequantisation warp
-constexpr int kPfThreads = (kPfSoftmaxWarps + kPfDequantWarps) * 32;
+constexpr int kPfMmaWarp = kPfSoftmaxWarps + kPfDequantWarps;
+constexpr int kPfLoadWarps = 2;               // one per plane (K, V)
+constexpr int kPfThreads = (kPfMmaWarp + 1 + kPfLoadWarps) * 32;
 constexpr int kPfSoftmaxThreads = kPfSoftmaxWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kPfLazyMax = 8.0f;            // log2 units the row's reference maximum may trail
 constexpr uint32_t kPfLazyExp = 4;            // binades the V exponent reference may trail
 
 // Shared-memory layout (bytes from a 1024-aligned base).  A fp16 tile is 128 keys x D dims as
-// D/64 chunks of [128 rows x 128 B], 128-byte swizzled: [K tile 0][V tile 0][K tile 1][V tile 1].
-// Before the first tile the query halves are staged over tiles 1 (rows of D + 8 halves), and after
-// the last the fp32 output rows over tiles 0-1 (rows of D + 4 floats).
+// D/64 chunks of [128 rows x 128 B], 128-byte swizzled; kPfPairs K/V tile pairs (key tile j uses
+// pair j % kPfPairs): [K 0][V 0][K 1][V 1].  Before the first tile the query halves are staged from
+// pair 1 on (rows of D + 8 halves), and after the last the fp32 output rows over pairs 0-1 (rows
+// of D + 4 floats).  Then kPfRawStages staging buffers of packed rows as the cache holds them,
+// [plane][128 keys][kWindow words] (key tile j in stage j % kPfRawStages): a row of D/8 + 1 words
+// arrives with the 16-byte-aligned window of cache bytes around it, at its own word offset 0..3.
 template <int D>
 struct PfLayout {
     static constexpr uint32_t kTile = (D / 64) * kPfKeys * 128;
     static constexpr uint32_t kQStride = D + 8;                                   // halves per staged row
     static constexpr uint32_t kQStage = 2u * kPfRows * kQStride * 2;              // high + low
     static constexpr uint32_t kOStride = D + 4;                                   // floats per staged row
-    static constexpr uint32_t kMisc = ((4 * kTile > 2 * kTile + kQStage ? 4 * kTile : 2 * kTile + kQStage) +
+    static constexpr uint32_t kMisc = ((2 * kPfPairs * kTile > 2 * kTile + kQStage ? 2 * kPfPairs * kTile : 2 * kTile + kQStage) +
                                        1023u) & ~1023u;
     static_assert(kPfRows * kOStride * 4 <= 4 * kTile, "output staging");
+    static constexpr uint32_t kRowWords = D / 8 + 1;                              // packed row: codes + scale
+    static constexpr uint32_t kChunks = (kRowWords + 3 + 3) / 4;                  // 16-byte chunks of a window
+    static constexpr uint32_t kWindow = 4 * kChunks;
+    static constexpr uint32_t kRawStage = 2u * kPfKeys * kWindow * 4;
+    static constexpr uint32_t kRaw = kMisc;
     // misc region
-    static constexpr uint32_t kSk = kMisc;                           // [2][128] f32 key scales s'_K
-    static constexpr uint32_t kSv = kSk + 2 * kPfKeys * 4;           // [2][128] V scale words
-    static constexpr uint32_t kEblk = kSv + 2 * kPfKeys * 4;         // [2][4] per-warp max V exponent
-    static constexpr uint32_t kRowMax = kEblk + 2 * 4 * 4;           // [2 tiles][2 halves][128] f32
+    static constexpr uint32_t kSk = kRaw + kPfRawStages * kRawStage;    // [kring][128] f32 s'_K * k0 (0: no key)
+    static constexpr uint32_t kDeadF = kSk + kPfKRing * kPfKeys * 4;  // [kring][4] u32: a dequantising warp saw a key with no row
+    static constexpr uint32_t kSv = kDeadF + kPfKRing * 4 * 4;       // [pairs][128] f32 s'_V
+    static constexpr uint32_t kEblk = kSv + kPfPairs * kPfKeys * 4;  // [pairs][4] per-warp max V exponent
+    static constexpr uint32_t kRowMax = kEblk + kPfPairs * 4 * 4;    // [2 tiles][2 halves][128] f32
     static constexpr uint32_t kRowL = kRowMax + 2 * 2 * kPfRows * 4;  // [2][128] f32
-    static constexpr uint32_t kAlpha = kRowL + 2 * kPfRows * 4;      // [128] f32
+    static constexpr uint32_t kAlpha = kRowL + 2 * kPfRows * 4;      // [128] f32 2^-e of each row
     static constexpr uint32_t kSigns = kAlpha + kPfRows * 4;         // [D] f32
     static constexpr uint32_t kBars = (kSigns + D * 4 + 7u) & ~7u;   // mbarriers
-    // kv_full[2], pv_done[2], s_full[2], p_full[2], q_ready, flush, rows[2], q_stage, epi[2]
-    static constexpr int kNumBars = 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1 + 2;
+    // k_full[kring], k_free[pairs], v_full[pairs], v_free[pairs], pv_done[2], s_full[2], p_full[2], q_ready,
+    // flush, q_stage, epi[2], pairs[4][2], raw_full[stages], raw_free[stages]
+    static constexpr int kNumBars = kPfKRing + 3 * kPfPairs + 2 + 2 + 2 + 1 + 1 + 1 + 2 + 8 + 2 * kPfRawStages;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kFlags = kTmemSlot + 4;
     static constexpr uint32_t kBytes = kFlags + 4 + 1024;            // + alignment slack
@@ -107,17 +128,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive 32-bit tensor-memory columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -130,11 +140,38 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+// 16 lanes x 256 bits, four times along the columns (16 registers): thread i = 4 g + t gets, for
+// repetition c, r[4c] = (lane g, column 8c + 2t), r[4c + 1] = (g, 8c + 2t + 1), r[4c + 2] = (g + 8,
+// 8c + 2t), r[4c + 3] = (g + 8, 8c + 2t + 1), lanes counted from the address's lane.
+__device__ __forceinline__ void tmem_ld_q4(uint32_t taddr, uint32_t* r) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st_q4(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+// the same layout, one repetition (4 registers)
+__device__ __forceinline__ void tmem_st_q1(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+// the same layout, eight repetitions (32 registers)
+__device__ __forceinline__ void tmem_ld_q8(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
 
@@ -152,15 +189,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 // Byte offset of 16-byte chunk c (0..7) of row r in a [rows x 128 B] block with the 128-byte
 // swizzle the tensor-core descriptors expect: the chunk index is XOR-ed with r mod 8.
 __device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
-
-// Eight codes of one word (dims 8w .. 8w+7) as fp16 (code - zp) in dimension order.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t zp) {
-    const uint32_t zl = zp_lo_half(zp) * 0x10001u, zh = zp_hi_half(zp) * 0x10001u;
-    uint32_t o[4];
-    unpack_word(w, zl, zh, o);   // (e0,e4) (e1,e5) (e2,e6) (e3,e7)
-    return make_uint4(prmt(o[0], o[1], 0x5410u), prmt(o[2], o[3], 0x5410u), prmt(o[0], o[1], 0x7632u),
-                      prmt(o[2], o[3], 0x7632u));
-}
 
 template <int D, typename QT, typename OT>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ AttnParams p) {
@@ -198,37 +226,55 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const int nkt = cta_lim >= 0 ? cta_lim / kPfKeys + 1 : 0;
 
     float* sk = reinterpret_cast<float*>(smem + Ly::kSk);
-    uint32_t* sv = reinterpret_cast<uint32_t*>(smem + Ly::kSv);
+    float* sv = reinterpret_cast<float*>(smem + Ly::kSv);
     uint32_t* eblkw = reinterpret_cast<uint32_t*>(smem + Ly::kEblk);
     float* rowmax = reinterpret_cast<float*>(smem + Ly::kRowMax);
     float* rowl = reinterpret_cast<float*>(smem + Ly::kRowL);
     float* alpha = reinterpret_cast<float*>(smem + Ly::kAlpha);
     float* sgn = reinterpret_cast<float*>(smem + Ly::kSigns);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBars);
-    uint64_t* kv_full = bars;        // [2] dequantised tile ready (128 arrivals)
-    uint64_t* pv_done = bars + 2;    // [2] P.V of the tile done (commit): its tiles and S buffer free
-    uint64_t* s_full = bars + 4;     // [2] S of the tile in tensor memory (commit)
-    uint64_t* p_full = bars + 6;     // [2] P of the tile in tensor memory (256 arrivals)
-    uint64_t* q_ready = bars + 8;    // queries in tensor memory, staging free (256 arrivals)
-    uint64_t* flush = bars + 9;      // the MMA thread's last commit (teardown)
-    // barriers among the 256 row threads (bounded waits, unlike a hardware named barrier): the
-    // row-maximum exchange of tiles of each parity, the query staging, the epilogue's two steps
-    uint64_t* rows_sync = bars + 10;
-    uint64_t* q_stage = bars + 12;
-    uint64_t* epi = bars + 13;
+    // The K and V halves of a tile pair live apart: K tile j is free once S of tile j is done, V tile
+    // j once its P.V is.  "K converted" is kept per key tile mod kPfKRing so that no record is
+    // overwritten before the rows of its tile have read it (tile j + 4 waits for S of tile j + 2,
+    // which waits for P.V of tile j).
+    uint64_t* k_full = bars;                    // [kring] K tile and scales of tile j (128 arrivals)
+    uint64_t* k_free = k_full + kPfKRing;       // [pairs] K tile j % 2 read by S of tile j (commit)
+    uint64_t* v_full = k_free + kPfPairs;       // [pairs] V tile and scales of tile j (128 arrivals)
+    uint64_t* v_free = v_full + kPfPairs;       // [pairs] V tile j % 2 read by P.V of tile j (commit)
+    uint64_t* pv_done = v_free + kPfPairs;      // [2] P.V of tile j done (commit): S buffer j % 2 and O free
+    uint64_t* s_full = pv_done + 2;             // [2] S of the tile in tensor memory (commit)
+    uint64_t* p_full = s_full + 2;              // [2] P of the tile in tensor memory (256 arrivals)
+    uint64_t* q_ready = p_full + 2;             // queries in tensor memory, staging free (256 arrivals)
+    uint64_t* flush = q_ready + 1;              // the MMA thread's last commit (teardown)
+    // barriers among the 256 row threads (bounded waits, unlike a hardware named barrier): the query
+    // staging, and the epilogue's staged output rows
+    uint64_t* q_stage = flush + 1;
+    uint64_t* epi = q_stage + 1;
+    uint64_t* raw_full = epi + 1;            // [stages] packed rows of a key tile landed (64 lanes)
+    uint64_t* raw_free = raw_full + kPfRawStages;   // [stages] that stage converted (128 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kFlags);
 
     if (threadIdx.x == 0) {
+        for (int b = 0; b < kPfKRing; ++b) mbar_init(&k_full[b], kPfDequantWarps * 32);
+        for (int b = 0; b < kPfPairs; ++b) {
+            mbar_init(&k_free[b], 1);
+            mbar_init(&v_full[b], kPfDequantWarps * 32);
+            mbar_init(&v_free[b], 1);
+        }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&kv_full[b], kPfDequantWarps * 32);
             mbar_init(&pv_done[b], 1);
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], kPfSoftmaxThreads);
         }
         mbar_init(q_ready, kPfSoftmaxThreads);
         mbar_init(flush, 1);
-        for (int i = 0; i < 5; ++i) mbar_init(&rows_sync[i], kPfSoftmaxThreads);   // rows_sync[2], q_stage, epi[2]
+        mbar_init(q_stage, kPfSoftmaxThreads);
+        mbar_init(epi, kPfSoftmaxThreads);
+        for (int i = 0; i < kPfRawStages; ++i) {
+            mbar_init(&raw_full[i], kPfLoadWarps * 32);
+            mbar_init(&raw_free[i], kPfDequantWarps * 32);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -253,7 +299,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         if (atomicExch(const_cast<int*>(abort_flag), 1) == 0) count_status(p.status, 3);
         return false;
     };
-    // all 256 row threads meet (warp-uniform result)
+    // the row threads counted by the barrier meet (warp-uniform result)
     auto rows_meet = [&](uint64_t* bar, uint32_t parity) -> bool {
         mbar_arrive(bar);
         return __all_sync(0xffffffffu, wait(bar, parity));
@@ -265,36 +311,70 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         __half* qs_hi = reinterpret_cast<__half*>(ktile(1));
         __half* qs_lo = qs_hi + kPfRows * Ly::kQStride;
-        // ---- rotate the queries: warp w the rows 16 w .. 16 w + 15 (lanes across dimensions)
-        for (int i = 0; i < kPfRows / kPfSoftmaxWarps; ++i) {
-            const int R = warp * (kPfRows / kPfSoftmaxWarps) + i;
-            const int qt = qt0 + R / G, gg = R % G;
-            if (nkt > 0 && qt < qlen) {
-                const float a = rotate_query<D, QT>(p.q, ((int64_t)(q0 + qt) * Hq + h * G + gg) * D, sgn,
-                                                    qs_hi + R * Ly::kQStride, qs_lo + R * Ly::kQStride, p.c,
-                                                    p.softmax_scale);
-                if (lane == 0) alpha[R] = a;
-            } else {
-                for (int k = lane; k < D; k += 32) qs_hi[R * Ly::kQStride + k] = qs_lo[R * Ly::kQStride + k] = __float2half(0.0f);
-                if (lane == 0) alpha[R] = 0.0f;
+        // ---- rotate the queries, lanes across dimensions.  A warp loads a batch of rows before it
+        // transforms any (one memory latency per batch), then rotates four at a time (interleaved
+        // butterflies): v = H_d (D q), a power-of-two prescale 2^e bringing max|v| into
+        // [2^14, 2^15), and fp16 high + low halves (qh + ql carries about 22 bits: a plain fp16 copy
+        // turns large keys into logit errors a heavy-tailed cache shows).
+        // Warp w rotates rows 16 w .. 16 w + 15 in two batches of eight.
+        auto rotate_rows = [&](int first, auto nrows_c) {
+            constexpr int NR = decltype(nrows_c)::value;
+            float x[NR][D / 32];
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                const int R = first + i;
+                const int qt = qt0 + R / G, gg = R % G;
+                const bool live = nkt > 0 && qt < qlen;
+                const int64_t qoff = ((int64_t)(q0 + (live ? qt : 0)) * Hq + h * G + gg) * D;
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k)
+                    x[i][k] = live ? load_elem<QT>(p.q, qoff + lane + 32 * k) * sgn[lane + 32 * k] : 0.0f;
             }
+#pragma unroll
+            for (int i0 = 0; i0 < NR; i0 += 4) {
+                float (&xb)[4][D / 32] = *reinterpret_cast<float(*)[4][D / 32]>(&x[i0][0]);
+                warp_fwht_batch<D, 4>(xb);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int R = first + i0 + v;
+                    float mx = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < D / 32; ++k) mx = fmaxf(mx, fabsf(xb[v][k]));
+                    const int e = prescale_exponent(warp_max(mx));
+                    const float sc = exp2i(e);
+#pragma unroll
+                    for (int k = 0; k < D / 32; ++k) {
+                        const float y = xb[v][k] * sc;
+                        const __half hi = __float2half_rn(y);
+                        qs_hi[R * Ly::kQStride + lane + 32 * k] = hi;
+                        qs_lo[R * Ly::kQStride + lane + 32 * k] = __float2half_rn(y - __half2float(hi));
+                    }
+                    if (lane == 0) alpha[R] = exp2i(-e);   // rows with no query (zeros) give 2^0
+                }
+            }
+        };
+        {
+            constexpr int RPW = kPfRows / kPfSoftmaxWarps;
+            rotate_rows(warp * RPW, std::integral_constant<int, 8>{});
+            rotate_rows(warp * RPW + 8, std::integral_constant<int, 8>{});
         }
         bool ok = rows_meet(q_stage, 0);
-        // ---- this thread's half of its row into tensor memory (high, then low halves)
+        // ---- this thread's half of its row into tensor memory (high, then low halves), each group
+        // of eight dimensions in the tile order 0, 4, 1, 5, 2, 6, 3, 7
         if (ok) {
             constexpr int kWords = D / 4;   // 32-bit words of a half row
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
-                const uint32_t* src = reinterpret_cast<const uint32_t*>((part ? qs_lo : qs_hi) + r * Ly::kQStride) +
-                                      hf * kWords;
+                const uint4* src = reinterpret_cast<const uint4*>((part ? qs_lo : qs_hi) + r * Ly::kQStride) +
+                                   hf * (kWords / 4);
                 uint32_t w[kWords];
 #pragma unroll
                 for (int j = 0; j < kWords; j += 4) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(src + j);
-                    w[j] = v.x;
-                    w[j + 1] = v.y;
-                    w[j + 2] = v.z;
-                    w[j + 3] = v.w;
+                    const uint4 v = src[j / 4];   // halves d0..d7 of one group
+                    w[j] = prmt(v.x, v.z, 0x5410u);       // (d0, d4)
+                    w[j + 1] = prmt(v.x, v.z, 0x7632u);   // (d1, d5)
+                    w[j + 2] = prmt(v.y, v.w, 0x5410u);   // (d2, d6)
+                    w[j + 3] = prmt(v.y, v.w, 0x7632u);   // (d3, d7)
                 }
                 const uint32_t ta = tmem + lane_base + (part ? Tm::kQl : Tm::kQh) + hf * kWords;
                 if constexpr (kWords == 32) {
@@ -308,64 +388,99 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         }
         tc_fence_before();
         mbar_arrive(q_ready);
-        const float al = alpha[r];
-        const int qt_r = qt0 + r / G;
-        const int pos_r = qt_r < qlen ? pos0 + qt_r : -1;   // last visible key of this row
-        float m = kNegBig, l = 0.0f;
-        uint32_t E = 0;   // reference biased exponent of the V scales
+        // ---- the key tiles.  Warp w owns the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15 in the 16-lane
+        // tensor-memory layout: thread (g, t) = (lane / 4, lane % 4) holds rows ra = rbase + g and
+        // rb = ra + 8 and, of every group of 8 key columns, columns 2t and 2t + 1; a row's maximum
+        // and sum meet over its four threads by two shuffles.
+        const int rbase = 32 * (warp & 3) + 16 * (warp >> 2);
+        const int t4 = lane & 3;
+        const int ra = rbase + (lane >> 2), rb = ra + 8;
+        const uint32_t trow = tmem + ((uint32_t)rbase << 16);
+        const float rs_a = alpha[ra], rs_b = alpha[rb];   // 2^-e of each row's query prescale
+        const int qta = qt0 + ra / G, qtb = qt0 + rb / G;
+        const int pos_a = qta < qlen ? pos0 + qta : -1, pos_b = qtb < qlen ? pos0 + qtb : -1;   // last visible key
+        float m_a = kNegBig, m_b = kNegBig;     // reference maxima (log2 units)
+        float l_a = 0.0f, l_b = 0.0f;           // this thread's part of the sums of 2^(127-E) p
+        uint32_t E = 0;                         // reference biased exponent of the V scales (0: none yet)
+        const uint32_t* deadf = reinterpret_cast<const uint32_t*>(smem + Ly::kDeadF);
 
         for (int j = 0; j < nkt && ok; ++j) {
             const int b = j & 1;
             const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-            ok = wait(&s_full[b], ph) && wait(&kv_full[b], ph);
+            const int kb = j % kPfPairs, kr = j % kPfKRing;
+            ok = wait(&s_full[b], ph) && wait(&k_full[kr], (uint32_t)(j / kPfKRing) & 1u) &&
+                 wait(&v_full[kb], (uint32_t)(j / kPfPairs) & 1u);
             if (__any_sync(0xffffffffu, !ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t scol = (b ? Tm::kS1 : Tm::kS0) + (uint32_t)hf * 64u;
-            uint32_t s[64];
-            tmem_ld32(tmem + lane_base + scol, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld32(tmem + lane_base + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            const uint32_t scol = trow + (b ? Tm::kS1 : Tm::kS0);
+            uint32_t s[64];   // s[4i], s[4i + 1]: row a, columns 8i + 2t, + 1; s[4i + 2], s[4i + 3]: row b
+            tmem_ld_q8(scol, s);
+            tmem_ld_q8(scol + 64, s + 32);
             tmem_ld_wait();
-            const int key0 = j * kPfKeys + hf * 64;
-            const float* skb = sk + b * kPfKeys + hf * 64;
-            float bm = -INFINITY;
-            const bool full = key0 + 63 <= pos_r;   // no causal mask in this half-tile
+            // x = S * s'_K * k0 (0 scale: no key), masked; the row maxima
+            const int key0 = j * kPfKeys;
+            const float* skb = sk + kr * kPfKeys + 2 * t4;
+            const bool clean = (deadf[kr * 4] | deadf[kr * 4 + 1] | deadf[kr * 4 + 2] | deadf[kr * 4 + 3]) == 0u &&
+                               key0 + kPfKeys - 1 <= min(pos_a, pos_b);
+            float bma = -INFINITY, bmb = -INFINITY;
+            if (__all_sync(0xffffffffu, clean)) {   // every key live and visible to both rows
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 k4 = *reinterpret_cast<const float4*>(skb + c);
-                const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+                for (int i = 0; i < 16; ++i) {
+                    const float2 k2 = *reinterpret_cast<const float2*>(skb + 8 * i);
+                    const float2 xa = mul_f32x2(make_float2(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1])), k2);
+                    const float2 xb = mul_f32x2(make_float2(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])), k2);
+                    s[4 * i] = __float_as_uint(xa.x);
+                    s[4 * i + 1] = __float_as_uint(xa.y);
+                    s[4 * i + 2] = __float_as_uint(xb.x);
+                    s[4 * i + 3] = __float_as_uint(xb.y);
+                    bma = fmaxf(bma, fmaxf(xa.x, xa.y));
+                    bmb = fmaxf(bmb, fmaxf(xb.x, xb.y));
+                }
+            } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool vis = kk[e] > 0.0f && (full || key0 + c + e <= pos_r);
-                    const float x = vis ? __uint_as_float(s[c + e]) * kk[e] * al : -INFINITY;
-                    s[c + e] = __float_as_uint(x);
-                    bm = fmaxf(bm, x);
+                for (int i = 0; i < 16; ++i) {
+                    const float2 k2 = *reinterpret_cast<const float2*>(skb + 8 * i);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float kk = e ? k2.y : k2.x;
+                        const int key = key0 + 8 * i + 2 * t4 + e;
+                        const float xa = kk > 0.0f && key <= pos_a ? __uint_as_float(s[4 * i + e]) * kk : -INFINITY;
+                        const float xb = kk > 0.0f && key <= pos_b ? __uint_as_float(s[4 * i + 2 + e]) * kk : -INFINITY;
+                        s[4 * i + e] = __float_as_uint(xa);
+                        s[4 * i + 2 + e] = __float_as_uint(xb);
+                        bma = fmaxf(bma, xa);
+                        bmb = fmaxf(bmb, xb);
+                    }
                 }
             }
-            float* rm = rowmax + (b * 2) * kPfRows;
-            rm[hf * kPfRows + r] = bm;
-            if (!rows_meet(&rows_sync[b], ph)) {
-                ok = false;
-                break;
-            }
-            bm = fmaxf(bm, rm[(1 - hf) * kPfRows + r]);
-            // reference maximum and V exponent (the same decisions in both halves of a row; E in
-            // every row, from the tile's per-warp maxima)
-            const bool up = bm > m + kPfLazyMax;
-            const float fm = up ? fast_exp2(m - bm) : 1.0f;
-            if (up) m = bm;
-            const uint32_t* eb4 = eblkw + b * 4;
+            bma = fmaxf(bma, __shfl_xor_sync(0xffffffffu, bma, 1));
+            bmb = fmaxf(bmb, __shfl_xor_sync(0xffffffffu, bmb, 1));
+            bma = fmaxf(bma, __shfl_xor_sync(0xffffffffu, bma, 2));
+            bmb = fmaxf(bmb, __shfl_xor_sync(0xffffffffu, bmb, 2));
+            // in log2 units (rs > 0: a power of two scales exactly); the four threads of a row take
+            // the same decisions
+            bma *= rs_a;
+            bmb *= rs_b;
+            const bool up_a = bma > m_a + kPfLazyMax, up_b = bmb > m_b + kPfLazyMax;
+            const float fm_a = up_a ? fast_exp2(m_a - bma) : 1.0f, fm_b = up_b ? fast_exp2(m_b - bmb) : 1.0f;
+            if (up_a) m_a = bma;
+            if (up_b) m_b = bmb;
+            const uint32_t* eb4 = eblkw + kb * 4;
             const uint32_t eb = max(max(eb4[0], eb4[1]), max(eb4[2], eb4[3]));
+            const uint32_t Eeff = E ? E : 127u;
             float fe = 1.0f;
-            if (eb > E + kPfLazyExp || (E == 0u && eb > 0u)) {
-                fe = (E == 0u || eb - E > 126u) ? 0.0f : __uint_as_float((127u + E - eb) << 23);
+            if (E == 0u ? eb > 0u : eb > E + kPfLazyExp) {
+                // rebase from 2^(127 - Eeff) to 2^(127 - eb); 0 when the jump underflows
+                fe = eb > Eeff + 126u ? 0.0f : __uint_as_float((127u + Eeff - eb) << 23);
                 E = eb;
             }
-            l *= fm;
-            const float f = fm * fe;
-            if (j > 0 && __any_sync(0xffffffffu, f != 1.0f)) {
+            const float f_a = fm_a * fe, f_b = fm_b * fe;
+            l_a *= f_a;
+            l_b *= f_b;
+            if (j > 0 && __any_sync(0xffffffffu, f_a != 1.0f || f_b != 1.0f)) {
                 // O must hold P.V of the previous tile before it is rescaled
                 ok = wait(&pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u);
                 if (__any_sync(0xffffffffu, !ok)) {
@@ -373,183 +488,298 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     break;
                 }
                 tc_fence_after();
+                const float2 fa2 = make_float2(f_a, f_a), fb2 = make_float2(f_b, f_b);
 #pragma unroll
-                for (int c0 = 0; c0 < D / 2; c0 += 16) {
+                for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[16];
-                    tmem_ld16(tmem + lane_base + Tm::kO + hf * (D / 2) + c0, o);
+                    tmem_ld_q4(trow + Tm::kO + c0, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_st16(tmem + lane_base + Tm::kO + hf * (D / 2) + c0, o);
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 oa = mul_f32x2(make_float2(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1])), fa2);
+                        const float2 ob = mul_f32x2(make_float2(__uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3])), fb2);
+                        o[4 * i] = __float_as_uint(oa.x);
+                        o[4 * i + 1] = __float_as_uint(oa.y);
+                        o[4 * i + 2] = __float_as_uint(ob.x);
+                        o[4 * i + 3] = __float_as_uint(ob.y);
+                    }
+                    tmem_st_q4(trow + Tm::kO + c0, o);
                 }
                 tmem_st_wait();
             }
-            // weights w = p * s'_V * 2^-E as fp16 pairs, written over this half's first 32 S columns
-            const float wsc = __uint_as_float((254u - E) << 23);   // 2^(127 - E)
-            const uint32_t* svb = sv + b * kPfKeys + hf * 64;
-            float ls = 0.0f;
+            // p' = 2^(x rs - m + 127 - E), w = p' s'_V as fp16 pairs over the first 64 S columns: the
+            // pair of columns 8i + 2t, + 1 goes to column 8 (i / 2) + 2t + i % 2 (the V tile holds its
+            // rows in the matching order)
+            const float eoff = (float)(127 - (int)(E ? E : 127u));
+            const float2 rsa2 = make_float2(rs_a, rs_a), rsb2 = make_float2(rs_b, rs_b);
+            const float2 moa2 = make_float2(eoff - m_a, eoff - m_a), mob2 = make_float2(eoff - m_b, eoff - m_b);
+            const float* svb = sv + kb * kPfKeys + 2 * t4;
+            float2 lsa = make_float2(0.0f, 0.0f), lsb = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                uint32_t pw[16];
+            for (int q = 0; q < 8; ++q) {
+                uint32_t pw[4];
 #pragma unroll
-                for (int c = c0; c < c0 + 32; c += 4) {
-                    const uint4 v4 = *reinterpret_cast<const uint4*>(svb + c);
-                    const uint32_t vv[4] = {v4.x, v4.y, v4.z, v4.w};
-                    float w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float pr = fast_exp2(__uint_as_float(s[c + e]) - m);
-                        ls += pr;
-                        w[e] = pr * (__uint_as_float(vv[e] & 0xFFFFFFF0u) * wsc);
-                    }
-                    pw[(c - c0) / 2] = pack_f16x2(w[0], w[1]);
-                    pw[(c - c0) / 2 + 1] = pack_f16x2(w[2], w[3]);
+                for (int i = 2 * q; i < 2 * q + 2; ++i) {
+                    const float2 v2 = *reinterpret_cast<const float2*>(svb + 8 * i);
+                    const float2 ea = fma_f32x2(make_float2(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1])), rsa2, moa2);
+                    const float2 eb2 = fma_f32x2(make_float2(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])), rsb2, mob2);
+                    const float2 pa = make_float2(fast_exp2(ea.x), fast_exp2(ea.y));
+                    const float2 pb = make_float2(fast_exp2(eb2.x), fast_exp2(eb2.y));
+                    lsa = add_f32x2(lsa, pa);
+                    lsb = add_f32x2(lsb, pb);
+                    const float2 wa = mul_f32x2(pa, v2), wb = mul_f32x2(pb, v2);
+                    const int e = i & 1;
+                    pw[e] = pack_f16x2(wa.x, wa.y);
+                    pw[2 + e] = pack_f16x2(wb.x, wb.y);
                 }
-                tmem_st16(tmem + lane_base + scol + c0 / 2, pw);
+                tmem_st_q1(scol + 8 * q, pw);
             }
-            l += ls;
+            l_a += lsa.x + lsa.y;
+            l_b += lsb.x + lsb.y;
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&p_full[b]);
         }
-        // ---- epilogue: O / l, scaled back by 2^(E - 127), staged, un-rotated
+        // ---- epilogue: O / l' (the 2^(127 - E) of both cancels), staged in dimension order, un-rotated
         if (ok && nkt > 0) ok = wait(&pv_done[(nkt - 1) & 1], (uint32_t)((nkt - 1) >> 1) & 1u);
         tc_fence_after();
-        rowl[hf * kPfRows + r] = l;
-        ok = rows_meet(&epi[0], 0) && ok;
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+        // the last P.V is done, so nothing reads the tile pairs the staging below overwrites
         const bool good = __all_sync(0xffffffffu, ok) && nkt > 0;
-        const float lt = l + rowl[(1 - hf) * kPfRows + r];
-        const float es = E ? __uint_as_float(E << 23) : 0.0f;
-        const float sc = lt > 0.0f ? es / lt : 0.0f;
-        float* ostage = reinterpret_cast<float*>(tiles);
-        if (good) {
+        const float sc_a = l_a > 0.0f ? 1.0f / l_a : 0.0f, sc_b = l_b > 0.0f ? 1.0f / l_b : 0.0f;
+        float* ost_a = reinterpret_cast<float*>(tiles) + ra * Ly::kOStride;
+        float* ost_b = reinterpret_cast<float*>(tiles) + rb * Ly::kOStride;
 #pragma unroll
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + Tm::kO + hf * (D / 2) + c0, o);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[16];
+            if (good) {
+                tmem_ld_q4(trow + Tm::kO + c0, o);
                 tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) ostage[r * Ly::kOStride + hf * (D / 2) + c0 + e] = __uint_as_float(o[e]) * sc;
             }
-        } else {
-            for (int e = 0; e < D / 2; ++e) ostage[r * Ly::kOStride + hf * (D / 2) + e] = 0.0f;
+            // column 8w + j holds dimension 8w + (0, 4, 1, 5, 2, 6, 3, 7)[j]
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int c = c0 + 8 * i + 2 * t4 + e;
+                    const int d = (c & ~7) + ((c & 1) << 2) + ((c & 7) >> 1);
+                    ost_a[d] = good ? __uint_as_float(o[4 * i + e]) * sc_a : 0.0f;
+                    ost_b[d] = good ? __uint_as_float(o[4 * i + 2 + e]) * sc_b : 0.0f;
+                }
+            }
         }
-        if (!rows_meet(&epi[1], 0)) ok = false;
+        if (!rows_meet(epi, 0)) ok = false;
+        const float* ost = reinterpret_cast<const float*>(tiles);
         for (int i = 0; i < kPfRows / kPfSoftmaxWarps && ok; ++i) {
             const int R = warp * (kPfRows / kPfSoftmaxWarps) + i;
             const int qt = qt0 + R / G, gg = R % G;
             if (qt >= qlen) continue;
             float xv[D / 32];
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) xv[k] = ostage[R * Ly::kOStride + lane + 32 * k];
+            for (int k = 0; k < D / 32; ++k) xv[k] = ost[R * Ly::kOStride + lane + 32 * k];
             unrotate_store<D, OT>(xv, 1.0f, sgn, p.c, p.out, ((int64_t)(q0 + qt) * Hq + h * G + gg) * D);
         }
-    } else {
+    } else if (warp < kPfMmaWarp) {
         // ================================================================ dequantisation of key tiles
         const int k = threadIdx.x - kPfSoftmaxThreads;   // this thread's key of every tile
-        const bool issuer = k == 0;                        // warp 8, lane 0: also issues the MMAs
+        constexpr int NW = Ly::kRowWords;                 // words of a row: codes, then the scale word
+        const float k0 = p.c * p.softmax_scale * kLog2e;  // raw score -> log2 logit, before 2^-e
+        // word offset of this key's rows in their windows: rows of token slot r start at byte
+        // (r H + h) (D/2 + 4) of a block plane, the cache and its block and plane strides are
+        // multiples of 16 bytes, and D/2 + 4 is 4 mod 16
+        const int row_off = ((k % kBlockSize) * H + h) & 3;
+        // the V tile row of this key: the weights of S columns 16 q + 8 e + 2 t + b sit at
+        // contraction position 16 q + 4 t + 2 e + b (the 16-lane tensor-memory layout they are
+        // written in)
+        const uint32_t vrow = (uint32_t)((k & ~15) + 4 * ((k >> 1) & 3) + 2 * ((k >> 3) & 1) + (k & 1));
+        for (int j = 0; j < nkt; ++j) {
+            const int kb = j % kPfPairs, st = j % kPfRawStages;
+            bool ok = wait(&raw_full[st], (uint32_t)(j / kPfRawStages) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            // this key's K and V windows (16-byte loads; lanes k..k+7 hit eight distinct 16-byte bank
+            // groups), then the row's words from its offset; a key the loaders skipped (none, or
+            // past the CTA's last key) reads as zero words: scale 0
+            const uint4* win4 = reinterpret_cast<const uint4*>(smem + Ly::kRaw + st * Ly::kRawStage) + k * Ly::kChunks;
+            uint32_t kw[2][NW];
+#pragma unroll
+            for (int pl = 0; pl < 2; ++pl) {
+                uint32_t wv[Ly::kWindow];
+#pragma unroll
+                for (int c = 0; c < (int)Ly::kChunks; ++c) {
+                    const uint4 v = win4[pl * kPfKeys * Ly::kChunks + c];
+                    wv[4 * c] = v.x;
+                    wv[4 * c + 1] = v.y;
+                    wv[4 * c + 2] = v.z;
+                    wv[4 * c + 3] = v.w;
+                }
+#pragma unroll
+                for (int w = 0; w < NW + 1; ++w) wv[w] = (row_off & 2) ? wv[w + 2] : wv[w];
+#pragma unroll
+                for (int w = 0; w < NW; ++w) kw[pl][w] = (row_off & 1) ? wv[w + 1] : wv[w];
+            }
+            mbar_arrive(&raw_free[st]);
+            // K half, then V half, each once its tile is free (K: S of tile j - 2 done, V: its P.V)
+#pragma unroll
+            for (int pl = 0; pl < 2; ++pl) {
+                ok = !(j == 1 && pl == 0) || wait(q_ready, 0);        // the query staging sat on pair 1
+                if (ok && j >= kPfPairs) ok = wait(pl ? &v_free[kb] : &k_free[kb], (uint32_t)(j / kPfPairs - 1) & 1u);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                uint8_t* t = pl ? vtile(kb) : ktile(kb);
+                const uint32_t trow = pl ? vrow : (uint32_t)k;
+                const uint32_t zp = kw[pl][Gm::KW] & 15u;
+                const uint32_t zl = zp_lo_half(zp) * 0x10001u, zh = zp_hi_half(zp) * 0x10001u;
+#pragma unroll
+                for (int w = 0; w < Gm::KW; ++w) {
+                    // code - zp of dimensions 8w + (0, 4), (1, 5), (2, 6), (3, 7): the tile order
+                    uint32_t o[4];
+                    unpack_word(kw[pl][w], zl, zh, o);
+                    *reinterpret_cast<uint4*>(t + (uint32_t)(w / 8) * (kPfKeys * 128u) + swz128(trow, (uint32_t)(w % 8))) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                if (pl == 0) {
+                    sk[(j % kPfKRing) * kPfKeys + k] = __uint_as_float(kw[0][Gm::KW] & 0xFFFFFFF0u) * k0;
+                    const uint32_t nodead = __ballot_sync(0xffffffffu, kw[0][Gm::KW] == 0u);
+                    if (lane == 0)
+                        reinterpret_cast<uint32_t*>(smem + Ly::kDeadF)[(j % kPfKRing) * 4 + (warp - kPfSoftmaxWarps)] = nodead;
+                } else {
+                    const uint32_t vsw = kw[1][Gm::KW];
+                    sv[kb * kPfKeys + k] = __uint_as_float(vsw & 0xFFFFFFF0u);
+                    const uint32_t wmax = __reduce_max_sync(0xffffffffu, vsw);   // positive floats order like their bits
+                    if (lane == 0) eblkw[kb * 4 + (warp - kPfSoftmaxWarps)] = (wmax >> 23) & 0xFFu;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
+                mbar_arrive(pl ? &v_full[kb] : &k_full[j % kPfKRing]);
+            }
+            if (!ok) break;
+        }
+    } else if (warp > kPfMmaWarp) {
+        // ================================================================ loads of packed rows
+        // Loader warp l copies plane l (K or V) of each key tile into its staging buffer with 16-byte
+        // asynchronous copies of each row's aligned window: copy t of a lane moves chunk
+        // i = lane + 32 t of the tile's plane in (key, chunk) order, which is also the staging
+        // order.  Keys past the CTA's last key, or in a block the table does not name, are
+        // zero-filled (scale word 0: no key).  A window never leaves the cache: the cache starts on
+        // a 16-byte boundary (the entry point checks) and its size is a multiple of 16 bytes.
+        constexpr int C = Ly::kChunks;
+        constexpr int kCopies = kPfKeys * C / 32;
+        static_assert(kPfKeys * C % 32 == 0, "whole copies per lane");
+        const int pl = warp - kPfMmaWarp - 1;
         const int32_t* table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
-        constexpr int NW = Gm::KW + 1;                    // words of a row: codes, then the scale word
+        const int64_t tok_stride = (int64_t)H * Gm::RB, blk_stride = 2 * kBlockSize * tok_stride;
+        // the plane of block 0; a row's window is at blk * blk_stride + ((h RB + r tok_stride) & ~15)
+        const uint8_t* base = p.cache + (int64_t)pl * kBlockSize * tok_stride;
+        // copy t of this lane, the same for every tile: its key (bits 24..30) and its window chunk's
+        // byte offset from the block's plane (bits 0..23)
+        uint32_t cp[kCopies];
+#pragma unroll
+        for (int t = 0; t < kCopies; ++t) {
+            const int i = lane + 32 * t, key = i / C, c = i - key * C;
+            const uint32_t row = (uint32_t)h * (uint32_t)Gm::RB + (uint32_t)(key % kBlockSize) * (uint32_t)tok_stride;
+            cp[t] = ((uint32_t)key << 24) | ((row & ~15u) + 16u * (uint32_t)c);
+        }
+        // lane b < 8: the table entry of keys 16 b .. 16 b + 15 of tile j (-1: no such key); loaded
+        // one tile ahead and only checked when used, so that the load is never waited for
+        auto lookup = [&](int j) -> int {
+            return lane < kPfKeys / kBlockSize && j * kPfKeys + lane * kBlockSize <= cta_lim
+                       ? __ldg(table + j * (kPfKeys / kBlockSize) + lane)
+                       : -1;
+        };
+        int blk_next = nkt > 0 ? lookup(0) : -1;
+        bool ok = true;
+        for (int j = 0; j < nkt && ok; ++j) {
+            const int st = j % kPfRawStages;
+            if (j >= kPfRawStages) ok = wait(&raw_free[st], (uint32_t)(j / kPfRawStages - 1) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            int blkv = blk_next;
+            if (j + 1 < nkt) blk_next = lookup(j + 1);
+            if (blkv != -1 && (blkv < 0 || (int64_t)blkv >= p.num_blocks)) {   // a block the table does not name
+                if (pl == 0) count_status(p.status, 1);
+                blkv = -1;
+            }
+            const uint32_t dst = smem_u32(smem + Ly::kRaw + st * Ly::kRawStage) + (uint32_t)(pl * kPfKeys * C * 16);
+            const int key_lim = cta_lim - j * kPfKeys;    // last key of this tile the CTA sees
+#pragma unroll
+            for (int t = 0; t < kCopies; ++t) {
+                const int key = (int)(cp[t] >> 24);
+                const int blk = __shfl_sync(0xffffffffu, blkv, key / kBlockSize);
+                const bool live = blk >= 0 && key <= key_lim;
+                const uint8_t* src = base + (int64_t)(live ? blk : 0) * blk_stride + (cp[t] & 0xFFFFFFu);
+                cp_async16_zfill(dst + 16u * (uint32_t)(lane + 32 * t), src, live);
+            }
+            cp_async_arrive_noinc(&raw_full[st]);
+        }
+        cp_async_wait_all();   // no copy outlives the CTA
+    } else if (lane == 0) {
+        // ================================================================ the MMA issuer
+        // Issues whichever is ready next: S of tile js (its tile pair dequantised, its S buffer read
+        // by P.V of tile js - 2) or P.V of tile jp (its weights in tensor memory).  S runs at most
+        // two tiles ahead of P.V.
         constexpr uint32_t idS = idesc_f16(kPfKeys, 0), idPV = idesc_f16(D, 1);
-        uint32_t cur[2][NW], nxt[2][NW];
-        bool cur_ok = false, nxt_ok = false;
-        auto fetch = [&](int j, uint32_t (&w)[2][NW], bool& okk) {
-            const int key = j * kPfKeys + k;
-            okk = false;
-            if (key <= cta_lim) {
-                const int blk = __ldg(table + key / kBlockSize);
-                if (blk >= 0 && (int64_t)blk < p.num_blocks) {
-                    okk = true;
+        auto issue_s = [&](int j) {
+            const uint32_t sd = tmem + ((j & 1) ? Tm::kS1 : Tm::kS0);
+            const uint32_t kbase = smem_u32(ktile(j % kPfPairs));
 #pragma unroll
-                    for (int pl = 0; pl < 2; ++pl) {
-                        const uint32_t* row = reinterpret_cast<const uint32_t*>(
-                            p.cache + (((int64_t)blk * 2 + pl) * kBlockSize + key % kBlockSize) * H * Gm::RB +
-                            (int64_t)h * Gm::RB);
+            for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                        for (int i = 0; i < NW; ++i) w[pl][i] = __ldg(row + i);
-                    }
-                } else if (key % kBlockSize == 0) {
-                    count_status(p.status, 1);
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(
+                        kbase + (uint32_t)(kk / 4) * (kPfKeys * 128u) + (uint32_t)(kk % 4) * 32u, 16u, 1024u);
+                    mma_ts(sd, tmem + (half ? Tm::kQl : Tm::kQh) + 8u * kk, bd, idS, half > 0 || kk > 0);
                 }
             }
+            mma_commit(&s_full[j & 1]);
+            mma_commit(&k_free[j % kPfPairs]);
         };
-        // the MMA issue of P.V for tile t (issuer thread only)
-        auto issue_pv = [&](int t) -> bool {
-            const int b = t & 1;
-            if (!wait(&p_full[b], (uint32_t)(t >> 1) & 1u)) return false;
-            tc_fence_after();
-            const uint32_t pcol = tmem + (b ? Tm::kS1 : Tm::kS0);
-            const uint32_t vb = smem_u32(vtile(b));
+        auto issue_pv = [&](int t) {
+            const uint32_t pcol = tmem + ((t & 1) ? Tm::kS1 : Tm::kS0);
+            const uint32_t vb = smem_u32(vtile(t % kPfPairs));
 #pragma unroll
             for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-                const uint32_t a = pcol + (kk < 4 ? 8u * kk : 64u + 8u * (kk - 4));
+                const uint32_t a = pcol + 8u * kk;   // P of keys 16 kk .. 16 kk + 15 (in contraction order)
                 const uint64_t bd = smem_desc_sw128(vb + (uint32_t)kk * 16u * 128u, kPfKeys * 128u, 1024u);
                 mma_ts(tmem + Tm::kO, a, bd, idPV, t > 0 || kk > 0);
             }
-            mma_commit(&pv_done[b]);
-            return true;
+            mma_commit(&pv_done[t & 1]);
+            mma_commit(&v_free[t % kPfPairs]);
         };
-        if (nkt > 0) fetch(0, cur, cur_ok);
-        bool ok = true;
-        for (int j = 0; j < nkt && ok; ++j) {
-            const int b = j & 1;
-            if (j == 1) ok = wait(q_ready, 0);                           // the query staging sat on tiles 1
-            if (ok && j >= 2) ok = wait(&pv_done[b], (uint32_t)((j - 2) >> 1) & 1u);   // tiles b free
-            if (!__all_sync(0xffffffffu, ok)) break;
-            if (j + 1 < nkt) fetch(j + 1, nxt, nxt_ok);
-            uint8_t* kt = ktile(b);
-            uint8_t* vt = vtile(b);
-#pragma unroll
-            for (int pl = 0; pl < 2; ++pl) {
-                uint8_t* t = pl ? vt : kt;
-                const uint32_t zp = cur[pl][Gm::KW] & 15u;
-#pragma unroll
-                for (int w = 0; w < Gm::KW; ++w) {
-                    const uint4 v = cur_ok ? dequant_word(cur[pl][w], zp) : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(t + (uint32_t)(w / 8) * (kPfKeys * 128u) + swz128((uint32_t)k, (uint32_t)(w % 8))) = v;
+        bool ok = nkt == 0 || wait(q_ready, 0);
+        int js = 0, jp = 0;
+        uint64_t t0 = global_timer_ns();
+        uint32_t nap = 32;
+        while (ok && jp < nkt) {
+            bool did = false;
+            if (js < nkt && js < jp + 2 && mbar_test_wait(&k_full[js % kPfKRing], (uint32_t)(js / kPfKRing) & 1u) &&
+                (js < 2 || mbar_test_wait(&pv_done[js & 1], (uint32_t)((js - 2) >> 1) & 1u))) {
+                tc_fence_after();
+                issue_s(js++);
+                did = true;
+            }
+            if (jp < js && mbar_test_wait(&p_full[jp & 1], (uint32_t)(jp >> 1) & 1u)) {
+                tc_fence_after();
+                issue_pv(jp++);
+                did = true;
+            }
+            if (did) {
+                nap = 32;
+                t0 = global_timer_ns();
+            } else {
+                if (*abort_flag) {
+                    ok = false;
+                } else if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                    if (atomicExch(const_cast<int*>(abort_flag), 1) == 0) count_status(p.status, 3);
+                    ok = false;
+                } else {
+                    __nanosleep(nap);
+                    nap = nap < 128u ? 2u * nap : 128u;
                 }
             }
-            sk[b * kPfKeys + k] = cur_ok ? __uint_as_float(cur[0][Gm::KW] & 0xFFFFFFF0u) : 0.0f;
-            const uint32_t vsw = cur_ok ? cur[1][Gm::KW] : 0u;
-            sv[b * kPfKeys + k] = vsw;
-            const uint32_t wmax = __reduce_max_sync(0xffffffffu, vsw);   // positive floats order like their bits
-            if (lane == 0) eblkw[b * 4 + (warp - kPfSoftmaxWarps)] = (wmax >> 23) & 0xFFu;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
-            mbar_arrive(&kv_full[b]);
-#pragma unroll
-            for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-                for (int i = 0; i < NW; ++i) cur[pl][i] = nxt[pl][i];
-            cur_ok = nxt_ok;
-            if (issuer) {
-                // S of tile j (its S buffer was last read by P.V of tile j - 2, waited for above)
-                bool mok = (j > 0 || wait(q_ready, 0)) && wait(&kv_full[b], (uint32_t)(j >> 1) & 1u);
-                if (mok) {
-                    tc_fence_after();
-                    const uint32_t sd = tmem + (b ? Tm::kS1 : Tm::kS0);
-                    const uint32_t kb = smem_u32(kt);
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                        for (int kk = 0; kk < KSTEPS; ++kk) {
-                            const uint64_t bd = smem_desc_sw128(
-                                kb + (uint32_t)(kk / 4) * (kPfKeys * 128u) + (uint32_t)(kk % 4) * 32u, 16u, 1024u);
-                            mma_ts(sd, tmem + (half ? Tm::kQl : Tm::kQh) + 8u * kk, bd, idS, half > 0 || kk > 0);
-                        }
-                    }
-                    mma_commit(&s_full[b]);
-                    if (j >= 1) mok = issue_pv(j - 1);
-                }
-                ok = mok;
-            }
-            __syncwarp();
         }
-        if (issuer) {
-            if (ok && nkt > 0) issue_pv(nkt - 1);
-            // every MMA issued has completed before the CTA tears tensor memory down
-            mma_commit(flush);
-            (void)mbar_wait(flush, 0);
-        }
+        // every MMA issued has completed before the CTA tears tensor memory down
+        mma_commit(flush);
+        (void)mbar_wait(flush, 0);
     }
 
     tc_fence_before();
