@@ -16,16 +16,18 @@
 //                       exponent of the V scales) as fp16 written back over S, and their sum l'
 //                       carries the same 2^(127 - E), so out = O / l' without it
 //   O += P_w (V - zp)  tcgen05.mma, A = P_w from tensor memory, B = the values dequantised to
-//                       fp16 in shared memory (the same row layout as K, read MN-major); O stays
-//                       in tensor memory for the whole key range
+//                       fp16 in shared memory (K's row layout, rows in the key order the weights
+//                       are laid out in, read MN-major); O stays in tensor memory for the whole
+//                       key range
 // and un-rotates its rows at the end.
 //
-// Warp roles (416 threads): warps 0-7 own the rows (warp w reads tensor-memory lanes
-// 32 (w % 4) .. + 31, the lower or upper half of the key columns for w < 4 or w >= 4; warps w and
-// w + 4 exchange their halves' maxima), rotate the queries and run the softmax and the epilogue;
-// warps 8-11 load the packed codes of the next key tile (one key per thread, registers
-// double-buffered) and dequantise them into the shared-memory tile pair of its parity; warp 12
-// allocates tensor memory and one of its threads issues every MMA.
+// Warp roles (480 threads): warps 0-7 own the rows, rotate the queries and run the softmax and
+// the epilogue (warp w the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15, read in the 16-lane
+// tensor-memory layout, so that a row's four threads meet by shuffles); warps 13-14 stage the
+// packed K and V rows of the coming key tiles in shared memory with asynchronous copies, four
+// tiles ahead; warps 8-11 dequantise a staged tile (one key per thread) into the fp16 K and V
+// tiles of its parity, each half once the MMA that read it before is done; warp 12 allocates
+// tensor memory and one of its threads issues every MMA, S or P.V, whichever is ready.
 // Dimension order: a tile row holds each code word's eight dimensions in the order the nibble
 // unpacking yields them (8w + 0, 4, 1, 5, 2, 6, 3, 7), so the dequantisation needs no permutes;
 // Q' is stored in tensor memory in the same order (the contraction over dimensions does not care),
@@ -150,14 +152,12 @@ __device__ __forceinline__ void tmem_ld_q4(uint32_t taddr, uint32_t* r) {
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_st_q4(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
 // the same layout, one repetition (4 registers)
+__device__ __forceinline__ void tmem_ld_q1(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_st_q1(uint32_t taddr, const uint32_t* r) {
     asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
                  "r"(r[2]), "r"(r[3])
@@ -489,21 +489,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 }
                 tc_fence_after();
                 const float2 fa2 = make_float2(f_a, f_a), fb2 = make_float2(f_b, f_b);
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[16];
-                    tmem_ld_q4(trow + Tm::kO + c0, o);
+                // eight columns at a time: the scores stay in registers meanwhile
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 8) {
+                    uint32_t o[4];
+                    tmem_ld_q1(trow + Tm::kO + c0, o);
                     tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 oa = mul_f32x2(make_float2(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1])), fa2);
-                        const float2 ob = mul_f32x2(make_float2(__uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3])), fb2);
-                        o[4 * i] = __float_as_uint(oa.x);
-                        o[4 * i + 1] = __float_as_uint(oa.y);
-                        o[4 * i + 2] = __float_as_uint(ob.x);
-                        o[4 * i + 3] = __float_as_uint(ob.y);
-                    }
-                    tmem_st_q4(trow + Tm::kO + c0, o);
+                    const float2 oa = mul_f32x2(make_float2(__uint_as_float(o[0]), __uint_as_float(o[1])), fa2);
+                    const float2 ob = mul_f32x2(make_float2(__uint_as_float(o[2]), __uint_as_float(o[3])), fb2);
+                    o[0] = __float_as_uint(oa.x);
+                    o[1] = __float_as_uint(oa.y);
+                    o[2] = __float_as_uint(ob.x);
+                    o[3] = __float_as_uint(ob.y);
+                    tmem_st_q1(trow + Tm::kO + c0, o);
                 }
                 tmem_st_wait();
             }
