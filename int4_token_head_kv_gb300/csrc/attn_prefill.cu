@@ -35,6 +35,8 @@
 // Tensor memory (512 columns): Q' high, Q' low, two S buffers (S of tile j + 1 is computed while
 // the softmax of tile j runs), O.  Hand-offs go through mbarriers (tcgen05.commit for the MMAs);
 // every wait is bounded and a wait that gives up is counted and winds the CTA down.
+#include <cudaTypedefs.h>
+
 #include <type_traits>
 
 #include "attn_common.cuh"
@@ -59,19 +61,17 @@ constexpr uint32_t kPfLazyExp = 4;            // binades the V exponent referenc
 
 // Shared-memory layout (bytes from a 1024-aligned base).  A fp16 tile is 128 keys x D dims as
 // D/64 chunks of [128 rows x 128 B], 128-byte swizzled; kPfPairs K/V tile pairs (key tile j uses
-// pair j % kPfPairs): [K 0][V 0][K 1][V 1].  Before the first tile the query halves are staged from
-// pair 1 on (rows of D + 8 halves), and after the last the fp32 output rows over pairs 0-1 (rows
-// of D + 4 floats).  Then kPfRawStages staging buffers of packed rows as the cache holds them,
+// pair j % kPfPairs): [K 0][V 0][K 1][V 1].  Before the first tile pair 1 holds the CTA's query rows
+// (K 1, the same layout) and the rotation matrix (V 1), and after the last the fp32 output rows sit
+// over pairs 0-1 (rows of D + 4 floats).  Then kPfRawStages staging buffers of packed rows as the cache holds them,
 // [plane][128 keys][kWindow words] (key tile j in stage j % kPfRawStages): a row of D/8 + 1 words
 // arrives with the 16-byte-aligned window of cache bytes around it, at its own word offset 0..3.
 template <int D>
 struct PfLayout {
     static constexpr uint32_t kTile = (D / 64) * kPfKeys * 128;
-    static constexpr uint32_t kQStride = D + 8;                                   // halves per staged row
-    static constexpr uint32_t kQStage = 2u * kPfRows * kQStride * 2;              // high + low
     static constexpr uint32_t kOStride = D + 4;                                   // floats per staged row
-    static constexpr uint32_t kMisc = ((2 * kPfPairs * kTile > 2 * kTile + kQStage ? 2 * kPfPairs * kTile : 2 * kTile + kQStage) +
-                                       1023u) & ~1023u;
+    static constexpr uint32_t kMisc = 2 * kPfPairs * kTile;
+    static_assert((D / 64) * D * 128 <= kTile, "rotation matrix staging");
     static_assert(kPfRows * kOStride * 4 <= 4 * kTile, "output staging");
     static constexpr uint32_t kRowWords = D / 8 + 1;                              // packed row: codes + scale
     static constexpr uint32_t kChunks = (kRowWords + 3 + 3) / 4;                  // 16-byte chunks of a window
@@ -83,14 +83,11 @@ struct PfLayout {
     static constexpr uint32_t kDeadF = kSk + kPfKRing * kPfKeys * 4;  // [kring][4] u32: a dequantising warp saw a key with no row
     static constexpr uint32_t kSv = kDeadF + kPfKRing * 4 * 4;       // [pairs][128] f32 s'_V
     static constexpr uint32_t kEblk = kSv + kPfPairs * kPfKeys * 4;  // [pairs][4] per-warp max V exponent
-    static constexpr uint32_t kRowMax = kEblk + kPfPairs * 4 * 4;    // [2 tiles][2 halves][128] f32
-    static constexpr uint32_t kRowL = kRowMax + 2 * 2 * kPfRows * 4;  // [2][128] f32
-    static constexpr uint32_t kAlpha = kRowL + 2 * kPfRows * 4;      // [128] f32 2^-e of each row
-    static constexpr uint32_t kSigns = kAlpha + kPfRows * 4;         // [D] f32
+    static constexpr uint32_t kSigns = kEblk + kPfPairs * 4 * 4;     // [D] f32
     static constexpr uint32_t kBars = (kSigns + D * 4 + 7u) & ~7u;   // mbarriers
     // k_full[kring], k_free[pairs], v_full[pairs], v_free[pairs], pv_done[2], s_full[2], p_full[2], q_ready,
-    // flush, q_stage, epi[2], pairs[4][2], raw_full[stages], raw_free[stages]
-    static constexpr int kNumBars = kPfKRing + 3 * kPfPairs + 2 + 2 + 2 + 1 + 1 + 1 + 2 + 8 + 2 * kPfRawStages;
+    // flush, q_tma, rot_in, rot_done, epi, raw_full[stages], raw_free[stages]
+    static constexpr int kNumBars = kPfKRing + 3 * kPfPairs + 2 + 2 + 2 + 1 + 1 + 3 + 1 + 2 * kPfRawStages;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kFlags = kTmemSlot + 4;
     static constexpr uint32_t kBytes = kFlags + 4 + 1024;            // + alignment slack
@@ -113,6 +110,35 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t n, uint32_t b_mn) {
     return (1u << 4) | (b_mn << 16) | ((n >> 3) << 17) | ((uint32_t)(kPfRows >> 4) << 24);
 }
+// the same with bf16 A and B
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n, uint32_t b_mn) {
+    return idesc_f16(n, b_mn) | (1u << 7) | (1u << 10);
+}
+
+// A and B both from shared memory (descriptors), D in tensor memory
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)acc)
+        : "memory");
+}
+
+// Tiled 3-D tensor copy global -> shared: the tensor map's box at (x, y, z), completion signalled on
+// the mbarrier (transaction bytes).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// position in a group of 16 contraction slots that the 16-lane tensor-memory layout gives the
+// value of column p (a thread's column pair 8i + 2t, + 1 is stored as word 8 (i / 2) + 2t + i % 2)
+__host__ __device__ constexpr int slot_of_column(int p) {
+    return (p & ~15) + 4 * ((p >> 1) & 3) + 2 * ((p >> 3) & 1) + (p & 1);
+}
 
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, bool acc) {
     asm volatile(
@@ -131,16 +157,6 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 
 // 16 lanes x 256 bits, four times along the columns (16 registers): thread i = 4 g + t gets, for
 // repetition c, r[4c] = (lane g, column 8c + 2t), r[4c + 1] = (g, 8c + 2t + 1), r[4c + 2] = (g + 8,
@@ -178,20 +194,13 @@ __device__ __forceinline__ void tmem_ld_q8(uint32_t taddr, uint32_t* r) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a [rows x 128 B] block with the 128-byte
 // swizzle the tensor-core descriptors expect: the chunk index is XOR-ed with r mod 8.
 __device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
 template <int D, typename QT, typename OT>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap qmap) {
     using Gm = Geo<D>;
     using Ly = PfLayout<D>;
     using Tm = PfTmem<D>;
@@ -228,9 +237,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     float* sk = reinterpret_cast<float*>(smem + Ly::kSk);
     float* sv = reinterpret_cast<float*>(smem + Ly::kSv);
     uint32_t* eblkw = reinterpret_cast<uint32_t*>(smem + Ly::kEblk);
-    float* rowmax = reinterpret_cast<float*>(smem + Ly::kRowMax);
-    float* rowl = reinterpret_cast<float*>(smem + Ly::kRowL);
-    float* alpha = reinterpret_cast<float*>(smem + Ly::kAlpha);
     float* sgn = reinterpret_cast<float*>(smem + Ly::kSigns);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBars);
     // The K and V halves of a tile pair live apart: K tile j is free once S of tile j is done, V tile
@@ -246,10 +252,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     uint64_t* p_full = s_full + 2;              // [2] P of the tile in tensor memory (256 arrivals)
     uint64_t* q_ready = p_full + 2;             // queries in tensor memory, staging free (256 arrivals)
     uint64_t* flush = q_ready + 1;              // the MMA thread's last commit (teardown)
-    // barriers among the 256 row threads (bounded waits, unlike a hardware named barrier): the query
-    // staging, and the epilogue's staged output rows
-    uint64_t* q_stage = flush + 1;
-    uint64_t* epi = q_stage + 1;
+    uint64_t* q_tma = flush + 1;                // the CTA's query rows in shared memory (bytes)
+    uint64_t* rot_in = q_tma + 1;               // the rotation matrix in shared memory (256 arrivals)
+    uint64_t* rot_done = rot_in + 1;            // the rotated queries in tensor memory (commit)
+    // the 256 row threads meet (a bounded wait, unlike a hardware named barrier) once the output
+    // rows are staged
+    uint64_t* epi = rot_done + 1;
     uint64_t* raw_full = epi + 1;            // [stages] packed rows of a key tile landed (64 lanes)
     uint64_t* raw_free = raw_full + kPfRawStages;   // [stages] that stage converted (128 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
@@ -269,7 +277,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         }
         mbar_init(q_ready, kPfSoftmaxThreads);
         mbar_init(flush, 1);
-        mbar_init(q_stage, kPfSoftmaxThreads);
+        mbar_init(q_tma, 1);
+        mbar_init(rot_in, kPfSoftmaxThreads);
+        mbar_init(rot_done, 1);
         mbar_init(epi, kPfSoftmaxThreads);
         for (int i = 0; i < kPfRawStages; ++i) {
             mbar_init(&raw_full[i], kPfLoadWarps * 32);
@@ -307,96 +317,91 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
     if (warp < kPfSoftmaxWarps) {
         // ================================================================ rows: softmax + epilogue
-        const int r = 32 * (warp & 3) + lane, hf = warp >> 2;
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        __half* qs_hi = reinterpret_cast<__half*>(ktile(1));
-        __half* qs_lo = qs_hi + kPfRows * Ly::kQStride;
-        // ---- rotate the queries, lanes across dimensions.  A warp loads a batch of rows before it
-        // transforms any (one memory latency per batch), then rotates four at a time (interleaved
-        // butterflies): v = H_d (D q), a power-of-two prescale 2^e bringing max|v| into
-        // [2^14, 2^15), and fp16 high + low halves (qh + ql carries about 22 bits: a plain fp16 copy
-        // turns large keys into logit errors a heavy-tailed cache shows).
-        // Warp w rotates rows 16 w .. 16 w + 15 in two batches of eight.
-        auto rotate_rows = [&](int first, auto nrows_c) {
-            constexpr int NR = decltype(nrows_c)::value;
-            float x[NR][D / 32];
-#pragma unroll
-            for (int i = 0; i < NR; ++i) {
-                const int R = first + i;
-                const int qt = qt0 + R / G, gg = R % G;
-                const bool live = nkt > 0 && qt < qlen;
-                const int64_t qoff = ((int64_t)(q0 + (live ? qt : 0)) * Hq + h * G + gg) * D;
-#pragma unroll
-                for (int k = 0; k < D / 32; ++k)
-                    x[i][k] = live ? load_elem<QT>(p.q, qoff + lane + 32 * k) * sgn[lane + 32 * k] : 0.0f;
-            }
-#pragma unroll
-            for (int i0 = 0; i0 < NR; i0 += 4) {
-                float (&xb)[4][D / 32] = *reinterpret_cast<float(*)[4][D / 32]>(&x[i0][0]);
-                warp_fwht_batch<D, 4>(xb);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int R = first + i0 + v;
-                    float mx = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < D / 32; ++k) mx = fmaxf(mx, fabsf(xb[v][k]));
-                    const int e = prescale_exponent(warp_max(mx));
-                    const float sc = exp2i(e);
-#pragma unroll
-                    for (int k = 0; k < D / 32; ++k) {
-                        const float y = xb[v][k] * sc;
-                        const __half hi = __float2half_rn(y);
-                        qs_hi[R * Ly::kQStride + lane + 32 * k] = hi;
-                        qs_lo[R * Ly::kQStride + lane + 32 * k] = __float2half_rn(y - __half2float(hi));
-                    }
-                    if (lane == 0) alpha[R] = exp2i(-e);   // rows with no query (zeros) give 2^0
-                }
-            }
-        };
-        {
-            constexpr int RPW = kPfRows / kPfSoftmaxWarps;
-            rotate_rows(warp * RPW, std::integral_constant<int, 8>{});
-            rotate_rows(warp * RPW + 8, std::integral_constant<int, 8>{});
-        }
-        bool ok = rows_meet(q_stage, 0);
-        // ---- this thread's half of its row into tensor memory (high, then low halves), each group
-        // of eight dimensions in the tile order 0, 4, 1, 5, 2, 6, 3, 7
-        if (ok) {
-            constexpr int kWords = D / 4;   // 32-bit words of a half row
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint4* src = reinterpret_cast<const uint4*>((part ? qs_lo : qs_hi) + r * Ly::kQStride) +
-                                   hf * (kWords / 4);
-                uint32_t w[kWords];
-#pragma unroll
-                for (int j = 0; j < kWords; j += 4) {
-                    const uint4 v = src[j / 4];   // halves d0..d7 of one group
-                    w[j] = prmt(v.x, v.z, 0x5410u);       // (d0, d4)
-                    w[j + 1] = prmt(v.x, v.z, 0x7632u);   // (d1, d5)
-                    w[j + 2] = prmt(v.y, v.w, 0x5410u);   // (d2, d6)
-                    w[j + 3] = prmt(v.y, v.w, 0x7632u);   // (d3, d7)
-                }
-                const uint32_t ta = tmem + lane_base + (part ? Tm::kQl : Tm::kQh) + hf * kWords;
-                if constexpr (kWords == 32) {
-                    tmem_st32(ta, w);
-                } else {
-#pragma unroll
-                    for (int c0 = 0; c0 < kWords; c0 += 16) tmem_st16(ta + c0, w + c0);
-                }
-            }
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(q_ready);
-        // ---- the key tiles.  Warp w owns the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15 in the 16-lane
-        // tensor-memory layout: thread (g, t) = (lane / 4, lane % 4) holds rows ra = rbase + g and
-        // rb = ra + 8 and, of every group of 8 key columns, columns 2t and 2t + 1; a row's maximum
-        // and sum meet over its four threads by two shuffles.
+        // Warp w owns the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15 in the 16-lane tensor-memory
+        // layout: thread (g, t) = (lane / 4, lane % 4) holds rows ra = rbase + g and rb = ra + 8 and,
+        // of every group of 8 columns, columns 2t and 2t + 1; a row's maximum and sum meet over its
+        // four threads by two shuffles.
         const int rbase = 32 * (warp & 3) + 16 * (warp >> 2);
         const int t4 = lane & 3;
         const int ra = rbase + (lane >> 2), rb = ra + 8;
         const uint32_t trow = tmem + ((uint32_t)rbase << 16);
-        const float rs_a = alpha[ra], rs_b = alpha[rb];   // 2^-e of each row's query prescale
+        // ---- the rotation v = H_d (D q) as a matrix product on the tensor cores: the query rows
+        // (loaded by the MMA thread) times B[p][k] = sign_k (-1)^popcount(n(p) & k), where row p of
+        // B is the dimension n(p) whose value column p must hold for the query halves below to land
+        // in the tiles' dimension order.  The entries are +-1, exact in the query type.
+        {
+            constexpr int kRowChunks = D / 8;   // 16-byte chunks of a B row
+            uint8_t* qb = vtile(1);
+            const uint32_t one = std::is_same<QT, __nv_bfloat16>::value ? 0x3F80u : 0x3C00u;
+            for (int ci = threadIdx.x; ci < D * kRowChunks; ci += kPfSoftmaxThreads) {
+                const int prow = ci / kRowChunks, k8 = ci % kRowChunks;
+                const int slot = slot_of_column(prow);
+                const int n = (slot & ~7) + ((slot & 7) >> 1) + 4 * (slot & 1);   // tile order 0, 4, 1, 5, ...
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 8 * k8 + 2 * e;
+                    const uint32_t lo = one | ((((uint32_t)__popc(n & k) & 1u) ^ (sgn[k] < 0.0f ? 1u : 0u)) << 15);
+                    const uint32_t hi = one | ((((uint32_t)__popc(n & (k + 1)) & 1u) ^ (sgn[k + 1] < 0.0f ? 1u : 0u)) << 15);
+                    w[e] = lo | (hi << 16);
+                }
+                *reinterpret_cast<uint4*>(qb + (uint32_t)(k8 / 8) * (uint32_t)(D * 128) + swz128((uint32_t)prow, (uint32_t)(k8 % 8))) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
+            mbar_arrive(rot_in);
+        }
+        // ---- a power-of-two prescale 2^e bringing the row's max |v| into [2^14, 2^15), then fp16
+        // high + low halves (qh + ql carries about 22 bits: a plain fp16 copy turns large keys into
+        // logit errors a heavy-tailed cache shows) into tensor memory, where S's MMAs read them
+        float rs_a = 1.0f, rs_b = 1.0f;   // 2^-e of each row
+        bool ok = wait(rot_done, 0);
+        if (__all_sync(0xffffffffu, ok)) {
+            tc_fence_after();
+            float v[D / 2];   // v[4i], v[4i + 1]: row a, columns 8i + 2t, + 1; v[4i + 2], v[4i + 3]: row b
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 64) tmem_ld_q8(trow + Tm::kS0 + c0, reinterpret_cast<uint32_t*>(v) + c0 / 2);
+            tmem_ld_wait();
+            float mxa = 0.0f, mxb = 0.0f;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                mxa = fmaxf(mxa, fmaxf(fabsf(v[4 * i]), fabsf(v[4 * i + 1])));
+                mxb = fmaxf(mxb, fmaxf(fabsf(v[4 * i + 2]), fabsf(v[4 * i + 3])));
+            }
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+            const int ea = prescale_exponent(mxa), eb = prescale_exponent(mxb);   // rows of zeros: 2^0
+            const float sca = exp2i(ea), scb = exp2i(eb);
+            rs_a = exp2i(-ea);
+            rs_b = exp2i(-eb);
+#pragma unroll
+            for (int q = 0; q < D / 16; ++q) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 2 * q + e;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const float sc = rr ? scb : sca;
+                        const float y0 = v[4 * i + 2 * rr] * sc, y1 = v[4 * i + 2 * rr + 1] * sc;
+                        const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
+                        const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
+                        hw[2 * rr + e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                        lw[2 * rr + e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+                    }
+                }
+                tmem_st_q1(trow + Tm::kQh + 8 * q, hw);
+                tmem_st_q1(trow + Tm::kQl + 8 * q, lw);
+            }
+            tmem_st_wait();
+        } else {
+            ok = false;
+        }
+        tc_fence_before();
+        mbar_arrive(q_ready);
+        // ---- the key tiles
         const int qta = qt0 + ra / G, qtb = qt0 + rb / G;
         const int pos_a = qta < qlen ? pos0 + qta : -1, pos_b = qtb < qlen ? pos0 + qtb : -1;   // last visible key
         float m_a = kNegBig, m_b = kNegBig;     // reference maxima (log2 units)
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // the V tile row of this key: the weights of S columns 16 q + 8 e + 2 t + b sit at
         // contraction position 16 q + 4 t + 2 e + b (the 16-lane tensor-memory layout they are
         // written in)
-        const uint32_t vrow = (uint32_t)((k & ~15) + 4 * ((k >> 1) & 3) + 2 * ((k >> 3) & 1) + (k & 1));
+        const uint32_t vrow = (uint32_t)slot_of_column(k);
         for (int j = 0; j < nkt; ++j) {
             const int kb = j % kPfPairs, st = j % kPfRawStages;
             bool ok = wait(&raw_full[st], (uint32_t)(j / kPfRawStages) & 1u);
@@ -716,6 +721,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // by P.V of tile js - 2) or P.V of tile jp (its weights in tensor memory).  S runs at most
         // two tiles ahead of P.V.
         constexpr uint32_t idS = idesc_f16(kPfKeys, 0), idPV = idesc_f16(D, 1);
+        // the CTA's query rows (token qt0 + R / G, head h G + R % G for row R) into pair 1's K tile,
+        // then their rotation into S buffer 0
+        {
+            mbar_arrive_expect_tx(q_tma, Ly::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(ktile(1) + c * (kPfRows * 128), &qmap, 64 * c, h * G, q0 + qt0, q_tma);
+            bool rok = wait(q_tma, 0) && wait(rot_in, 0);
+            if (rok) {
+                tc_fence_after();
+                constexpr uint32_t idR = std::is_same<QT, __nv_bfloat16>::value ? idesc_bf16(D, 0) : idesc_f16(D, 0);
+                const uint32_t qa = smem_u32(ktile(1)), qb = smem_u32(vtile(1));
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(qa + (uint32_t)(kk / 4) * (kPfRows * 128u) + (uint32_t)(kk % 4) * 32u, 16u, 1024u);
+                    const uint64_t bd = smem_desc_sw128(qb + (uint32_t)(kk / 4) * (uint32_t)(D * 128) + (uint32_t)(kk % 4) * 32u, 16u, 1024u);
+                    mma_ss(tmem + Tm::kS0, ad, bd, idR, kk > 0);
+                }
+                mma_commit(rot_done);
+            }
+        }
         auto issue_s = [&](int j) {
             const uint32_t sd = tmem + ((j & 1) ? Tm::kS1 : Tm::kS0);
             const uint32_t kbase = smem_u32(ktile(j % kPfPairs));
@@ -787,14 +813,51 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::atomic<void*> fn{nullptr};
+    void* f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || f == nullptr)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// The queries as a 3-D tensor [token][q head][D] of QT, read in boxes of [128 / G tokens][G heads]
+// [64 dims] with the 128-byte swizzle the MMA descriptors expect.  Tokens past the last read as 0.
+template <int D, typename QT>
+cudaError_t query_map(const AttnParams& p, CUtensorMap* map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.num_q_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * sizeof(QT), (cuuint64_t)p.Hq * D * sizeof(QT)};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)p.G, (cuuint32_t)(kPfRows / p.G)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = enc(map,
+                           std::is_same<QT, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           3, const_cast<void*>(static_cast<const void*>(p.q)), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D, typename QT, typename OT>
 cudaError_t launch_prefill_t(const AttnParams& p, int max_query_len, cudaStream_t stream) {
     const size_t smem = PfLayout<D>::kBytes;
     cudaError_t err = opt_in_smem<prefill_kernel<D, QT, OT>>(smem);
     if (err != cudaSuccess) return err;
+    if (p.num_q_tokens <= 0 || kPfRows % p.G != 0) return cudaErrorInvalidValue;
+    CUtensorMap qmap;
+    err = query_map<D, QT>(p, &qmap);
+    if (err != cudaSuccess) return err;
     const int BQ = kPfRows / p.G;
     dim3 grid((unsigned)(((max_query_len + BQ - 1) / BQ) * p.H), 1, p.num_seqs);
-    prefill_kernel<D, QT, OT><<<grid, kPfThreads, smem, stream>>>(p);
+    prefill_kernel<D, QT, OT><<<grid, kPfThreads, smem, stream>>>(p, qmap);
     return cudaGetLastError();
 }
 
