@@ -719,7 +719,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // ================================================================ the MMA issuer
         // Issues whichever is ready next: S of tile js (its tile pair dequantised, its S buffer read
         // by P.V of tile js - 2) or P.V of tile jp (its weights in tensor memory).  S runs at most
-        // two tiles ahead of P.V.
+        // two tiles ahead of P.V.  The issuer polls without sleeping: a suspended issuer would add
+        // its wake-up to every hand-off on the critical path.
         constexpr uint32_t idS = idesc_f16(kPfKeys, 0), idPV = idesc_f16(D, 1);
         // the CTA's query rows (token qt0 + R / G, head h G + R % G for row R) into pair 1's K tile,
         // then their rotation into S buffer 0
@@ -772,7 +773,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         bool ok = nkt == 0 || wait(q_ready, 0);
         int js = 0, jp = 0;
         uint64_t t0 = global_timer_ns();
-        uint32_t nap = 32;
         while (ok && jp < nkt) {
             bool did = false;
             if (js < nkt && js < jp + 2 && mbar_test_wait(&k_full[js % kPfKRing], (uint32_t)(js / kPfKRing) & 1u) &&
@@ -787,7 +787,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 did = true;
             }
             if (did) {
-                nap = 32;
                 t0 = global_timer_ns();
             } else {
                 if (*abort_flag) {
@@ -795,9 +794,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 } else if (global_timer_ns() - t0 > kWaitTimeoutNs) {
                     if (atomicExch(const_cast<int*>(abort_flag), 1) == 0) count_status(p.status, 3);
                     ok = false;
-                } else {
-                    __nanosleep(nap);
-                    nap = nap < 128u ? 2u * nap : 128u;
                 }
             }
         }
