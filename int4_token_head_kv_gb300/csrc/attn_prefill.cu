@@ -84,7 +84,8 @@ struct PfLayout {
     static constexpr uint32_t kSv = kDeadF + kPfKRing * 4 * 4;       // [pairs][128] f32 s'_V
     static constexpr uint32_t kEblk = kSv + kPfPairs * kPfKeys * 4;  // [pairs][4] per-warp max V exponent
     static constexpr uint32_t kSigns = kEblk + kPfPairs * 4 * 4;     // [D] f32
-    static constexpr uint32_t kBars = (kSigns + D * 4 + 7u) & ~7u;   // mbarriers
+    static constexpr uint32_t kSignBits = kSigns + D * 4;            // [D / 32] u32: bit j of word i: sign 32 i + j < 0
+    static constexpr uint32_t kBars = (kSignBits + D / 8 + 7u) & ~7u;   // mbarriers
     // k_full[kring], k_free[pairs], v_full[pairs], v_free[pairs], pv_done[2], s_full[2], p_full[2], q_ready,
     // flush, q_tma, rot_in, rot_done, epi, raw_full[stages], raw_free[stages]
     static constexpr int kNumBars = kPfKRing + 3 * kPfPairs + 2 + 2 + 2 + 1 + 1 + 3 + 1 + 2 * kPfRawStages;
@@ -136,6 +137,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 
 // position in a group of 16 contraction slots that the 16-lane tensor-memory layout gives the
 // value of column p (a thread's column pair 8i + 2t, + 1 is stored as word 8 (i / 2) + 2t + i % 2)
+// four words of fp16 (one = 0x3C00) or bf16 (one = 0x3F80) +-1: element j is negative where bit j of
+// neg8 is set (element 2e in the low half of word e)
+__device__ __forceinline__ void pm1_words(uint32_t neg8, uint32_t one, uint32_t (&w)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        w[e] = (one * 0x10001u) | (((neg8 >> (2 * e)) & 1u) << 15) | (((neg8 >> (2 * e + 1)) & 1u) << 31);
+}
+// the dimension a tile column holds: each group of 8 in the order 0, 4, 1, 5, 2, 6, 3, 7
+__host__ __device__ constexpr int dim_of_column(int c) { return (c & ~7) + ((c & 7) >> 1) + 4 * (c & 1); }
 __host__ __device__ constexpr int slot_of_column(int p) {
     return (p & ~15) + 4 * ((p >> 1) & 3) + 2 * ((p >> 3) & 1) + (p & 1);
 }
@@ -288,7 +298,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
+    uint32_t* signbits = reinterpret_cast<uint32_t*>(smem + Ly::kSignBits);
+    if (threadIdx.x < D) {   // whole warps (D is a multiple of 32)
+        const bool neg = p.signs[threadIdx.x] < 0.0f;
+        sgn[threadIdx.x] = neg ? -1.0f : 1.0f;
+        const uint32_t m = __ballot_sync(0xffffffffu, neg);
+        if (lane == 0) signbits[warp] = m;
+    }
     if (warp == kPfMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "n"(kTmemCols)
@@ -330,21 +346,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // B is the dimension n(p) whose value column p must hold for the query halves below to land
         // in the tiles' dimension order.  The entries are +-1, exact in the query type.
         {
-            constexpr int kRowChunks = D / 8;   // 16-byte chunks of a B row
+            // row p = tid / (256 / D) of B, its chunks (8 inputs k each) split over 256 / D threads;
+            // (-1)^popcount(n & k) = (-1)^popcount(n & 8 k8) (-1)^popcount(n & k % 8)
+            constexpr int kRowChunks = D / 8, kThreadsPerRow = kPfSoftmaxThreads / D, kChunksPerThread = kRowChunks / kThreadsPerRow;
             uint8_t* qb = vtile(1);
             const uint32_t one = std::is_same<QT, __nv_bfloat16>::value ? 0x3F80u : 0x3C00u;
-            for (int ci = threadIdx.x; ci < D * kRowChunks; ci += kPfSoftmaxThreads) {
-                const int prow = ci / kRowChunks, k8 = ci % kRowChunks;
-                const int slot = slot_of_column(prow);
-                const int n = (slot & ~7) + ((slot & 7) >> 1) + 4 * (slot & 1);   // tile order 0, 4, 1, 5, ...
-                uint32_t w[4];
+            const int prow = threadIdx.x / kThreadsPerRow;
+            const int n = dim_of_column(slot_of_column(prow));
+            uint32_t par8 = 0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int k = 8 * k8 + 2 * e;
-                    const uint32_t lo = one | ((((uint32_t)__popc(n & k) & 1u) ^ (sgn[k] < 0.0f ? 1u : 0u)) << 15);
-                    const uint32_t hi = one | ((((uint32_t)__popc(n & (k + 1)) & 1u) ^ (sgn[k + 1] < 0.0f ? 1u : 0u)) << 15);
-                    w[e] = lo | (hi << 16);
-                }
+            for (int j = 0; j < 8; ++j) par8 |= ((uint32_t)__popc(n & j) & 1u) << j;
+#pragma unroll
+            for (int it = 0; it < kChunksPerThread; ++it) {
+                const int k8 = (threadIdx.x % kThreadsPerRow) * kChunksPerThread + it;
+                const uint32_t sb = (signbits[k8 / 4] >> (8 * (k8 % 4))) & 0xFFu;
+                const uint32_t neg = par8 ^ sb ^ ((__popc(n & (8 * k8)) & 1) ? 0xFFu : 0u);
+                uint32_t w[4];
+                pm1_words(neg, one, w);
                 *reinterpret_cast<uint4*>(qb + (uint32_t)(k8 / 8) * (uint32_t)(D * 128) + swz128((uint32_t)prow, (uint32_t)(k8 % 8))) =
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
