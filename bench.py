@@ -387,6 +387,7 @@ def _gpu_arm(args):
         result["write"] = _write_bench(torch, kv, workloads, dev, args, hbm, kind)
         result["mixed_prefill_decode"] = _mixed_bench(torch, kv, workloads, dev, args, hbm, bf16, kind)
         result["int8_comparator"] = _int8_write_bench(torch, kv, workloads, dev, args, hbm)
+        result["int8_comparator"]["decode"] = _int8_decode_bench(torch, kv, workloads, dev, args, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = _cpu_baseline(args)
     if world > 1:
@@ -434,15 +435,24 @@ def _write_bench(torch, kv, workloads, dev, args, hbm, kind):
                               bytes_per_launch=nbytes, avg_ms=round(ms, 5))}
 
 
-def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=None):
+def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=None, bits=4):
     """Write every token of ``wl`` (untimed), then time ``reps`` back-to-back attention calls captured in
     one CUDA graph, over the whole batch or over the sequences ``sub`` (same cache).  Returns ms per call
-    and the segment length."""
+    and the segment length.  bits=8: the INT8 comparator's cache and decode call instead."""
     H, d = wl.num_kv_heads, wl.head_size
     signs = torch.from_numpy(wl.signs).to(dev)
-    cache = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
     import numpy as np
-    _write_history(torch, kv, wl, dev, signs, cache, np.arange(wl.key.shape[0]))
+    if bits == 4:
+        cache = torch.zeros(kv.kv_int4_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+        _write_history(torch, kv, wl, dev, signs, cache, np.arange(wl.key.shape[0]))
+        row_bytes = kv.kv_int4_row_bytes(d)
+    else:
+        cache = torch.zeros(kv.kv_int8_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+        step = 1 << 18
+        for r0 in range(0, wl.key.shape[0], step):
+            kv.kv_int8_write(wl.key[r0:r0 + step].to(dev), wl.value[r0:r0 + step].to(dev),
+                             torch.from_numpy(wl.slot_mapping[r0:r0 + step]).to(dev), cache)
+        row_bytes = kv.kv_int8_row_bytes(d)
     results = {}
     for name, seqs in (sub or {"all": None}).items():
         if seqs is None:
@@ -460,8 +470,12 @@ def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=Non
         out = torch.empty_like(q)
 
         def call():
-            kv.kv_int4_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, signs, max_query_len=max_q,
-                                       max_seq_len=max_len, out=out, segment_len=seg, workspace=ws)
+            if bits == 4:
+                kv.kv_int4_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, signs, max_query_len=max_q,
+                                           max_seq_len=max_len, out=out, segment_len=seg, workspace=ws)
+            else:
+                kv.kv_int8_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, max_query_len=max_q,
+                                           max_seq_len=max_len, out=out, segment_len=seg, workspace=ws)
         for _ in range(3):
             call()
         torch.cuda.synchronize()
@@ -471,7 +485,7 @@ def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=Non
                 call()
         g.replay()
         ms = _timed(torch, torch.cuda.current_stream(), lambda i: g.replay(), 1) / reps
-        kvb = int(lens_np.sum()) * 2 * H * kv.kv_int4_row_bytes(d) + 2 * q.numel() * q.element_size()
+        kvb = int(lens_np.sum()) * 2 * H * row_bytes + 2 * q.numel() * q.element_size()
         results[name] = {"ms": ms, "seg": seg, "bytes": kvb, "seqs": seqs, "qlens": qlens, "lens": lens_np}
         del g, ws, out, q
     del cache
@@ -530,6 +544,28 @@ def _int8_write_bench(torch, kv, workloads, dev, args, hbm):
                       "frac": round(gbs / hbm, 4), "ms_per_call": round(ms, 5), "bytes_per_call": nbytes},
             "cache_bytes_per_token": 2 * H * kv.kv_int8_row_bytes(d),
             "int4_cache_bytes_per_token": 2 * H * kv.kv_int4_row_bytes(d)}
+
+
+def _int8_decode_bench(torch, kv, workloads, dev, args, hbm):
+    """INT4 and INT8 decode attention on the long-context workload, timed the same way (one CUDA graph
+    of back-to-back calls over a cache larger than L2) on the same box."""
+    wl = workloads.long_context_decode(seed=args.seed)
+    reps = 50
+    res = {}
+    for bits in (4, 8):
+        r = _attention_calls(torch, kv, wl, dev, reps=reps, segment_len=args.segment_len, bits=bits)["all"]
+        rb = kv.kv_int4_row_bytes(wl.head_size) if bits == 4 else kv.kv_int8_row_bytes(wl.head_size)
+        gbs = _gbs(r["bytes"], r["ms"])
+        res[f"int{bits}"] = {"ms_per_call": round(r["ms"], 5), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                             "decode_tokens_per_s": round(len(wl.seq_lens) / (r["ms"] * 1e-3), 1),
+                             "context_tokens_per_s": round(float(wl.seq_lens.sum()) / (r["ms"] * 1e-3), 1),
+                             "kv_bytes_per_token_per_layer": 2 * wl.num_kv_heads * rb, "segment_len": r["seg"]}
+    res["workload"] = ("long_context_decode: 8 seqs x 131072 tokens, 64 q / 8 kv heads, head 128; one decode "
+                       "attention call per step (no write), graph-replayed %d times back to back" % reps)
+    res["int8_over_int4_time"] = round(res["int8"]["ms_per_call"] / res["int4"]["ms_per_call"], 3)
+    res["int4_kv_bytes_saving_vs_int8"] = round(1 - res["int4"]["kv_bytes_per_token_per_layer"] /
+                                                res["int8"]["kv_bytes_per_token_per_layer"], 4)
+    return res
 
 
 # ------------------------------------------------------------------------------- CPU oracle

@@ -1,12 +1,13 @@
 /*
  * kv_int4.h -- C ABI of the INT4 per-(token, head) KV-cache library for NVIDIA GB300 (sm_103a).
  *
- * Two operations, both asynchronous on the caller's CUDA stream:
+ * Two operations, both asynchronous on the caller's CUDA stream, and the INT8 comparator's pair:
  *
  *   kv_int4_write            rotate, quantise and pack new K/V head vectors into a paged cache;
- *   kv_int8_write            the INT8 per-(token, head) comparator's cache write;
  *   kv_int4_paged_attention  causal attention of queries over that cache (decode, split-KV
- *                            segments, chunked prefill).
+ *                            segments, chunked prefill);
+ *   kv_int8_write            the INT8 per-(token, head) comparator's cache write;
+ *   kv_int8_paged_attention  decode attention over the INT8 comparator's cache.
  *
  * The caller owns every buffer.  The library never allocates device or host memory: the
  * attention's split-KV partials live in a caller-provided workspace whose size
@@ -192,6 +193,32 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
                                        const float* rht_signs, int32_t segment_len, void* out,
                                        kv_int4_dtype out_dtype, void* workspace,
                                        size_t workspace_bytes, kv_int4_stream_t stream);
+
+/*
+ * kv_int8_paged_attention -- decode attention over the INT8 comparator's cache (as written by
+ * kv_int8_write), the read side of the comparison the pages make between the INT4 mode and INT8
+ * per-(token, head) quantisation ("PR #40835 report", summary; "tests/quantization/
+ * test_per_token_kv_cache.py", INT8_CONFIG and _quantize_per_token_head_ref).
+ *
+ * Every sequence must have exactly one query token (max_query_len 1; a larger value returns
+ * KV_INT4_EUNSUPPORTED and launches nothing).  With x_K, x_V the cached rows decoded as code * s
+ * (no rotation, no zero-point), out = softmax(softmax_scale * q . x_K) x_V.  The computation is the
+ * decode path of kv_int4_paged_attention with INT8 rows: the same split-KV segments, the same
+ * segment-length rule and workspace size (kv_int4_attention_workspace_bytes with these arguments),
+ * the same partials and combine, the query and the output not rotated.  Arguments, alignment,
+ * supported sizes, clamping and error behaviour as kv_int4_paged_attention, without rht_signs.
+ */
+kv_int4_status kv_int8_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                       int32_t num_q_heads, const uint8_t* cache,
+                                       int64_t num_blocks, int32_t num_kv_heads,
+                                       int32_t head_size, int32_t block_size,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, const int32_t* query_start_loc,
+                                       int32_t num_seqs, int32_t max_query_len,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       int32_t segment_len, void* out, kv_int4_dtype out_dtype,
+                                       void* workspace, size_t workspace_bytes,
+                                       kv_int4_stream_t stream);
 
 /*
  * kv_int4_paged_attention_noalloc -- the same attention for callers that cannot allocate device

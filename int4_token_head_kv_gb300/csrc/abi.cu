@@ -198,20 +198,7 @@ bool ws_layout(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int
     return true;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t kv_int4_attention_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
-                                         int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
-    if (num_seqs <= 0 || max_seq_len < 0) return 0;
-    const int32_t seg = kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len);
-    WsLayout w;
-    if (!ws_layout(num_q_heads, num_kv_heads, head_size, num_seqs, max_seq_len, seg, &w)) return 0;
-    return w.total;
-}
-
-kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
                                        int32_t num_q_heads, const uint8_t* cache, int64_t num_blocks,
                                        int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -234,7 +221,9 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     if (segment_len % kBlockSize != 0 || num_seqs > 65535) return KV_INT4_EUNSUPPORTED;
     if (!(softmax_scale == softmax_scale)) return KV_INT4_EINVAL;
     if (num_q_tokens == 0 || num_seqs == 0) return KV_INT4_OK;
-    if (!q || !cache || !block_tables || !seq_lens || !query_start_loc || !rht_signs || !out) return KV_INT4_EINVAL;
+    if (!q || !cache || !block_tables || !seq_lens || !query_start_loc || (bits == 4 && !rht_signs) || !out)
+        return KV_INT4_EINVAL;
+    if (bits == 8 && max_query_len > 1) return KV_INT4_EUNSUPPORTED;   // the INT8 comparator decodes only
     if (max_query_len < 1 || max_blocks_per_seq < 1) return KV_INT4_EINVAL;
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache)) return KV_INT4_EALIGN;
 
@@ -290,9 +279,51 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     const DType qd = q_dtype == KV_INT4_BF16 ? DType::BF16 : DType::F16;
     const DType od = out_dtype == KV_INT4_BF16 ? DType::BF16 : (out_dtype == KV_INT4_F16 ? DType::F16 : DType::F32);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode(p, head_size, ctas, qd, od, s);
-    if (e == cudaSuccess && max_query_len > 1) e = launch_prefill(p, head_size, max_query_len, qd, od, s);
+    cudaError_t e = launch_decode(p, head_size, ctas, qd, od, s, bits);
+    if (e == cudaSuccess && bits == 4 && max_query_len > 1) e = launch_prefill(p, head_size, max_query_len, qd, od, s);
     return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kv_int4_attention_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                         int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
+    if (num_seqs <= 0 || max_seq_len < 0) return 0;
+    const int32_t seg = kv_int4_attention_segment_len(num_seqs, max_seq_len, segment_len);
+    WsLayout w;
+    if (!ws_layout(num_q_heads, num_kv_heads, head_size, num_seqs, max_seq_len, seg, &w)) return 0;
+    return w.total;
+}
+
+kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                       int32_t num_q_heads, const uint8_t* cache, int64_t num_blocks,
+                                       int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                                       int32_t max_query_len, int32_t max_seq_len, float softmax_scale,
+                                       const float* rht_signs, int32_t segment_len, void* out,
+                                       kv_int4_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                       kv_int4_stream_t stream) {
+    return paged_attention_impl(4, q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads, head_size,
+                                block_size, block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                max_query_len, max_seq_len, softmax_scale, rht_signs, segment_len, out, out_dtype,
+                                workspace, workspace_bytes, stream);
+}
+
+kv_int4_status kv_int8_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                       int32_t num_q_heads, const uint8_t* cache, int64_t num_blocks,
+                                       int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                                       int32_t max_query_len, int32_t max_seq_len, float softmax_scale,
+                                       int32_t segment_len, void* out, kv_int4_dtype out_dtype, void* workspace,
+                                       size_t workspace_bytes, kv_int4_stream_t stream) {
+    return paged_attention_impl(8, q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads, head_size,
+                                block_size, block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                max_query_len, max_seq_len, softmax_scale, nullptr, segment_len, out, out_dtype,
+                                workspace, workspace_bytes, stream);
 }
 
 kv_int4_status kv_int4_selftest_wait_timeout(uint64_t timeout_ns, kv_int4_stream_t stream) {

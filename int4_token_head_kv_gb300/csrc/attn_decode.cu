@@ -63,11 +63,19 @@ constexpr uint32_t kLazyExp = 4;     // binades the V exponent reference may fal
 constexpr uint32_t kCodeLo = 0x64006400u;   // (1024, 1024)
 constexpr uint32_t kCodeHi = 0xD400D400u;   // (-64, -64)
 
+// Cached rows: BITS = 4 is the INT4 cache (D/2 code bytes, then the scale word with the zero-point
+// in its low nibble), BITS = 8 the INT8 comparator (D int8 codes, then the fp32 scale).
+template <int D, int BITS>
+struct RowGeo {
+    static constexpr int RB = BITS == 4 ? D / 2 + 4 : D + 4;   // bytes per row
+    static constexpr int SW = BITS == 4 ? D / 8 : D / 4;       // index of the scale word
+};
+
 // Ring depth: 5 stages with up to 4 query heads per kv head, 4 with 8 (whose query records are
-// twice as large), so that two CTAs fit an SM.
-template <bool WIDE>
+// twice as large), so that two CTAs fit an SM; INT8 blocks are twice as large, 2 stages.
+template <bool WIDE, int BITS>
 struct WalkerShape {
-    static constexpr int kStages = WIDE ? 4 : 5;
+    static constexpr int kStages = BITS == 8 ? 2 : (WIDE ? 4 : 5);
 };
 
 struct DecodeSmem {
@@ -87,11 +95,11 @@ constexpr uint32_t kStateBytes = kMaxStages * 8u + 2u * 8u    // ring and query 
                                  + kTableWin * 4u             // block-table window
                                  + kMaxHead * 4u;             // signs
 
-template <int D, bool WIDE>
+template <int D, bool WIDE, int BITS>
 __host__ __device__ inline DecodeSmem decode_smem_layout(int H, int Hq) {
-    using Sh = WalkerShape<WIDE>;
+    using Sh = WalkerShape<WIDE, BITS>;
     DecodeSmem s;
-    s.stage_bytes = 2u * kBlockSize * (uint32_t)H * Geo<D>::RB;
+    s.stage_bytes = 2u * kBlockSize * (uint32_t)H * RowGeo<D, BITS>::RB;
     s.qrec_bytes = decode_qrec_words(D, H, Hq / H) * 4u;
     s.q_off = (Sh::kStages * s.stage_bytes + 127u) & ~127u;
     s.nq = 2;
@@ -143,7 +151,7 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // (32-bit words): for kv head h, 32-dimension group j and lane, the QW fp16x2 words that lane feeds
 // to the score mma; then alpha[Hq rounded up to 4] (raw score -> log2-domain logit, before the
 // key's scale) and qsum[Hq rounded up to 4] (sum of the stored high + low halves of each vector).
-template <int D, bool WIDE, typename QT>
+template <int D, bool WIDE, int BITS, typename QT>
 __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnParams p) {
     constexpr int QW = WIDE ? 8 : 4, KWPT = D / 32;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -159,9 +167,10 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
         float* qsum = alpha + Hq4;
         __half* qh = reinterpret_cast<__half*>(qsum + Hq4);
         __half* ql = qh + Hq * D;
-        for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
+        // INT8 queries are not rotated (sign +1, no transform, no 1/sqrt(d) of the transform)
+        for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = BITS == 4 && p.signs[i] < 0.0f ? -1.0f : 1.0f;
         __syncthreads();
-        const float lsc = p.c * p.softmax_scale * kLog2e;
+        const float lsc = (BITS == 4 ? p.c : 1.0f) * p.softmax_scale * kLog2e;
         for (int v0 = warp; v0 < Hq; v0 += 4 * 8) {   // four vectors per warp at a time
             float x[4][D / 32];
 #pragma unroll
@@ -173,7 +182,7 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
                                      : 0.0f;
             }
             // v = H_d D q; a power-of-two prescale brings max|v| into [2^14, 2^15) for the halves
-            warp_fwht_batch<D, 4>(x);
+            if constexpr (BITS == 4) warp_fwht_batch<D, 4>(x);
             float mx[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -216,9 +225,10 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
                 if (lane == 0 && v0 + 8 * k < Hq) qsum[v0 + 8 * k] = sum[k];
         }
         __syncthreads();
-        // Score-mma B fragments.  Lane (g, t) of kv head h's warp feeds, for code word W = t + 4 j
-        // of a key row (dims 8W .. 8W+7), the pairs (8W+2hh, 8W+2hh+4) and (8W+2hh+1, 8W+2hh+5)
-        // of its column's vector, hh = 0, 1.  Columns: G == 8, head g (high halves; the low
+        // Score-mma B fragments.  Lane (g, t) of kv head h's warp feeds, for the group W = t + 4 j of
+        // dims 8W .. 8W+7 of a key row, the pairs (8W+2hh, 8W+2hh+4) and (8W+2hh+1, 8W+2hh+5) of its
+        // column's vector, hh = 0, 1 (the order of the unpacked nibbles); with INT8 codes the pairs
+        // (8W+4hh, 8W+4hh+1) and (8W+4hh+2, 8W+4hh+3).  Columns: G == 8, head g (high halves; the low
         // halves follow as a second tile); otherwise head g >> 1, the high half for even g and the
         // low half for odd g.
         uint32_t* rec = p.ws_q + (size_t)seq * p.qrec_words;
@@ -234,12 +244,13 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
             uint32_t w[QW];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const int d0 = 8 * W + 2 * hh;
-                w[2 * hh] = live ? pack_halves(qv[d0], qv[d0 + 4]) : 0u;
-                w[2 * hh + 1] = live ? pack_halves(qv[d0 + 1], qv[d0 + 5]) : 0u;
+                const int d0 = BITS == 4 ? 8 * W + 2 * hh : 8 * W + 4 * hh;
+                const int s1 = BITS == 4 ? 4 : 1, s2 = BITS == 4 ? 1 : 2;   // second of a pair; next pair
+                w[2 * hh] = live ? pack_halves(qv[d0], qv[d0 + s1]) : 0u;
+                w[2 * hh + 1] = live ? pack_halves(qv[d0 + s2], qv[d0 + s2 + s1]) : 0u;
                 if constexpr (WIDE) {
-                    w[4 + 2 * hh] = live ? pack_halves(qv2[d0], qv2[d0 + 4]) : 0u;
-                    w[5 + 2 * hh] = live ? pack_halves(qv2[d0 + 1], qv2[d0 + 5]) : 0u;
+                    w[4 + 2 * hh] = live ? pack_halves(qv2[d0], qv2[d0 + s1]) : 0u;
+                    w[5 + 2 * hh] = live ? pack_halves(qv2[d0 + s2], qv2[d0 + s2 + s1]) : 0u;
                 }
             }
             uint4* dst = reinterpret_cast<uint4*>(rec) + (size_t)idx * (QW / 4);
@@ -259,18 +270,19 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
 
 // ------------------------------------------------------------------ 1. split-KV unit walker
 
-template <int D, bool WIDE>
+template <int D, bool WIDE, int BITS>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ AttnParams p) {
     using Gm = Geo<D>;
+    using Rw = RowGeo<D, BITS>;
     constexpr int QW = WIDE ? 8 : 4;      // fragment words per lane per 32-dimension group
     constexpr int NLS = WIDE ? 32 : 16;
-    constexpr int kStages = WalkerShape<WIDE>::kStages;
+    constexpr int kStages = WalkerShape<WIDE, BITS>::kStages;
     constexpr uint32_t PO = decode_po_floats(D, WIDE ? 8 : 1);
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = p.H, G = p.G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const DecodeSmem lay = decode_smem_layout<D, WIDE>(H, p.Hq);
+    const DecodeSmem lay = decode_smem_layout<D, WIDE, BITS>(H, p.Hq);
     const int nq = (int)lay.nq;
     uint8_t* ring = smem;
     uint8_t* qbuf = smem + lay.q_off;
@@ -624,14 +636,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     kp[b] = ring + (size_t)st[b] * stage_bytes;
-                    vp[b] = kp[b] + (size_t)kBlockSize * H * Gm::RB;
+                    vp[b] = kp[b] + (size_t)kBlockSize * H * Rw::RB;
                 }
                 // ---- scores Codes_K Q'^T for both blocks, high and low halves of Q'
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
-                    const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp[b] + (tk0 * H + h) * Gm::RB);
-                    const uint32_t* kr1 = reinterpret_cast<const uint32_t*>(kp[b] + (tk1 * H + h) * Gm::RB);
-                    const uint32_t ks0 = kr0[Gm::KW], ks1 = kr1[Gm::KW];
+                    const uint32_t* kr0 = reinterpret_cast<const uint32_t*>(kp[b] + (tk0 * H + h) * Rw::RB);
+                    const uint32_t* kr1 = reinterpret_cast<const uint32_t*>(kp[b] + (tk1 * H + h) * Rw::RB);
+                    const uint32_t ks0 = kr0[Rw::SW], ks1 = kr1[Rw::SW];
                     // two independent accumulation chains per block: the high- and low-half tiles
                     // when G = 8, the two halves of each code word otherwise
                     float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -640,8 +652,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 #pragma unroll
                         for (int q = 0; q < Gm::KWPT; ++q) {
                             uint32_t a0[4], a1[4];
-                            unpack_word(kr0[t + 4 * q], kCodeLo, kCodeHi, a0);
-                            unpack_word(kr1[t + 4 * q], kCodeLo, kCodeHi, a1);
+                            if constexpr (BITS == 4) {
+                                unpack_word(kr0[t + 4 * q], kCodeLo, kCodeHi, a0);
+                                unpack_word(kr1[t + 4 * q], kCodeLo, kCodeHi, a1);
+                            } else {
+                                unpack_i8(kr0[2 * (t + 4 * q)], kr0[2 * (t + 4 * q) + 1], a0);
+                                unpack_i8(kr1[2 * (t + 4 * q)], kr1[2 * (t + 4 * q) + 1], a1);
+                            }
                             if constexpr (WIDE) {
                                 mma_f16_16816(c, a0[0], a1[0], a0[1], a1[1], qb[2 * q][0], qb[2 * q][1]);
                                 mma_f16_16816(c, a0[2], a1[2], a0[3], a1[3], qb[2 * q + 1][0], qb[2 * q + 1][1]);
@@ -657,9 +674,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     for (int e = 0; e < 4; ++e) c[e] += c2[e];
                     const int tb = (k + b) * kBlockSize;   // token offset of this block in the unit
                     const bool v0 = ok[b] && tb + tk0 < u.w, v1 = ok[b] && tb + tk1 < u.w;
-                    const float sk0 = __uint_as_float(ks0 & 0xFFFFFFF0u), sk1 = __uint_as_float(ks1 & 0xFFFFFFF0u);
-                    // score = S - zp sum(Q'), then the key's scale and the logit factor
-                    const float zk0 = nibble_to_float(ks0), zk1 = nibble_to_float(ks1);
+                    constexpr uint32_t kScaleMask = BITS == 4 ? 0xFFFFFFF0u : 0xFFFFFFFFu;   // INT8: plain fp32
+                    const float sk0 = __uint_as_float(ks0 & kScaleMask), sk1 = __uint_as_float(ks1 & kScaleMask);
+                    // score = S - zp sum(Q'), then the key's scale and the logit factor (INT8: no zp)
+                    const float zk0 = BITS == 4 ? nibble_to_float(ks0) : 0.0f, zk1 = BITS == 4 ? nibble_to_float(ks1) : 0.0f;
                     if constexpr (WIDE) {   // x = (token tk0: heads hb, hb+1; token tk1: heads hb, hb+1)
                         x[b][0] = v0 ? fmaf(-zk0, qs0, c[0]) * sk0 * al0 : -INFINITY;
                         x[b][1] = v0 ? fmaf(-zk0, qs1, c[1]) * sk0 * al1 : -INFINITY;
@@ -670,10 +688,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         x[b][2] = v1 ? fmaf(-zk1, qs0, c[2] + c[3]) * sk1 * al0 : -INFINITY;
                         x[b][1] = x[b][3] = -INFINITY;
                     }
-                    const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp[b] + (tk0 * H + h) * Gm::RB);
-                    const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp[b] + (tk1 * H + h) * Gm::RB);
-                    vs0[b] = v0 ? vg0[Gm::KW] : 0u;   // invisible tokens: scale word 0 (exponent 0, weight 0)
-                    vs1[b] = v1 ? vg1[Gm::KW] : 0u;
+                    const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp[b] + (tk0 * H + h) * Rw::RB);
+                    const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp[b] + (tk1 * H + h) * Rw::RB);
+                    vs0[b] = v0 ? vg0[Rw::SW] : 0u;   // invisible tokens: scale word 0 (exponent 0, weight 0)
+                    vs1[b] = v1 ? vg1[Rw::SW] : 0u;
                 }
                 // ---- one online-softmax update for heads hb (, hb+1) over the 32 tokens
                 float bm0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
@@ -732,12 +750,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
                     if (!ok[b]) continue;
-                    const float sv0 = __uint_as_float(vs0[b] & 0xFFFFFFF0u) * wsc;
-                    const float sv1 = __uint_as_float(vs1[b] & 0xFFFFFFF0u) * wsc;
+                    constexpr uint32_t kVMask = BITS == 4 ? 0xFFFFFFF0u : 0xFFFFFFFFu;
+                    const float sv0 = __uint_as_float(vs0[b] & kVMask) * wsc;
+                    const float sv1 = __uint_as_float(vs1[b] & kVMask) * wsc;
                     // weights w = p * s'_V * 2^-E (invisible tokens: 0)
                     const float wa0 = pr[b][0] * sv0, wa1 = pr[b][1] * sv0;   // token tk0
                     const float wb0 = pr[b][2] * sv1, wb1 = pr[b][3] * sv1;   // token tk1
-                    const float zv0 = nibble_to_float(vs0[b]), zv1 = nibble_to_float(vs1[b]);
+                    const float zv0 = BITS == 4 ? nibble_to_float(vs0[b]) : 0.0f, zv1 = BITS == 4 ? nibble_to_float(vs1[b]) : 0.0f;
                     uint32_t bb0, bb1;
                     if constexpr (WIDE) {
                         // All eight columns are heads: plain fp16 weights (they are not exponentiated
@@ -757,24 +776,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         bb0 = movmatrix_trans(hi_lo_f16x2(wa0));
                         bb1 = movmatrix_trans(hi_lo_f16x2(wb0));
                     }
-                    const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp[b] + ((t)*H + h) * Gm::RB);
-                    const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 4) * H + h) * Gm::RB);
-                    const uint32_t* vr2 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 8) * H + h) * Gm::RB);
-                    const uint32_t* vr3 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 12) * H + h) * Gm::RB);
+                    const uint32_t* vr0 = reinterpret_cast<const uint32_t*>(vp[b] + ((t)*H + h) * Rw::RB);
+                    const uint32_t* vr1 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 4) * H + h) * Rw::RB);
+                    const uint32_t* vr2 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 8) * H + h) * Rw::RB);
+                    const uint32_t* vr3 = reinterpret_cast<const uint32_t*>(vp[b] + ((t + 12) * H + h) * Rw::RB);
+                    // dims 8G + i of two rows as fp16 pairs
+                    auto dims8 = [&](const uint32_t* ra, const uint32_t* rb, int G8, uint32_t (&u)[8]) {
+                        if constexpr (BITS == 4) unpack_word_pair(ra[G8], rb[G8], kCodeLo, kCodeHi, u);
+                        else unpack_i8_pair(ra[2 * G8], ra[2 * G8 + 1], rb[2 * G8], rb[2 * G8 + 1], u);
+                    };
                     if constexpr (D == 128) {
                         uint32_t ua[8], ubv[8], uc[8], ud[8];
-                        unpack_word_pair(vr0[g], vr1[g], kCodeLo, kCodeHi, ua);            // d = 8g + i, tokens t, t+4
-                        unpack_word_pair(vr0[g + 8], vr1[g + 8], kCodeLo, kCodeHi, ubv);   // d = 64 + 8g + i
-                        unpack_word_pair(vr2[g], vr3[g], kCodeLo, kCodeHi, uc);            // tokens t+8, t+12
-                        unpack_word_pair(vr2[g + 8], vr3[g + 8], kCodeLo, kCodeHi, ud);
+                        dims8(vr0, vr1, g, ua);        // d = 8g + i, tokens t, t+4
+                        dims8(vr0, vr1, g + 8, ubv);   // d = 64 + 8g + i
+                        dims8(vr2, vr3, g, uc);        // tokens t+8, t+12
+                        dims8(vr2, vr3, g + 8, ud);
 #pragma unroll
                         for (int mt = 0; mt < 8; ++mt) {
                             mma_f16_16816(o[mt], ua[mt], ubv[mt], uc[mt], ud[mt], bb0, bb1);
                         }
                     } else {
                         uint32_t ua[8], uc[8];
-                        unpack_word_pair(vr0[g], vr1[g], kCodeLo, kCodeHi, ua);   // d = 8g + i
-                        unpack_word_pair(vr2[g], vr3[g], kCodeLo, kCodeHi, uc);
+                        dims8(vr0, vr1, g, ua);   // d = 8g + i
+                        dims8(vr2, vr3, g, uc);
 #pragma unroll
                         for (int mt = 0; mt < 4; ++mt) {
                             mma_f16_16816(o[mt], ua[mt], ua[4 + mt], uc[mt], uc[4 + mt], bb0, bb1);
@@ -878,7 +902,7 @@ __host__ __device__ inline size_t combine_smem_bytes(int W, int G) {
 // the accumulator slots lane + 32 j of the fragment-ordered partials (whole 512-byte rows, so
 // every load is coalesced, several records in flight), and the chunk states are then folded in
 // chunk order through shared memory, normalised, and the G outputs un-rotated by the group's warps.
-template <int D, bool WIDE, typename OT>
+template <int D, bool WIDE, int BITS, typename OT>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttnParams p) {
     constexpr int NLS = WIDE ? 32 : 16;
     constexpr int NT = Geo<D>::MT * NLS;   // float4 slots of one record
@@ -895,7 +919,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     float* sout = reinterpret_cast<float*>(sml + kCombineWarps * 4);   // [groups][G][SO]
     // Up to the wait on the walker this kernel reads only host inputs, so it overlaps the walker's
     // last CTAs on the SMs they have left.
-    for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
+    if constexpr (BITS == 4)
+        for (int i = threadIdx.x; i < D; i += blockDim.x) sgn[i] = p.signs[i] < 0.0f ? -1.0f : 1.0f;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // decode segments of sequence b (0 for other sequences), as the walker counts them
     auto segments_of = [&](int b) -> int {
@@ -1042,16 +1067,21 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
         float x[D / 32];
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) x[k] = gout[col * SO + lane + 32 * k];
-        unrotate_store<D, OT>(x, 1.0f, sgn, p.c, p.out, obase + (int64_t)col * D);
+        if constexpr (BITS == 4) {
+            unrotate_store<D, OT>(x, 1.0f, sgn, p.c, p.out, obase + (int64_t)col * D);
+        } else {   // INT8: the output is not rotated
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) store_elem<OT>(p.out, obase + (int64_t)col * D + lane + 32 * k, x[k]);
+        }
     }
 }
 
 // ------------------------------------------------------------------ launchers
 
-template <int D, bool WIDE, typename QT, typename OT>
+template <int D, bool WIDE, int BITS, typename QT, typename OT>
 cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stream) {
-    const DecodeSmem lay = decode_smem_layout<D, WIDE>(p.H, p.Hq);
-    cudaError_t err = opt_in_smem<decode_kernel<D, WIDE>>(lay.total);
+    const DecodeSmem lay = decode_smem_layout<D, WIDE, BITS>(p.H, p.Hq);
+    cudaError_t err = opt_in_smem<decode_kernel<D, WIDE, BITS>>(lay.total);
     if (err != cudaSuccess) return err;
     // All three kernels are programmatic dependents of their predecessor: each starts its set-up
     // while the previous kernel finishes and waits for it (griddep_wait) before touching its
@@ -1067,7 +1097,7 @@ cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stre
     qcfg.stream = stream;
     qcfg.attrs = &attr;
     qcfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&qcfg, qrot_kernel<D, WIDE, QT>, p);
+    err = cudaLaunchKernelEx(&qcfg, qrot_kernel<D, WIDE, BITS, QT>, p);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t wcfg = {};
     wcfg.gridDim = dim3((unsigned)num_ctas);
@@ -1076,14 +1106,14 @@ cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stre
     wcfg.stream = stream;
     wcfg.attrs = &attr;
     wcfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&wcfg, decode_kernel<D, WIDE>, p);
+    err = cudaLaunchKernelEx(&wcfg, decode_kernel<D, WIDE, BITS>, p);
     if (err != cudaSuccess) return err;
 
     const int W = p.combine_warps;
     const int64_t items = (int64_t)p.num_seqs * p.H;
     const int64_t per_cta = kCombineWarps / W;
     const size_t csmem = combine_smem_bytes<D, WIDE>(W, p.G);
-    err = opt_in_smem<combine_kernel<D, WIDE, OT>>(csmem);
+    err = opt_in_smem<combine_kernel<D, WIDE, BITS, OT>>(csmem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((items + per_cta - 1) / per_cta));
@@ -1092,22 +1122,22 @@ cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stre
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<D, WIDE, OT>, p);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, WIDE, BITS, OT>, p);
 }
 
-template <int D, bool WIDE, typename QT>
+template <int D, bool WIDE, int BITS, typename QT>
 cudaError_t decode_by_out(const AttnParams& p, int num_ctas, DType out_dt, cudaStream_t s) {
     switch (out_dt) {
-        case DType::F16: return launch_decode_t<D, WIDE, QT, __half>(p, num_ctas, s);
-        case DType::BF16: return launch_decode_t<D, WIDE, QT, __nv_bfloat16>(p, num_ctas, s);
-        default: return launch_decode_t<D, WIDE, QT, float>(p, num_ctas, s);
+        case DType::F16: return launch_decode_t<D, WIDE, BITS, QT, __half>(p, num_ctas, s);
+        case DType::BF16: return launch_decode_t<D, WIDE, BITS, QT, __nv_bfloat16>(p, num_ctas, s);
+        default: return launch_decode_t<D, WIDE, BITS, QT, float>(p, num_ctas, s);
     }
 }
 
-template <int D, bool WIDE>
+template <int D, bool WIDE, int BITS>
 cudaError_t decode_by_q(const AttnParams& p, int num_ctas, DType q_dt, DType out_dt, cudaStream_t s) {
-    return q_dt == DType::BF16 ? decode_by_out<D, WIDE, __nv_bfloat16>(p, num_ctas, out_dt, s)
-                               : decode_by_out<D, WIDE, __half>(p, num_ctas, out_dt, s);
+    return q_dt == DType::BF16 ? decode_by_out<D, WIDE, BITS, __nv_bfloat16>(p, num_ctas, out_dt, s)
+                               : decode_by_out<D, WIDE, BITS, __half>(p, num_ctas, out_dt, s);
 }
 
 }  // namespace
@@ -1123,13 +1153,20 @@ int decode_grid_size(int64_t max_weight_total, int64_t max_units) {
 }
 
 cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int bits) {
     const bool wide = p.G == 8;
+    if (bits == 8) {
+        if (head_size == 128)
+            return wide ? decode_by_q<128, true, 8>(p, num_ctas, q_dt, out_dt, stream)
+                        : decode_by_q<128, false, 8>(p, num_ctas, q_dt, out_dt, stream);
+        return wide ? decode_by_q<64, true, 8>(p, num_ctas, q_dt, out_dt, stream)
+                    : decode_by_q<64, false, 8>(p, num_ctas, q_dt, out_dt, stream);
+    }
     if (head_size == 128)
-        return wide ? decode_by_q<128, true>(p, num_ctas, q_dt, out_dt, stream)
-                    : decode_by_q<128, false>(p, num_ctas, q_dt, out_dt, stream);
-    return wide ? decode_by_q<64, true>(p, num_ctas, q_dt, out_dt, stream)
-                : decode_by_q<64, false>(p, num_ctas, q_dt, out_dt, stream);
+        return wide ? decode_by_q<128, true, 4>(p, num_ctas, q_dt, out_dt, stream)
+                    : decode_by_q<128, false, 4>(p, num_ctas, q_dt, out_dt, stream);
+    return wide ? decode_by_q<64, true, 4>(p, num_ctas, q_dt, out_dt, stream)
+                : decode_by_q<64, false, 4>(p, num_ctas, q_dt, out_dt, stream);
 }
 
 }  // namespace kvi4

@@ -283,6 +283,31 @@ __device__ __forceinline__ void unpack_word_pair(uint32_t wa, uint32_t wb, uint3
     }
 }
 
+// ----------------------------------------------------------------------- int8 code unpacking
+// Four int8 codes of a word as offset binary x + 128 (the sign bit flipped) under the fp16 exponent
+// byte 0x64 give 1024 + x + 128 exactly; subtracting 1152 leaves x.
+constexpr uint32_t kI8Exp = 0x64646464u, kI8Flip = 0x80808080u, kI8Bias = 0x64806480u;   // (1152, 1152)
+
+// Dimensions 0..3 (word w0) and 4..7 (word w1) of a row as fp16 pairs (0, 1), (2, 3), (4, 5), (6, 7).
+__device__ __forceinline__ void unpack_i8(uint32_t w0, uint32_t w1, uint32_t (&o)[4]) {
+    const uint32_t u0 = w0 ^ kI8Flip, u1 = w1 ^ kI8Flip;
+    o[0] = hsub2(prmt(u0, kI8Exp, 0x5140u), kI8Bias);
+    o[1] = hsub2(prmt(u0, kI8Exp, 0x7362u), kI8Bias);
+    o[2] = hsub2(prmt(u1, kI8Exp, 0x5140u), kI8Bias);
+    o[3] = hsub2(prmt(u1, kI8Exp, 0x7362u), kI8Bias);
+}
+
+// The same eight dimensions of two rows a and b: o[i] = (a's dimension i, b's dimension i).
+__device__ __forceinline__ void unpack_i8_pair(uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1, uint32_t (&o)[8]) {
+    const uint32_t m[4] = {prmt(a0 ^ kI8Flip, b0 ^ kI8Flip, 0x5140u), prmt(a0 ^ kI8Flip, b0 ^ kI8Flip, 0x7362u),
+                           prmt(a1 ^ kI8Flip, b1 ^ kI8Flip, 0x5140u), prmt(a1 ^ kI8Flip, b1 ^ kI8Flip, 0x7362u)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {   // m[k] = (a_2k, b_2k, a_2k+1, b_2k+1)
+        o[2 * k] = hsub2(prmt(m[k], kI8Exp, 0x4140u), kI8Bias);
+        o[2 * k + 1] = hsub2(prmt(m[k], kI8Exp, 0x4342u), kI8Bias);
+    }
+}
+
 // Token order inside a 16-token block used by the attention kernels: mma row / key index r maps
 // to token tau(r) = ((r & 7) >> 1) + 4 * (r & 1) + 8 * (r >> 3).  It makes the four rows a thread
 // reads for P.V (tokens t, t+4, t+8, t+12 of lane quad t) fall in distinct shared-memory banks.

@@ -67,8 +67,9 @@ cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStre
 cudaError_t launch_write_int8(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
 // Decode path: query rotation, the split-KV segment walker, and the combine that finishes every
 // decode sequence.  num_ctas is the walker's grid (decode_grid_size).
+// bits: 4 for the INT4 cache, 8 for the INT8 comparator's cache (no rotation, no zero-points)
 cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
-                          cudaStream_t stream);
+                          cudaStream_t stream, int bits);
 int decode_grid_size(int64_t max_weight_total, int64_t max_units);
 constexpr int kDecodeMaxUnits = 256;   // split-KV units one walker CTA may own
 

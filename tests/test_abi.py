@@ -19,7 +19,7 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kv_int4_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(kv_int[48]_\w+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -109,6 +109,29 @@ def test_attention_validation_and_workspace_policy(lib):
     assert auto % 32 == 0 and 32 <= auto <= 4096
     assert lib.kv_int4_attention_segment_len(1, 16, 0) == 32     # floor: one block pair
     assert lib.kv_int4_attention_segment_len(4096, 1 << 20, 0) == 4096   # ceiling
+
+
+def test_int8_attention_validation(lib):
+    f = lib.kv_int8_paged_attention
+    f.restype = ctypes.c_int
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float,
+                  i32, vp, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    fake = 1 << 20
+    base = dict(q=fake, qd=1, nq=2, hq=32, cache=fake, nb=64, h=8, d=128, bs=16, bt=fake, mb=4, sl=fake, qsl=fake,
+                ns=2, mql=1, msl=64, scale=0.088, seg=0, out=fake, od=2, ws=None, wsb=0, st=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(*a.values())
+
+    assert call(mql=2) == 2                # decode only: a chunk of several queries is not built
+    assert call(h=3, hq=24) == 2
+    assert call(d=96) == 2
+    assert call(cache=None) == 1
+    assert call(q=fake + 8) == 3
+    assert call(msl=131072, seg=4096, mb=8192) == 4   # the INT4 call's workspace, required and missing
+    assert call(nq=0) == 0
 
 
 def test_status_strings(lib):

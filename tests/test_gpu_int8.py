@@ -75,3 +75,97 @@ def test_int8_edge_vectors(dtype):
     wl.key = torch.from_numpy(x[:, None, :]).to(dtype)
     wl.value = torch.from_numpy(-x[:, None, :]).to(dtype)
     _check(wl, fill=0x11)
+
+
+# ---------------------------------------------------------------------------- INT8 decode attention
+# kv_int8_paged_attention against oracle/int8.py's paged_attention over the oracle's own INT8 cache
+# (checked byte-identical to the GPU's first): |gpu - oracle| <= 2e-3 + 1e-2 |oracle|, as for INT4.
+
+def _int8_attention_case(wl, seqs=None, kv_heads=None, segment_len=None, out_dtype=torch.float32):
+    import int4_token_head_kv_gb300 as kv
+    from gpu_helpers import assert_attention_close, dev, status
+    H, d = wl.num_kv_heads, wl.head_size
+    cache = torch.zeros(kv.kv_int8_cache_shape(wl.num_blocks, wl.block_size, H, d), dtype=torch.uint8, device=dev())
+    rows = None if seqs is None else np.concatenate([np.arange(wl.token_start[b], wl.token_start[b + 1]) for b in seqs])
+    k, v, s = (wl.key, wl.value, wl.slot_mapping) if rows is None else (wl.key[rows], wl.value[rows], wl.slot_mapping[rows])
+    kv.kv_int8_write(k.to(dev()).contiguous(), v.to(dev()).contiguous(),
+                     torch.from_numpy(np.ascontiguousarray(s)).to(dev()), cache)
+    seg = wl.segment_len if segment_len is None else segment_len
+    out = kv.kv_int8_paged_attention(
+        wl.query.to(dev()), cache, torch.from_numpy(wl.block_tables).to(dev()),
+        torch.from_numpy(wl.seq_lens).to(dev()), torch.from_numpy(wl.query_start_loc).to(dev()),
+        wl.softmax_scale, max_query_len=wl.max_query_len, max_seq_len=wl.max_seq_len, out_dtype=out_dtype,
+        segment_len=seg)
+    torch.cuda.synchronize()
+    ref_cache = np.zeros(o8.cache_shape(wl.num_blocks, wl.block_size, H, d), np.uint8)
+    o8.write(k, v, s, ref_cache)
+    got = cache.cpu().numpy()
+    if seqs is None:
+        assert np.array_equal(got, ref_cache), "GPU INT8 cache differs from the oracle's"
+    ref = o8.paged_attention(wl.query, ref_cache, wl.block_tables, wl.seq_lens, wl.query_start_loc, wl.softmax_scale,
+                             seqs=seqs, kv_heads=kv_heads)
+    err = assert_attention_close(out, ref, wl.name + " (int8)")
+    st = status()
+    assert not any(st.values()), st
+    return err
+
+
+@pytest.mark.parametrize("H,G,d", [(1, 1, 64), (2, 4, 128), (4, 2, 64), (8, 8, 128), (8, 1, 64), (1, 8, 128)])
+def test_int8_decode_head_groupings(H, G, d):
+    # ragged contexts across block and segment edges
+    wl = workloads.make_attention_workload("int8_groupings", [1, 15, 16, 17, 300, 64, 1024, 77], [1] * 8, H * G, H, d,
+                                           seed=11, segment_len=64)
+    _int8_attention_case(wl)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
+def test_int8_decode_output_dtypes(out_dtype):
+    wl = workloads.tiny_write_decode()
+    _int8_attention_case(wl, out_dtype=out_dtype)
+
+
+def test_int8_decode_gqa_batch_full_size():
+    _int8_attention_case(workloads.gqa_decode_batch(), segment_len=0)
+
+
+def test_int8_decode_long_context_full_size_sampled():
+    # at the library's segment length (what the benchmark times)
+    wl = workloads.long_context_decode()
+    _int8_attention_case(wl, seqs=[0, 7], kv_heads=[0, 5], segment_len=0)
+
+
+def test_int8_decode_mixed_magnitudes():
+    wl = workloads.make_attention_workload("int8_magnitudes", [500, 33, 2000], [1, 1, 1], 16, 4, 128, seed=12,
+                                           segment_len=256)
+    scale = torch.ones(wl.key.shape[0], 1, 1)
+    scale[::7] = 300.0
+    scale[3::11] = 1e-3
+    wl.key = (wl.key.float() * scale).to(wl.key.dtype)
+    wl.value = (wl.value.float() * scale).to(wl.value.dtype)
+    _int8_attention_case(wl)
+
+
+def test_int8_attention_rejects_prefill_chunks():
+    import int4_token_head_kv_gb300 as kv
+    wl = workloads.make_attention_workload("int8_prefill", [64], [8], 4, 4, 64, seed=13)
+    from gpu_helpers import dev
+    cache = torch.zeros(kv.kv_int8_cache_shape(wl.num_blocks, 16, 4, 64), dtype=torch.uint8, device=dev())
+    with pytest.raises(RuntimeError):
+        kv.kv_int8_paged_attention(wl.query.to(dev()), cache, torch.from_numpy(wl.block_tables).to(dev()),
+                                   torch.from_numpy(wl.seq_lens).to(dev()),
+                                   torch.from_numpy(wl.query_start_loc).to(dev()), wl.softmax_scale,
+                                   max_query_len=8, max_seq_len=64)
+
+
+def test_int8_empty_context_gives_zeros():
+    import int4_token_head_kv_gb300 as kv
+    from gpu_helpers import dev
+    d = 128
+    cache = torch.zeros(kv.kv_int8_cache_shape(4, 16, 2, d), dtype=torch.uint8, device=dev())
+    q = torch.randn(2, 4, d, device=dev(), dtype=torch.bfloat16)
+    out = kv.kv_int8_paged_attention(q, cache, torch.zeros(2, 1, dtype=torch.int32, device=dev()),
+                                     torch.tensor([0, 0], dtype=torch.int32, device=dev()),
+                                     torch.tensor([0, 1, 2], dtype=torch.int32, device=dev()), d ** -0.5,
+                                     max_query_len=1, max_seq_len=0, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
