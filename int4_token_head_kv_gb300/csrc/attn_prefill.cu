@@ -593,15 +593,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             }
         }
         if (!rows_meet(epi, 0)) ok = false;
+        // un-rotation out = c D H x, four rows at a time (their butterfly chains interleave)
         const float* ost = reinterpret_cast<const float*>(tiles);
-        for (int i = 0; i < kPfRows / kPfSoftmaxWarps && ok; ++i) {
-            const int R = warp * (kPfRows / kPfSoftmaxWarps) + i;
-            const int qt = qt0 + R / G, gg = R % G;
-            if (qt >= qlen) continue;
-            float xv[D / 32];
+        constexpr int RPW = kPfRows / kPfSoftmaxWarps;
+#pragma unroll 1
+        for (int i0 = 0; i0 < RPW && ok; i0 += 4) {
+            float xv[4][D / 32];
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) xv[k] = ost[R * Ly::kOStride + lane + 32 * k];
-            unrotate_store<D, OT>(xv, 1.0f, sgn, p.c, p.out, ((int64_t)(q0 + qt) * Hq + h * G + gg) * D);
+            for (int v = 0; v < 4; ++v)
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) xv[v][k] = ost[(warp * RPW + i0 + v) * Ly::kOStride + lane + 32 * k];
+            warp_fwht_batch<D, 4>(xv);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int R = warp * RPW + i0 + v;
+                const int qt = qt0 + R / G, gg = R % G;
+                if (qt >= qlen) continue;
+                const int64_t ooff = ((int64_t)(q0 + qt) * Hq + h * G + gg) * D;
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k)
+                    store_elem<OT>(p.out, ooff + lane + 32 * k, xv[v][k] * p.c * sgn[lane + 32 * k]);
+            }
         }
     } else if (warp < kPfMmaWarp) {
         // ================================================================ dequantisation of key tiles
