@@ -209,7 +209,7 @@ def gather_rows(cache: np.ndarray, block_table_row: np.ndarray, seq_len: int, pl
 
 
 def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softmax_scale, signs,
-                    seqs=None, kv_heads=None) -> np.ndarray:
+                    seqs=None, kv_heads=None, window_left=-1, softcap=0.0, alibi_slopes=None) -> np.ndarray:
     """Causal softmax attention over the dequantised, un-rotated paged cache, in fp64.
 
     query [Nq, Hq, d] (original domain); sequence b owns query rows
@@ -217,6 +217,14 @@ def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softm
     seq_len[b] - q_len[b] + t, seeing keys 0 .. that position.  Query head g reads kv head
     g // (Hq / H).  Returns fp64 [Nq, Hq, d]; rows of sequences or kv heads that are not selected
     (``seqs`` / ``kv_heads``) are NaN.  An empty key range gives a zero output.
+
+    Options of the unified-attention interface ("tests/quantization/test_per_token_kv_cache.py",
+    ``window_size`` and ``softcap`` arguments; the PR #40633 description lists sliding window,
+    softcap and ALiBi among the shared helpers), in this order on the scaled logit
+    s_j = softmax_scale * q . k_j of key j for a query at position pos:
+      softcap > 0:           s_j <- softcap * tanh(s_j / softcap)
+      alibi_slopes [Hq]:     s_j <- s_j + slope_g * (j - pos)
+      window_left >= 0:      key j is visible only if pos - j <= window_left (besides j <= pos).
     """
     q = _as_f32_array(query).astype(np.float64)
     nq, hq, d = q.shape
@@ -237,11 +245,16 @@ def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softm
             for t in range(qlen):
                 pos = L - qlen + t
                 nkeys = max(0, min(pos + 1, L))
+                first = max(0, pos - window_left) if window_left >= 0 else 0   # first visible key
                 for g in range(h * G, (h + 1) * G):
-                    if nkeys == 0:
+                    if nkeys <= first:
                         out[q0 + t, g] = 0.0
                         continue
-                    s = softmax_scale * (khat[:nkeys] @ q[q0 + t, g])
+                    s = softmax_scale * (khat[first:nkeys] @ q[q0 + t, g])
+                    if softcap > 0:
+                        s = softcap * np.tanh(s / softcap)
+                    if alibi_slopes is not None:
+                        s = s + float(alibi_slopes[g]) * (np.arange(first, nkeys) - pos)
                     w = np.exp(s - s.max())
-                    out[q0 + t, g] = (w @ vhat[:nkeys]) / w.sum()
+                    out[q0 + t, g] = (w @ vhat[first:nkeys]) / w.sum()
     return out

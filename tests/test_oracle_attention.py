@@ -86,8 +86,9 @@ def test_identical_keys_give_the_mean_value():
     np.testing.assert_allclose(out[0, 1], vhat.mean(0), atol=1e-12)
 
 
-def _brute_force(wl, cache):
-    """Independent restatement: scipy's Hadamard and softmax, explicit per-key loops."""
+def _brute_force(wl, cache, bias=None):
+    """Independent restatement: scipy's Hadamard and softmax, explicit per-key loops.  bias(g, j,
+    pos, s) -> the logit of key j (None: masked) overrides the plain scaled dot product."""
     d = wl.head_size
     hm = scipy.linalg.hadamard(d).astype(np.float64)
     G = wl.num_q_heads // wl.num_kv_heads
@@ -117,7 +118,16 @@ def _brute_force(wl, cache):
                         vecs.append(wl.signs * (hm @ y) / np.sqrt(d))
                     ks.append(vecs[0])
                     vs.append(vecs[1])
-                p = scipy.special.softmax(wl.softmax_scale * np.array(ks) @ q[q0 + t, g])
+                logits = wl.softmax_scale * np.array(ks) @ q[q0 + t, g]
+                if bias is not None:
+                    kept = [(bias(g, j, pos, float(logits[j])), j) for j in range(pos + 1)]
+                    kept = [(x, j) for x, j in kept if x is not None]
+                    if not kept:
+                        continue
+                    p = scipy.special.softmax(np.array([x for x, _ in kept]))
+                    out[q0 + t, g] = p @ np.array([vs[j] for _, j in kept])
+                    continue
+                p = scipy.special.softmax(logits)
                 out[q0 + t, g] = p @ np.array(vs)
     return out
 
@@ -168,3 +178,71 @@ def test_score_side_correction_identity():
     qrot = (oracle.hadamard(d) @ (signs * q)) / np.sqrt(d)       # R q in fp64
     split = sp * (codes.astype(np.float64) @ qrot - zp * qrot.sum())
     np.testing.assert_allclose(split, oracle.decode_rows(rows, signs) @ q, rtol=1e-10, atol=1e-10)
+
+
+# ---------------------------------------------------------------- options: window, softcap, ALiBi
+# The unified-attention interface's window_size / softcap arguments ("tests/quantization/
+# test_per_token_kv_cache.py") and the ALiBi helper the PR #40633 description lists, each pinned
+# against the brute force (its own per-key loop, math.tanh, explicit bias) and closed forms.
+
+def test_window_zero_returns_the_current_value():
+    wl = workloads.make_attention_workload("t", [29, 40], [1, 3], 4, 2, 64, seed=21)
+    cache = _cache_for(wl)
+    out = _run(wl, cache, window_left=0)
+    for b in range(2):
+        L = int(wl.seq_lens[b])
+        q0, q1 = int(wl.query_start_loc[b]), int(wl.query_start_loc[b + 1])
+        for t in range(q1 - q0):
+            pos = L - (q1 - q0) + t
+            for g in range(4):
+                vhat = oracle.decode_rows(oracle.gather_rows(cache, wl.block_tables[b], L, 1, g // 2), wl.signs)
+                np.testing.assert_allclose(out[q0 + t, g], vhat[pos], atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [3, 16, 100])
+def test_window_matches_brute_force(window):
+    wl = workloads.make_attention_workload("t", [19, 5, 33], [4, 1, 7], 6, 2, 64, seed=22)
+    cache = _cache_for(wl)
+    ref = _brute_force(wl, cache, bias=lambda g, j, pos, s: s if pos - j <= window else None)
+    np.testing.assert_allclose(_run(wl, cache, window_left=window), ref, rtol=1e-10, atol=1e-12)
+
+
+def test_softcap_matches_brute_force_and_vanishes_when_large():
+    import math
+    wl = workloads.make_attention_workload("t", [19, 5, 33], [4, 1, 7], 6, 2, 64, seed=23)
+    wl.query = (wl.query.float() * 8.0).to(wl.query.dtype)   # logits large enough for the cap to bite
+    cache = _cache_for(wl)
+    cap = 5.0
+    ref = _brute_force(wl, cache, bias=lambda g, j, pos, s: cap * math.tanh(s / cap))
+    np.testing.assert_allclose(_run(wl, cache, softcap=cap), ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(_run(wl, cache, softcap=1e12), _run(wl, cache), rtol=1e-9, atol=1e-12)
+
+
+def test_alibi_matches_brute_force_and_limits():
+    wl = workloads.make_attention_workload("t", [19, 5, 33], [4, 1, 7], 6, 2, 64, seed=24)
+    cache = _cache_for(wl)
+    slopes = np.array([0.0, 0.5, 0.125, 1.0, 0.03125, 2.0])
+    ref = _brute_force(wl, cache, bias=lambda g, j, pos, s: s + slopes[g] * (j - pos))
+    np.testing.assert_allclose(_run(wl, cache, alibi_slopes=slopes), ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(_run(wl, cache, alibi_slopes=np.zeros(6)), _run(wl, cache), atol=0)
+    # a steep slope leaves only the newest key
+    steep = _run(wl, cache, alibi_slopes=np.full(6, 1e4))
+    np.testing.assert_allclose(steep, _run(wl, cache, window_left=0), atol=1e-12)
+
+
+def test_options_compose_in_order():
+    import math
+    wl = workloads.make_attention_workload("t", [33], [5], 4, 2, 64, seed=25)
+    wl.query = (wl.query.float() * 6.0).to(wl.query.dtype)
+    cache = _cache_for(wl)
+    cap, window = 4.0, 9
+    slopes = np.array([0.25, 0.5, 0.0625, 1.0])
+
+    def bias(g, j, pos, s):
+        if pos - j > window:
+            return None
+        return cap * math.tanh(s / cap) + slopes[g] * (j - pos)
+
+    ref = _brute_force(wl, cache, bias=bias)
+    got = _run(wl, cache, window_left=window, softcap=cap, alibi_slopes=slopes)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
