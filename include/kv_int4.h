@@ -195,6 +195,39 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
                                        size_t workspace_bytes, kv_int4_stream_t stream);
 
 /*
+ * kv_int4_paged_attention_ex -- kv_int4_paged_attention with the unified-attention interface's
+ * options ("tests/quantization/test_per_token_kv_cache.py", the window_size and softcap arguments
+ * of unified_attention; the PR #40633 description lists sliding window, softcap and ALiBi among
+ * the helpers the packed read path shares).  On the scaled logit s_j = softmax_scale * q . x_K,j
+ * of key j for a query at position pos, in this order:
+ *   softcap > 0            s_j <- softcap * tanh(s_j / softcap)
+ *   alibi_slopes != NULL   s_j <- s_j + alibi_slopes[g] * (j - pos), g the query head
+ *   window_left >= 0       key j is visible only if pos - j <= window_left (besides j <= pos)
+ * options NULL, or window_left < 0, softcap 0 and alibi_slopes NULL: exactly
+ * kv_int4_paged_attention.  alibi_slopes: DEVICE fp32 [num_q_heads], 4-byte aligned.
+ * Returns KV_INT4_EINVAL for a negative or non-finite softcap; everything else as
+ * kv_int4_paged_attention (same workspace).  The options are read at the call.
+ */
+typedef struct {
+    int32_t window_left;        /* < 0: no window */
+    float softcap;              /* 0: none */
+    const float* alibi_slopes;  /* NULL: none */
+} kv_int4_attn_options;
+
+kv_int4_status kv_int4_paged_attention_ex(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                          int32_t num_q_heads, const uint8_t* cache,
+                                          int64_t num_blocks, int32_t num_kv_heads,
+                                          int32_t head_size, int32_t block_size,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* seq_lens, const int32_t* query_start_loc,
+                                          int32_t num_seqs, int32_t max_query_len,
+                                          int32_t max_seq_len, float softmax_scale,
+                                          const float* rht_signs, int32_t segment_len, void* out,
+                                          kv_int4_dtype out_dtype, void* workspace,
+                                          size_t workspace_bytes, kv_int4_stream_t stream,
+                                          const kv_int4_attn_options* options);
+
+/*
  * kv_int8_paged_attention -- decode attention over the INT8 comparator's cache (as written by
  * kv_int8_write), the read side of the comparison the pages make between the INT4 mode and INT8
  * per-(token, head) quantisation ("PR #40835 report", summary; "tests/quantization/

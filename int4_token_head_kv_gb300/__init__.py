@@ -22,6 +22,12 @@ _STAT_COUNT = 8
 _DTYPES = {torch.float16: KV_INT4_F16, torch.bfloat16: KV_INT4_BF16, torch.float32: KV_INT4_F32}
 
 
+class AttnOptions(ctypes.Structure):
+    """kv_int4_attn_options: window_left (< 0: none), softcap (0: none), alibi_slopes (device
+    pointer to fp32 [num_q_heads], or None)."""
+    _fields_ = [("window_left", ctypes.c_int32), ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p)]
+
+
 class KVInt4Error(RuntimeError):
     """A non-OK status returned by the C library."""
 
@@ -53,6 +59,8 @@ def _load():
     lib.kv_int4_paged_attention.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp,
                                             i32, i32, i32, f32, vp, i32, vp, ctypes.c_int, vp, szt, vp]
     lib.kv_int4_paged_attention.restype = ctypes.c_int
+    lib.kv_int4_paged_attention_ex.argtypes = lib.kv_int4_paged_attention.argtypes + [ctypes.POINTER(AttnOptions)]
+    lib.kv_int4_paged_attention_ex.restype = ctypes.c_int
     lib.kv_int8_paged_attention.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp,
                                             i32, i32, i32, f32, i32, vp, ctypes.c_int, vp, szt, vp]
     lib.kv_int8_paged_attention.restype = ctypes.c_int
@@ -170,8 +178,11 @@ def kv_int4_attention_workspace_bytes(num_q_heads: int, num_kv_heads: int, head_
 def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,
                             seq_lens: torch.Tensor, query_start_loc: torch.Tensor, softmax_scale: float,
                             rht_signs: torch.Tensor, max_query_len: int, max_seq_len: int, out=None,
-                            out_dtype=None, segment_len: int = 0, workspace=None, stream=None) -> torch.Tensor:
-    """Causal paged attention of ``query`` [Nq, Hq, d] over the INT4 cache; returns ``out``."""
+                            out_dtype=None, segment_len: int = 0, workspace=None, stream=None,
+                            window_left: int = -1, softcap: float = 0.0, alibi_slopes=None) -> torch.Tensor:
+    """Causal paged attention of ``query`` [Nq, Hq, d] over the INT4 cache; returns ``out``.  With
+    ``window_left >= 0``, ``softcap > 0`` or ``alibi_slopes`` (fp32 [Hq] on the device) the call
+    goes through kv_int4_paged_attention_ex."""
     _cuda(query, "query", (torch.float16, torch.bfloat16))
     _cuda(kv_cache, "kv_cache", (torch.uint8,))
     _cuda(block_tables, "block_tables", (torch.int32,))
@@ -195,12 +206,22 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = load().kv_int4_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H,
-                                      d, bs, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
-                                      query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
-                                      float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(),
-                                      _DTYPES[out.dtype], ws_ptr, ws_bytes, _stream(stream))
-    _check("kv_int4_paged_attention", st)
+    args = (query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs, block_tables.data_ptr(),
+            block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
+            float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype], ws_ptr,
+            ws_bytes, _stream(stream))
+    if window_left >= 0 or softcap != 0.0 or alibi_slopes is not None:
+        if alibi_slopes is not None:
+            _cuda(alibi_slopes, "alibi_slopes", (torch.float32,))
+            if alibi_slopes.shape != (Hq,):
+                raise ValueError("alibi_slopes must be [num_q_heads]")
+        opts = AttnOptions(int(window_left), float(softcap),
+                           alibi_slopes.data_ptr() if alibi_slopes is not None else None)
+        st = load().kv_int4_paged_attention_ex(*args, ctypes.byref(opts))
+        _check("kv_int4_paged_attention_ex", st)
+    else:
+        st = load().kv_int4_paged_attention(*args)
+        _check("kv_int4_paged_attention", st)
     return out
 
 

@@ -206,7 +206,7 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
                                        int32_t max_query_len, int32_t max_seq_len, float softmax_scale,
                                        const float* rht_signs, int32_t segment_len, void* out,
                                        kv_int4_dtype out_dtype, void* workspace, size_t workspace_bytes,
-                                       kv_int4_stream_t stream) {
+                                       kv_int4_stream_t stream, const kv_int4_attn_options* options) {
     if (num_q_tokens < 0 || num_seqs < 0 || num_blocks < 0 || max_query_len < 0 || max_seq_len < 0 ||
         max_blocks_per_seq < 0 || segment_len < 0)
         return KV_INT4_EINVAL;
@@ -220,6 +220,7 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
         return KV_INT4_EUNSUPPORTED;
     if (segment_len % kBlockSize != 0 || num_seqs > 65535) return KV_INT4_EUNSUPPORTED;
     if (!(softmax_scale == softmax_scale)) return KV_INT4_EINVAL;
+    if (options && !(options->softcap >= 0.0f && options->softcap <= 3.0e38f)) return KV_INT4_EINVAL;
     if (num_q_tokens == 0 || num_seqs == 0) return KV_INT4_OK;
     if (!q || !cache || !block_tables || !seq_lens || !query_start_loc || (bits == 4 && !rht_signs) || !out)
         return KV_INT4_EINVAL;
@@ -272,6 +273,26 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
     p.len_cap = (int)len_cap;
     p.softmax_scale = softmax_scale;
     p.c = (float)(1.0 / std::sqrt((double)head_size));
+    p.opts = 0;
+    p.window_left = -1;
+    p.cap_l2 = 0.0f;
+    p.inv_cap_l2 = 0.0f;
+    p.alibi = nullptr;
+    if (options) {
+        if (options->window_left >= 0) {
+            p.opts |= kOptWindow;
+            p.window_left = options->window_left;
+        }
+        if (options->softcap > 0.0f) {
+            p.opts |= kOptSoftcap;
+            p.cap_l2 = (float)((double)options->softcap * 1.4426950408889634);
+            p.inv_cap_l2 = 1.0f / p.cap_l2;
+        }
+        if (options->alibi_slopes) {
+            p.opts |= kOptAlibi;
+            p.alibi = options->alibi_slopes;
+        }
+    }
 
     const int64_t max_units = (int64_t)num_seqs * (((int64_t)max_seq_len + seg - 1) / seg);
     // balance weight bound: the blocks, plus at most one padded unit per sequence
@@ -309,7 +330,22 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     return paged_attention_impl(4, q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads, head_size,
                                 block_size, block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
                                 max_query_len, max_seq_len, softmax_scale, rht_signs, segment_len, out, out_dtype,
-                                workspace, workspace_bytes, stream);
+                                workspace, workspace_bytes, stream, nullptr);
+}
+
+kv_int4_status kv_int4_paged_attention_ex(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                          int32_t num_q_heads, const uint8_t* cache, int64_t num_blocks,
+                                          int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                                          int32_t max_query_len, int32_t max_seq_len, float softmax_scale,
+                                          const float* rht_signs, int32_t segment_len, void* out,
+                                          kv_int4_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                          kv_int4_stream_t stream, const kv_int4_attn_options* options) {
+    return paged_attention_impl(4, q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads, head_size,
+                                block_size, block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                max_query_len, max_seq_len, softmax_scale, rht_signs, segment_len, out, out_dtype,
+                                workspace, workspace_bytes, stream, options);
 }
 
 kv_int4_status kv_int8_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
@@ -323,7 +359,7 @@ kv_int4_status kv_int8_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     return paged_attention_impl(8, q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads, head_size,
                                 block_size, block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
                                 max_query_len, max_seq_len, softmax_scale, nullptr, segment_len, out, out_dtype,
-                                workspace, workspace_bytes, stream);
+                                workspace, workspace_bytes, stream, nullptr);
 }
 
 kv_int4_status kv_int4_selftest_wait_timeout(uint64_t timeout_ns, kv_int4_stream_t stream) {

@@ -37,6 +37,20 @@ __device__ __forceinline__ void store_elem<float>(void* base, int64_t i, float x
     static_cast<float*>(base)[i] = x;
 }
 
+// The attention options on one visible key's logit x (log2 units) for a query at position pos and
+// key j: softcap C tanh(x / C) (tanh(y) = 1 - 2 / (e^{2y} + 1)), then the ALiBi bias
+// slope_l2 (j - pos), then the window (-inf when pos - j > window_left).  Masked keys stay -inf.
+__device__ __forceinline__ float apply_opts(float x, int j, int pos, float slope_l2, const AttnParams& p) {
+    if (!(x > -INFINITY)) return x;
+    if (p.opts & kOptSoftcap) {
+        const float e = fast_exp2(2.0f * kLog2e * (x * p.inv_cap_l2));   // e^{2y}, y = x / C
+        x = p.cap_l2 * (1.0f - 2.0f / (e + 1.0f));
+    }
+    if (p.opts & kOptAlibi) x = fmaf(slope_l2, (float)(j - pos), x);
+    if ((p.opts & kOptWindow) && pos - j > p.window_left) x = -INFINITY;
+    return x;
+}
+
 // Walsh-Hadamard transform (unnormalised, natural order) of a D-vector spread over a warp:
 // lane l holds x[k] = v[l + 32 k].  Strides below 32 pair lanes, larger strides pair slots.
 template <int D>

@@ -270,7 +270,9 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
 
 // ------------------------------------------------------------------ 1. split-KV unit walker
 
-template <int D, bool WIDE, int BITS>
+// OPTS: the call has window / softcap / ALiBi options (a separate instantiation, so that the plain
+// path carries none of their registers)
+template <int D, bool WIDE, int BITS, bool OPTS>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_constant__ AttnParams p) {
     using Gm = Geo<D>;
     using Rw = RowGeo<D, BITS>;
@@ -541,6 +543,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     uint32_t qb[Gm::KSTEPS][WIDE ? 4 : 2];
     float al0 = 0.0f, al1 = 0.0f;     // logit factor of heads hb, hb + 1
     float qs0 = 0.0f, qs1 = 0.0f;     // sum(Q') of those heads (high + low halves as stored)
+    float sl0 = 0.0f, sl1 = 0.0f;     // their ALiBi slopes in log2 units
     float WZ0 = 0.0f, WZ1 = 0.0f;     // sum(w zp) per head
     int run = -1, prev_seq = -1;
     bool stop = false;
@@ -582,6 +585,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             al1 = (WIDE && hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
             qs0 = (hb < G) ? qsum[h * G + hb] : 0.0f;
             qs1 = (WIDE && hb + 1 < G) ? qsum[h * G + hb + 1] : 0.0f;
+            if constexpr (OPTS) {
+                const bool alibi = (p.opts & kOptAlibi) != 0;
+                sl0 = alibi && hb < G ? __ldg(p.alibi + h * G + hb) * kLog2e : 0.0f;
+                sl1 = alibi && WIDE && hb + 1 < G ? __ldg(p.alibi + h * G + hb + 1) * kLog2e : 0.0f;
+            }
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();   // this warp's reads of the buffer come before the count
@@ -603,6 +611,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         WZ0 = WZ1 = 0.0f;
         eref = 0;
         const int li0 = ustart[j] - Bs;
+        // the decode query's position (the staged metadata is gone: the ring has overwritten it)
+        const int posd = OPTS ? min(__ldg(p.seq_lens + u.x), p.len_cap) - 1 : 0;
         const int nbu = (u.w + kBlockSize - 1) / kBlockSize;
 
         // Two blocks (32 tokens) per iteration: their score chains, one softmax update and their
@@ -687,6 +697,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         x[b][0] = v0 ? fmaf(-zk0, qs0, c[0] + c[1]) * sk0 * al0 : -INFINITY;
                         x[b][2] = v1 ? fmaf(-zk1, qs0, c[2] + c[3]) * sk1 * al0 : -INFINITY;
                         x[b][1] = x[b][3] = -INFINITY;
+                    }
+                    if constexpr (OPTS) {   // window / softcap / ALiBi
+                        const int jb = u.y * kBlockSize + tb;   // position of this block's first token
+                        x[b][0] = apply_opts(x[b][0], jb + tk0, posd, sl0, p);
+                        x[b][2] = apply_opts(x[b][2], jb + tk1, posd, sl0, p);
+                        if constexpr (WIDE) {
+                            x[b][1] = apply_opts(x[b][1], jb + tk0, posd, sl1, p);
+                            x[b][3] = apply_opts(x[b][3], jb + tk1, posd, sl1, p);
+                        }
                     }
                     const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp[b] + (tk0 * H + h) * Rw::RB);
                     const uint32_t* vg1 = reinterpret_cast<const uint32_t*>(vp[b] + (tk1 * H + h) * Rw::RB);
@@ -1081,7 +1100,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
 template <int D, bool WIDE, int BITS, typename QT, typename OT>
 cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stream) {
     const DecodeSmem lay = decode_smem_layout<D, WIDE, BITS>(p.H, p.Hq);
-    cudaError_t err = opt_in_smem<decode_kernel<D, WIDE, BITS>>(lay.total);
+    const bool opts = BITS == 4 && p.opts != 0;
+    auto walker = opts ? decode_kernel<D, WIDE, BITS, BITS == 4> : decode_kernel<D, WIDE, BITS, false>;
+    cudaError_t err = opts ? opt_in_smem<decode_kernel<D, WIDE, BITS, BITS == 4>>(lay.total)
+                           : opt_in_smem<decode_kernel<D, WIDE, BITS, false>>(lay.total);
     if (err != cudaSuccess) return err;
     // All three kernels are programmatic dependents of their predecessor: each starts its set-up
     // while the previous kernel finishes and waits for it (griddep_wait) before touching its
@@ -1106,7 +1128,7 @@ cudaError_t launch_decode_t(const AttnParams& p, int num_ctas, cudaStream_t stre
     wcfg.stream = stream;
     wcfg.attrs = &attr;
     wcfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&wcfg, decode_kernel<D, WIDE, BITS>, p);
+    err = cudaLaunchKernelEx(&wcfg, walker, p);
     if (err != cudaSuccess) return err;
 
     const int W = p.combine_warps;

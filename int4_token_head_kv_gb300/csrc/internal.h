@@ -59,7 +59,16 @@ struct AttnParams {
     int wph_shift;            // log2(8 / H): consumer warps per kv head
     float softmax_scale;
     float c;                  // fp32(1 / sqrt(head_size))
+    // options of the unified-attention interface, on the scaled logit s of key j at query position
+    // pos, in log2 units (x = s log2 e): x <- C tanh(x / C), x <- x + slope log2e (j - pos), key
+    // visible only if pos - j <= window_left
+    int opts;                 // kOptWindow | kOptSoftcap | kOptAlibi
+    int window_left;
+    float cap_l2;             // C = softcap log2 e
+    float inv_cap_l2;         // 1 / C
+    const float* alibi;       // [Hq] slopes (natural-log units)
 };
+constexpr int kOptWindow = 1, kOptSoftcap = 2, kOptAlibi = 4;
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
@@ -86,6 +95,9 @@ inline constexpr uint32_t decode_po_floats(int D, int G) { return (uint32_t)(D /
 
 cudaError_t launch_prefill(const AttnParams& p, int head_size, int max_query_len, DType q_dt, DType out_dt,
                            cudaStream_t stream);
+// The prefill kernel instantiated with the logit options (p.opts != 0); launch_prefill calls it.
+cudaError_t launch_prefill_opts(const AttnParams& p, int head_size, int max_query_len, DType q_dt, DType out_dt,
+                                cudaStream_t stream);
 
 int num_sms();
 

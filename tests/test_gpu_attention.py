@@ -247,3 +247,62 @@ def test_contexts_longer_than_max_seq_len_are_clamped_alike():
     ref_cache = oracle_cache(wl)
     wl.seq_lens = np.minimum(wl.seq_lens, cap).astype(np.int32)
     assert_attention_close(out, oracle_attention(wl, ref_cache), "clamped contexts")
+
+
+# ------------------------------------------------------------------- window / softcap / ALiBi options
+# kv_int4_paged_attention_ex against the oracle's definition of the same options (decode split-KV
+# walker and prefill kernel alike; several segments per sequence so the options meet the combine).
+
+def _run_opts(wl, window_left=-1, softcap=0.0, slopes=None, segment_len=None):
+    import int4_token_head_kv_gb300 as kv
+    from gpu_helpers import assert_attention_close, dev, gpu_cache, gpu_write, oracle_cache, status
+    cache = gpu_cache(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_size)
+    gpu_write(wl.key, wl.value, wl.slot_mapping, wl.signs, cache)
+    seg = wl.segment_len if segment_len is None else segment_len
+    out = kv.kv_int4_paged_attention(
+        wl.query.to(dev()), cache, torch.from_numpy(wl.block_tables).to(dev()),
+        torch.from_numpy(wl.seq_lens).to(dev()), torch.from_numpy(wl.query_start_loc).to(dev()),
+        wl.softmax_scale, torch.from_numpy(wl.signs).to(dev()), max_query_len=wl.max_query_len,
+        max_seq_len=wl.max_seq_len, out_dtype=torch.float32, segment_len=seg, window_left=window_left,
+        softcap=softcap, alibi_slopes=None if slopes is None else torch.tensor(slopes, dtype=torch.float32,
+                                                                                 device=dev()))
+    torch.cuda.synchronize()
+    import oracle
+    ref = oracle.paged_attention(wl.query, oracle_cache(wl), wl.block_tables, wl.seq_lens, wl.query_start_loc,
+                                 wl.softmax_scale, wl.signs, window_left=window_left, softcap=softcap,
+                                 alibi_slopes=slopes)
+    assert_attention_close(out, ref, wl.name + " (options)")
+    st = status()
+    assert not any(st.values()), st
+
+
+def _opts_workload(G, seed):
+    # decode contexts across segment edges and two prefill chunks (a diagonal and a full tile)
+    return workloads.make_attention_workload("opts", [700, 33, 1, 2100, 300, 1500], [1, 1, 1, 1, 160, 200],
+                                             8 * G, 8, 128, seed=seed, segment_len=256)
+
+
+@pytest.mark.parametrize("G", [4, 8])
+@pytest.mark.parametrize("window", [0, 37, 1000])
+def test_sliding_window(G, window):
+    _run_opts(_opts_workload(G, 31), window_left=window)
+
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_softcap(G):
+    wl = _opts_workload(G, 32)
+    wl.query = (wl.query.float() * 6.0).to(wl.query.dtype)   # logits large enough for the cap to bite
+    _run_opts(wl, softcap=5.0)
+
+
+@pytest.mark.parametrize("G", [1, 8])
+def test_alibi(G):
+    wl = _opts_workload(G, 33)
+    slopes = [2.0 ** (-(i % 8) - 1) for i in range(8 * G)]
+    _run_opts(wl, slopes=slopes)
+
+
+def test_options_together():
+    wl = _opts_workload(4, 34)
+    wl.query = (wl.query.float() * 4.0).to(wl.query.dtype)
+    _run_opts(wl, window_left=150, softcap=8.0, slopes=[0.03 * (i + 1) for i in range(32)])
