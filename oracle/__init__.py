@@ -209,14 +209,16 @@ def gather_rows(cache: np.ndarray, block_table_row: np.ndarray, seq_len: int, pl
 
 
 def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softmax_scale, signs,
-                    seqs=None, kv_heads=None, window_left=-1, softcap=0.0, alibi_slopes=None) -> np.ndarray:
+                    seqs=None, kv_heads=None, window_left=-1, softcap=0.0, alibi_slopes=None,
+                    row_decoder=None) -> np.ndarray:
     """Causal softmax attention over the dequantised, un-rotated paged cache, in fp64.
 
     query [Nq, Hq, d] (original domain); sequence b owns query rows
     query_start_loc[b] .. query_start_loc[b+1]-1, and its t-th query sits at position
     seq_len[b] - q_len[b] + t, seeing keys 0 .. that position.  Query head g reads kv head
     g // (Hq / H).  Returns fp64 [Nq, Hq, d]; rows of sequences or kv heads that are not selected
-    (``seqs`` / ``kv_heads``) are NaN.  An empty key range gives a zero output.
+    (``seqs`` / ``kv_heads``) are NaN.  An empty key range gives a zero output.  ``row_decoder``
+    (rows, signs) -> original-domain vectors reads another row format (default: the INT4 rows).
 
     Options of the unified-attention interface ("tests/quantization/test_per_token_kv_cache.py",
     ``window_size`` and ``softcap`` arguments; the PR #40633 description lists sliding window,
@@ -233,6 +235,7 @@ def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softm
     out = np.full((nq, hq, d), np.nan, dtype=np.float64)
     seqs = range(len(seq_lens)) if seqs is None else seqs
     kv_heads = range(H) if kv_heads is None else kv_heads
+    dec = decode_rows if row_decoder is None else row_decoder
     for b in seqs:
         L = int(seq_lens[b])
         q0, q1 = int(query_start_loc[b]), int(query_start_loc[b + 1])
@@ -240,8 +243,8 @@ def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softm
         if qlen == 0:
             continue
         for h in kv_heads:
-            khat = decode_rows(gather_rows(cache, block_tables[b], L, 0, h), signs)
-            vhat = decode_rows(gather_rows(cache, block_tables[b], L, 1, h), signs)
+            khat = dec(gather_rows(cache, block_tables[b], L, 0, h), signs)
+            vhat = dec(gather_rows(cache, block_tables[b], L, 1, h), signs)
             for t in range(qlen):
                 pos = L - qlen + t
                 nkeys = max(0, min(pos + 1, L))
