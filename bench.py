@@ -24,7 +24,8 @@ Sub-objects (each with its own roofline): ``gqa_decode_batch`` (32 sequences, le
 8 kv heads), ``mixed_prefill_decode`` (4 prefill chunks of 2048 queries over 4096 keys + 60 decode
 sequences: whole-call HBM fraction and the prefill part's dense-equivalent TFLOP/s against the
 measured bf16 tensor peak), ``int8_comparator`` (the INT8 per-(token, head) cache write on the
-write workload).
+write workload, and INT4 vs INT8 decode on the long-context workload), ``int2_lloyd_max`` (the INT2
+mode's write and long-context decode, timed the same way).
 
 Runs as N independent replicas under torchrun (the path does not shard across GPUs; no collective on
 the data path); ``--gpus N`` without torchrun starts the N local ranks itself.  ``--impl reference``
@@ -388,6 +389,7 @@ def _gpu_arm(args):
         result["mixed_prefill_decode"] = _mixed_bench(torch, kv, workloads, dev, args, hbm, bf16, kind)
         result["int8_comparator"] = _int8_write_bench(torch, kv, workloads, dev, args, hbm)
         result["int8_comparator"]["decode"] = _int8_decode_bench(torch, kv, workloads, dev, args, hbm)
+        result["int2_lloyd_max"] = _int2_bench(torch, kv, workloads, dev, args, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = _cpu_baseline(args)
     if world > 1:
@@ -438,7 +440,8 @@ def _write_bench(torch, kv, workloads, dev, args, hbm, kind):
 def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=None, bits=4):
     """Write every token of ``wl`` (untimed), then time ``reps`` back-to-back attention calls captured in
     one CUDA graph, over the whole batch or over the sequences ``sub`` (same cache).  Returns ms per call
-    and the segment length.  bits=8: the INT8 comparator's cache and decode call instead."""
+    and the segment length.  bits=8 / 2: the INT8 comparator's or the INT2 mode's cache and decode call
+    instead."""
     H, d = wl.num_kv_heads, wl.head_size
     signs = torch.from_numpy(wl.signs).to(dev)
     import numpy as np
@@ -447,12 +450,14 @@ def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=Non
         _write_history(torch, kv, wl, dev, signs, cache, np.arange(wl.key.shape[0]))
         row_bytes = kv.kv_int4_row_bytes(d)
     else:
-        cache = torch.zeros(kv.kv_int8_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+        shape, write, row_bytes = ((kv.kv_int8_cache_shape, kv.kv_int8_write, kv.kv_int8_row_bytes(d)) if bits == 8
+                                   else (kv.kv_int2_cache_shape, kv.kv_int2_write, kv.kv_int2_row_bytes(d)))
+        cache = torch.zeros(shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
         step = 1 << 18
         for r0 in range(0, wl.key.shape[0], step):
-            kv.kv_int8_write(wl.key[r0:r0 + step].to(dev), wl.value[r0:r0 + step].to(dev),
-                             torch.from_numpy(wl.slot_mapping[r0:r0 + step]).to(dev), cache)
-        row_bytes = kv.kv_int8_row_bytes(d)
+            extra = () if bits == 8 else (signs,)
+            write(wl.key[r0:r0 + step].to(dev), wl.value[r0:r0 + step].to(dev),
+                  torch.from_numpy(wl.slot_mapping[r0:r0 + step]).to(dev), *extra, cache)
     results = {}
     for name, seqs in (sub or {"all": None}).items():
         if seqs is None:
@@ -473,8 +478,11 @@ def _attention_calls(torch, kv, wl, dev, reps, rows=None, segment_len=0, sub=Non
             if bits == 4:
                 kv.kv_int4_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, signs, max_query_len=max_q,
                                            max_seq_len=max_len, out=out, segment_len=seg, workspace=ws)
-            else:
+            elif bits == 8:
                 kv.kv_int8_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, max_query_len=max_q,
+                                           max_seq_len=max_len, out=out, segment_len=seg, workspace=ws)
+            else:
+                kv.kv_int2_paged_attention(q, cache, tables, lens, qsl, wl.softmax_scale, signs, max_query_len=max_q,
                                            max_seq_len=max_len, out=out, segment_len=seg, workspace=ws)
         for _ in range(3):
             call()
@@ -565,6 +573,40 @@ def _int8_decode_bench(torch, kv, workloads, dev, args, hbm):
     res["int8_over_int4_time"] = round(res["int8"]["ms_per_call"] / res["int4"]["ms_per_call"], 3)
     res["int4_kv_bytes_saving_vs_int8"] = round(1 - res["int4"]["kv_bytes_per_token_per_layer"] /
                                                 res["int8"]["kv_bytes_per_token_per_layer"], 4)
+    return res
+
+
+def _int2_bench(torch, kv, workloads, dev, args, hbm):
+    """The INT2 Lloyd-Max mode: its write on the write-throughput workload and its decode attention on
+    the long-context workload, timed as the INT4 and INT8 figures are."""
+    wl = workloads.write_throughput(seed=args.seed)
+    H, d = wl.num_kv_heads, wl.head_size
+    k, v = wl.key.to(dev), wl.value.to(dev)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    signs = torch.from_numpy(wl.signs).to(dev)
+    cache = torch.zeros(kv.kv_int2_cache_shape(wl.num_blocks, 16, H, d), dtype=torch.uint8, device=dev)
+    nbytes = wl.num_tokens * (2 * H * d * k.element_size() + 2 * H * kv.kv_int2_row_bytes(d) + 8)
+    reps = max(50, min(2000, args.steps))
+    for _ in range(5):
+        kv.kv_int2_write(k, v, slots, signs, cache)
+    ms = _timed(torch, torch.cuda.current_stream(), lambda i: kv.kv_int2_write(k, v, slots, signs, cache), reps) / reps
+    gbs = _gbs(nbytes, ms)
+    res = {"write": {"tokens_per_s": round(wl.num_tokens / (ms * 1e-3), 1), "GB/s": round(gbs, 1),
+                     "frac": round(gbs / hbm, 4), "ms_per_call": round(ms, 5), "bytes_per_call": nbytes,
+                     "workload": "write_throughput: 65536 tokens, 8 kv heads, head 128, bf16"},
+           "cache_bytes_per_token": 2 * H * kv.kv_int2_row_bytes(d)}
+    del k, v, cache
+    wl = workloads.long_context_decode(seed=args.seed)
+    reps = 50
+    r = _attention_calls(torch, kv, wl, dev, reps=reps, segment_len=args.segment_len, bits=2)["all"]
+    gbs = _gbs(r["bytes"], r["ms"])
+    res["decode"] = {"ms_per_call": round(r["ms"], 5), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                     "decode_tokens_per_s": round(len(wl.seq_lens) / (r["ms"] * 1e-3), 1),
+                     "context_tokens_per_s": round(float(wl.seq_lens.sum()) / (r["ms"] * 1e-3), 1),
+                     "kv_bytes_per_token_per_layer": 2 * wl.num_kv_heads * kv.kv_int2_row_bytes(wl.head_size),
+                     "segment_len": r["seg"],
+                     "workload": "long_context_decode: 8 seqs x 131072 tokens, 64 q / 8 kv heads, head 128; one "
+                                 "decode attention call per step, graph-replayed %d times back to back" % reps}
     return res
 
 

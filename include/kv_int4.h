@@ -1,13 +1,16 @@
 /*
  * kv_int4.h -- C ABI of the INT4 per-(token, head) KV-cache library for NVIDIA GB300 (sm_103a).
  *
- * Two operations, both asynchronous on the caller's CUDA stream, and the INT8 comparator's pair:
+ * Two operations, both asynchronous on the caller's CUDA stream, and the pairs of the INT8
+ * comparator and of the INT2 Lloyd-Max mode:
  *
  *   kv_int4_write            rotate, quantise and pack new K/V head vectors into a paged cache;
  *   kv_int4_paged_attention  causal attention of queries over that cache (decode, split-KV
  *                            segments, chunked prefill);
  *   kv_int8_write            the INT8 per-(token, head) comparator's cache write;
- *   kv_int8_paged_attention  decode attention over the INT8 comparator's cache.
+ *   kv_int8_paged_attention  decode attention over the INT8 comparator's cache;
+ *   kv_int2_write            the INT2 per-(token, head) Lloyd-Max cache write;
+ *   kv_int2_paged_attention  decode attention over the INT2 cache.
  *
  * The caller owns every buffer.  The library never allocates device or host memory: the
  * attention's split-KV partials live in a caller-provided workspace whose size
@@ -125,6 +128,35 @@ kv_int4_status kv_int8_write(const void* k, const void* v, kv_int4_dtype dtype, 
                              int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
                              uint8_t* cache, int64_t num_blocks, int32_t block_size,
                              kv_int4_stream_t stream);
+
+/*
+ * INT2 Lloyd-Max rows: head_size / 4 code bytes (four 2-bit codes each), then the fp32 scale word
+ * (head_size / 4 + 4 bytes).
+ */
+int32_t kv_int2_row_bytes(int32_t head_size);
+
+/*
+ * kv_int2_write -- the INT2 per-(token, head) cache write ("[Feature] Triton INT4 / INT2
+ * per-token-head KV cache quantization", description: four 2-bit values per byte, Hadamard
+ * pre-rotation over the head dimension, dequantisation by a lookup of one of 4 Lloyd-Max centroids
+ * fitted over N(0, 1)).  The page fixes neither the centroids nor the scale; this library takes:
+ *   y = c * H_d * (D x) exactly as kv_int4_write (same rht_signs, same fp32 butterfly order);
+ *   sigma = max(fp32 sqrt(fp32(sum y_i^2) / d), 1e-6), the fp32 squares summed by folding the
+ *     vector in halves (a_i + a_{i + d/2}, then + a_{i + d/4}, ..., then a_0 + a_1);
+ *   r = fp32(1 / sigma); z_i = fp32(y_i * r);
+ *   code_i = [z_i >= -t] + [z_i >= 0] + [z_i >= t], standing for -b, -a, a, b, where a = 0.45278,
+ *     b = 1.51042, t = (a + b) / 2 = 0.98160 are the outputs and threshold of the 4-level
+ *     Lloyd-Max quantiser of N(0, 1) (J. Max, 1960), each rounded to fp32;
+ * stored as head_size / 4 bytes (element 4j + k in bits 2k, 2k + 1 of byte j) then the
+ * little-endian bits of sigma, at cache[slot / 16][plane][slot % 16][head] of a
+ * (num_blocks, 2, 16, num_kv_heads, head_size / 4 + 4) uint8 cache.  A reader reconstructs
+ * y_hat_i = sigma * centroid(code_i) and x_hat = the inverse rotation of y_hat.  Arguments,
+ * validation, skipped slots and error behaviour as kv_int4_write.
+ */
+kv_int4_status kv_int2_write(const void* k, const void* v, kv_int4_dtype dtype, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
+                             const float* rht_signs, uint8_t* cache, int64_t num_blocks,
+                             int32_t block_size, kv_int4_stream_t stream);
 
 /*
  * Bytes of workspace kv_int4_paged_attention needs for these sizes (same arguments as the
@@ -252,6 +284,31 @@ kv_int4_status kv_int8_paged_attention(const void* q, kv_int4_dtype q_dtype, int
                                        int32_t segment_len, void* out, kv_int4_dtype out_dtype,
                                        void* workspace, size_t workspace_bytes,
                                        kv_int4_stream_t stream);
+
+/*
+ * kv_int2_paged_attention -- decode attention over the INT2 Lloyd-Max cache (as written by
+ * kv_int2_write with the same rht_signs).  Every sequence must have exactly one query token
+ * (max_query_len 1; a larger value returns KV_INT4_EUNSUPPORTED and launches nothing).  With x_K,
+ * x_V the cached rows decoded as the inverse rotation of sigma * centroid(code),
+ * out = softmax(softmax_scale * q . x_K) x_V.  The computation is the decode path of
+ * kv_int4_paged_attention with INT2 rows: the query rotated as for INT4, the scores and P.V taken
+ * on the rotated codes through the centroid table (held as fp16: 0.45288 and 1.5107, a relative
+ * error of at most 2.3e-4 per centroid), the output un-rotated; the same split-KV segments,
+ * segment-length rule, workspace size (kv_int4_attention_workspace_bytes with these arguments),
+ * partials and combine.  Arguments, alignment, supported sizes, clamping and error behaviour as
+ * kv_int4_paged_attention.
+ */
+kv_int4_status kv_int2_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                       int32_t num_q_heads, const uint8_t* cache,
+                                       int64_t num_blocks, int32_t num_kv_heads,
+                                       int32_t head_size, int32_t block_size,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, const int32_t* query_start_loc,
+                                       int32_t num_seqs, int32_t max_query_len,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       const float* rht_signs, int32_t segment_len, void* out,
+                                       kv_int4_dtype out_dtype, void* workspace,
+                                       size_t workspace_bytes, kv_int4_stream_t stream);
 
 /*
  * kv_int4_paged_attention_noalloc -- the same attention for callers that cannot allocate device

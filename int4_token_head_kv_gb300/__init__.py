@@ -52,6 +52,10 @@ def _load():
     lib.kv_int8_row_bytes.restype = i32
     lib.kv_int8_write.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, vp, i64, i32, vp]
     lib.kv_int8_write.restype = ctypes.c_int
+    lib.kv_int2_row_bytes.argtypes = [i32]
+    lib.kv_int2_row_bytes.restype = i32
+    lib.kv_int2_write.argtypes = lib.kv_int4_write.argtypes
+    lib.kv_int2_write.restype = ctypes.c_int
     lib.kv_int4_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.kv_int4_attention_workspace_bytes.restype = szt
     lib.kv_int4_attention_segment_len.argtypes = [i32, i32, i32]
@@ -64,6 +68,8 @@ def _load():
     lib.kv_int8_paged_attention.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp,
                                             i32, i32, i32, f32, i32, vp, ctypes.c_int, vp, szt, vp]
     lib.kv_int8_paged_attention.restype = ctypes.c_int
+    lib.kv_int2_paged_attention.argtypes = lib.kv_int4_paged_attention.argtypes
+    lib.kv_int2_paged_attention.restype = ctypes.c_int
     lib.kv_int4_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
     lib.kv_int4_read_device_status.restype = ctypes.c_int
     lib.kv_int4_clear_device_status.argtypes = [vp]
@@ -117,6 +123,10 @@ def kv_int4_cache_shape(num_blocks: int, block_size: int, num_kv_heads: int, hea
 def kv_int4_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor, rht_signs: torch.Tensor,
                   kv_cache: torch.Tensor, stream=None) -> None:
     """Rotate, quantise and pack ``key``/``value`` [T, H, d] into ``kv_cache`` at ``slot_mapping``."""
+    _rotated_write("kv_int4_write", kv_int4_row_bytes, key, value, slot_mapping, rht_signs, kv_cache, stream)
+
+
+def _rotated_write(fn, row_bytes, key, value, slot_mapping, rht_signs, kv_cache, stream):
     _cuda(key, "key", (torch.float16, torch.bfloat16))
     _cuda(value, "value", (key.dtype,))
     _cuda(slot_mapping, "slot_mapping", (torch.int64,))
@@ -128,12 +138,12 @@ def kv_int4_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Te
     if slot_mapping.shape != (T,) or rht_signs.shape != (d,):
         raise ValueError("slot_mapping must be [num_tokens] and rht_signs [head_size]")
     if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.shape[3] != H or \
-            kv_cache.shape[4] != kv_int4_row_bytes(d):
-        raise ValueError(f"kv_cache must be {kv_int4_cache_shape('NB', 'bs', H, d)}")
-    st = load().kv_int4_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
-                            rht_signs.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2],
-                            _stream(stream))
-    _check("kv_int4_write", st)
+            kv_cache.shape[4] != row_bytes(d):
+        raise ValueError(f"kv_cache must be (NB, 2, bs, {H}, {row_bytes(d)})")
+    st = getattr(load(), fn)(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
+                             rht_signs.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2],
+                             _stream(stream))
+    _check(fn, st)
 
 
 def kv_int8_row_bytes(head_size: int) -> int:
@@ -163,6 +173,22 @@ def kv_int8_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Te
     st = load().kv_int8_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
                             kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], _stream(stream))
     _check("kv_int8_write", st)
+
+
+def kv_int2_row_bytes(head_size: int) -> int:
+    return int(load().kv_int2_row_bytes(head_size))
+
+
+def kv_int2_cache_shape(num_blocks: int, block_size: int, num_kv_heads: int, head_size: int):
+    """INT2 Lloyd-Max cache: (num_blocks, 2, block_size, H, head_size/4 + 4) uint8."""
+    return (num_blocks, 2, block_size, num_kv_heads, kv_int2_row_bytes(head_size))
+
+
+def kv_int2_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor, rht_signs: torch.Tensor,
+                  kv_cache: torch.Tensor, stream=None) -> None:
+    """Rotate ``key``/``value`` [T, H, d] as kv_int4_write does, quantise them to INT2 Lloyd-Max codes
+    and pack them into ``kv_cache`` at ``slot_mapping``."""
+    _rotated_write("kv_int2_write", kv_int2_row_bytes, key, value, slot_mapping, rht_signs, kv_cache, stream)
 
 
 def kv_int4_attention_segment_len(num_seqs: int, max_seq_len: int, segment_len: int = 0) -> int:
@@ -259,6 +285,44 @@ def kv_int8_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
                                       float(softmax_scale), segment_len, out.data_ptr(), _DTYPES[out.dtype], ws_ptr,
                                       ws_bytes, _stream(stream))
     _check("kv_int8_paged_attention", st)
+    return out
+
+
+def kv_int2_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,
+                            seq_lens: torch.Tensor, query_start_loc: torch.Tensor, softmax_scale: float,
+                            rht_signs: torch.Tensor, max_query_len: int, max_seq_len: int, out=None,
+                            out_dtype=None, segment_len: int = 0, workspace=None, stream=None) -> torch.Tensor:
+    """Decode attention of ``query`` [Nq, Hq, d] (one query token per sequence) over the INT2
+    Lloyd-Max cache; returns ``out``.  The workspace size is the INT4 call's."""
+    _cuda(query, "query", (torch.float16, torch.bfloat16))
+    _cuda(kv_cache, "kv_cache", (torch.uint8,))
+    _cuda(block_tables, "block_tables", (torch.int32,))
+    _cuda(seq_lens, "seq_lens", (torch.int32,))
+    _cuda(query_start_loc, "query_start_loc", (torch.int32,))
+    _cuda(rht_signs, "rht_signs", (torch.float32,))
+    Nq, Hq, d = query.shape
+    NB, two, bs, H, rb = kv_cache.shape
+    S = seq_lens.shape[0]
+    if two != 2 or rb != kv_int2_row_bytes(d) or rht_signs.shape != (d,):
+        raise ValueError("kv_cache / rht_signs do not match the query's head size")
+    if query_start_loc.shape != (S + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and query_start_loc [num_seqs + 1]")
+    if out is None:
+        out = torch.empty((Nq, Hq, d), dtype=out_dtype or query.dtype, device=query.device)
+    _cuda(out, "out", tuple(_DTYPES))
+    if out.shape != query.shape:
+        raise ValueError("out must have the query's shape")
+    need = kv_int4_attention_workspace_bytes(Hq, H, d, S, max_seq_len, segment_len)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kv_int2_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H,
+                                      d, bs, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+                                      query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
+                                      float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(),
+                                      _DTYPES[out.dtype], ws_ptr, ws_bytes, _stream(stream))
+    _check("kv_int2_paged_attention", st)
     return out
 
 

@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libkv_int4.so")
-SOURCES = ["abi.cu", "write.cu", "attn_decode.cu", "attn_prefill.cu", "attn_prefill_opts.cu", "noalloc.cu"]
-HEADERS = ["device.cuh", "attn_common.cuh", "attn_prefill.cuh", "internal.h"]
+SOURCES = ["abi.cu", "write.cu", "attn_decode.cu", "attn_decode_int8.cu", "attn_decode_int2.cu", "attn_prefill.cu", "attn_prefill_opts.cu", "noalloc.cu"]
+HEADERS = ["device.cuh", "attn_common.cuh", "attn_decode.cuh", "attn_prefill.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]

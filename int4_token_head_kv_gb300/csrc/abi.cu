@@ -150,6 +150,34 @@ kv_int4_status kv_int8_write(const void* k, const void* v, kv_int4_dtype dtype, 
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int32_t kv_int2_row_bytes(int32_t head_size) { return head_size > 0 ? head_size / 4 + 4 : 0; }
+
+kv_int4_status kv_int2_write(const void* k, const void* v, kv_int4_dtype dtype, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
+                             const float* rht_signs, uint8_t* cache, int64_t num_blocks, int32_t block_size,
+                             kv_int4_stream_t stream) {
+    if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0) return KV_INT4_EINVAL;
+    if (head_size != 64 && head_size != 128) return KV_INT4_EUNSUPPORTED;
+    if (block_size != kBlockSize || num_kv_heads > 64 || !valid_dtype_16(dtype)) return KV_INT4_EUNSUPPORTED;
+    if (num_tokens == 0) return KV_INT4_OK;
+    if (num_tokens * num_kv_heads * 2 >= (int64_t)1 << 31) return KV_INT4_EUNSUPPORTED;   // 32-bit vector index
+    if (!k || !v || !slot_mapping || !rht_signs || !cache) return KV_INT4_EINVAL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(cache)) return KV_INT4_EALIGN;
+    WriteParams p;
+    p.k = k;
+    p.v = v;
+    p.slots = slot_mapping;
+    p.signs = rht_signs;
+    p.cache = cache;
+    p.status = status_ptr();
+    p.num_tokens = num_tokens;
+    p.num_slots = num_blocks * block_size;
+    p.H = num_kv_heads;
+    p.c = (float)(1.0 / std::sqrt((double)head_size));
+    return from_cuda(launch_write_int2(p, head_size, dtype == KV_INT4_BF16 ? DType::BF16 : DType::F16,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int32_t kv_int4_attention_segment_len(int32_t num_seqs, int32_t max_seq_len, int32_t segment_len) {
     if (num_seqs < 0 || max_seq_len < 0 || segment_len < 0) return 0;
     if (segment_len > 0) return (segment_len % kBlockSize == 0) ? segment_len : 0;
@@ -222,9 +250,9 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
     if (!(softmax_scale == softmax_scale)) return KV_INT4_EINVAL;
     if (options && !(options->softcap >= 0.0f && options->softcap <= 3.0e38f)) return KV_INT4_EINVAL;
     if (num_q_tokens == 0 || num_seqs == 0) return KV_INT4_OK;
-    if (!q || !cache || !block_tables || !seq_lens || !query_start_loc || (bits == 4 && !rht_signs) || !out)
+    if (!q || !cache || !block_tables || !seq_lens || !query_start_loc || (bits != 8 && !rht_signs) || !out)
         return KV_INT4_EINVAL;
-    if (bits == 8 && max_query_len > 1) return KV_INT4_EUNSUPPORTED;   // the INT8 comparator decodes only
+    if (bits != 4 && max_query_len > 1) return KV_INT4_EUNSUPPORTED;   // the INT8 and INT2 modes decode only
     if (max_query_len < 1 || max_blocks_per_seq < 1) return KV_INT4_EINVAL;
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache)) return KV_INT4_EALIGN;
 
@@ -359,6 +387,21 @@ kv_int4_status kv_int8_paged_attention(const void* q, kv_int4_dtype q_dtype, int
     return paged_attention_impl(8, q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads, head_size,
                                 block_size, block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
                                 max_query_len, max_seq_len, softmax_scale, nullptr, segment_len, out, out_dtype,
+                                workspace, workspace_bytes, stream, nullptr);
+}
+
+kv_int4_status kv_int2_paged_attention(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                       int32_t num_q_heads, const uint8_t* cache, int64_t num_blocks,
+                                       int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                                       int32_t max_query_len, int32_t max_seq_len, float softmax_scale,
+                                       const float* rht_signs, int32_t segment_len, void* out,
+                                       kv_int4_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                       kv_int4_stream_t stream) {
+    return paged_attention_impl(2, q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads, head_size,
+                                block_size, block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                max_query_len, max_seq_len, softmax_scale, rht_signs, segment_len, out, out_dtype,
                                 workspace, workspace_bytes, stream, nullptr);
 }
 

@@ -308,6 +308,36 @@ __device__ __forceinline__ void unpack_i8_pair(uint32_t a0, uint32_t a1, uint32_
     }
 }
 
+// ----------------------------------------------------------------------- int2 centroid lookup
+// The INT2 mode's Lloyd-Max outputs -b, -a, a, b of N(0, 1) (codes 0..3; a = 0.45278, b = 1.51042,
+// J. Max 1960) as fp16 (0x3E0B = 1.5107, 0x373F = 0.45288), laid out as a byte table for prmt: code
+// c sits at bytes 2c, 2c + 1 of (kU2Lo, kU2Hi).
+constexpr uint32_t kU2Lo = 0xB73FBE0Bu;   // (-b, -a)
+constexpr uint32_t kU2Hi = 0x3E0B373Fu;   // (a, b)
+
+// The codes at bits 0-1 and 8-9 of v (other bits ignored) -> their centroids as an fp16 pair.  The
+// selector's nibbles are 2c0, 2c0 + 1, 2c1, 2c1 + 1: (c0 | c1 << 8) * 0x22 + 0x1010.
+__device__ __forceinline__ uint32_t u2_lookup(uint32_t v) {
+    return prmt(kU2Lo, kU2Hi, (v & 0x0303u) * 0x22u + 0x1010u);
+}
+
+// The 8 codes of a 16-bit group h (dims 0..3 in byte 0, 4..7 in byte 1, dim 4j + k at bits 2k of
+// byte j) -> 4 fp16 pairs (dim k, dim k + 4), k = 0..3: the order unpack_word gives INT4 nibbles.
+__device__ __forceinline__ void unpack_u2(uint32_t h, uint32_t (&o)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = u2_lookup(h >> (2 * k));
+}
+
+// The same 8 dims of two rows a and b: o[i] = (a's dim i, b's dim i), i = 0..7.
+__device__ __forceinline__ void unpack_u2_pair(uint32_t ha, uint32_t hb, uint32_t (&o)[8]) {
+    const uint32_t y0 = prmt(ha, hb, 0x0040u), y1 = prmt(ha, hb, 0x0051u);   // (a.byte j, b.byte j)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        o[k] = u2_lookup(y0 >> (2 * k));
+        o[4 + k] = u2_lookup(y1 >> (2 * k));
+    }
+}
+
 // Token order inside a 16-token block used by the attention kernels: mma row / key index r maps
 // to token tau(r) = ((r & 7) >> 1) + 4 * (r & 1) + 8 * (r >> 3).  It makes the four rows a thread
 // reads for P.V (tokens t, t+4, t+8, t+12 of lane quad t) fall in distinct shared-memory banks.

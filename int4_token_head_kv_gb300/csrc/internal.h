@@ -74,11 +74,19 @@ constexpr int kOptWindow = 1, kOptSoftcap = 2, kOptAlibi = 4;
 cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
 // INT8 per-(token, head) comparator rows (D codes + fp32 scale); p.signs and p.c are not used.
 cudaError_t launch_write_int8(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
+// INT2 Lloyd-Max rows (D/4 code bytes + the fp32 RMS scale) after the INT4 mode's rotation.
+cudaError_t launch_write_int2(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);
 // Decode path: query rotation, the split-KV segment walker, and the combine that finishes every
 // decode sequence.  num_ctas is the walker's grid (decode_grid_size).
-// bits: 4 for the INT4 cache, 8 for the INT8 comparator's cache (no rotation, no zero-points)
+// bits: 4 for the INT4 cache, 8 for the INT8 comparator's cache (no rotation, no zero-points), 2 for
+// the INT2 Lloyd-Max cache (rotated, centroids, no zero-points)
 cudaError_t launch_decode(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
                           cudaStream_t stream, int bits);
+// the INT8 and INT2 instantiations of the decode path (launch_decode calls them for bits 8 and 2)
+cudaError_t launch_decode_int8(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
+                               cudaStream_t stream);
+cudaError_t launch_decode_int2(const AttnParams& p, int head_size, int num_ctas, DType q_dt, DType out_dt,
+                               cudaStream_t stream);
 int decode_grid_size(int64_t max_weight_total, int64_t max_units);
 constexpr int kDecodeMaxUnits = 256;   // split-KV units one walker CTA may own
 

@@ -57,17 +57,15 @@ struct WriteSigns {
     float2 even[D / 4];
 };
 
-// One thread's half of an INT4 vector.  row: the vector's D/2 input pairs (pair m = elements 2m,
+// One thread's half of a rotated vector.  row: the vector's D/2 input pairs (pair m = elements 2m,
 // 2m + 1, low half first) in shared memory; t: this thread's element parity.  With Q = D/4, thread t
-// holds P[k] = (u_{2k+t}, u_{2(k+Q)+t}) in a register pair.  A butterfly at stride 2s (s < Q) of the
-// element index pairs local m with m + s, i.e. P[k] with P[k + s] lane by lane; the stride D/2
-// pairs the two lanes of P[k].  The output: the Q/4 code words this thread stores (t = 0: words
-// 0 .. Q/4 - 1; t = 1: words Q/4 .. Q/2 - 1) and the scale word.
+// ends with P[k] = (y_{2k+t}, y_{2(k+Q)+t}) in a register pair.  A butterfly at stride 2s (s < Q) of
+// the element index pairs local m with m + s, i.e. P[k] with P[k + s] lane by lane; the stride D/2
+// pairs the two lanes of P[k].
 template <int D, typename T>
-__device__ __forceinline__ void encode_half(const uint32_t* row, const WriteSigns<D>& sg, int t, float c,
-                                            uint32_t (&out)[D / 16 + 1]) {
+__device__ __forceinline__ void rotate_half(const uint32_t* row, const WriteSigns<D>& sg, int t, float c,
+                                            float2 (&P)[D / 4]) {
     constexpr int Q = D / 4;
-    float2 P[Q];
     const uint32_t* xm = sg.xmask[t];
     // stride 1: u_{2m+t} = a_m + (t ? -1 : 1) b_m, (a_m, b_m) = the sign-flipped input pair m
 #pragma unroll
@@ -113,6 +111,16 @@ __device__ __forceinline__ void encode_half(const uint32_t* row, const WriteSign
 #pragma unroll
     for (int k = 0; k < Q; ++k)
         P[k] = mul_f32x2(make_float2(__fadd_rn(P[k].x, P[k].y), __fsub_rn(P[k].x, P[k].y)), c2);
+}
+
+// One thread's half of an INT4 vector: the rotation, then the Q/4 code words this thread stores
+// (t = 0: words 0 .. Q/4 - 1; t = 1: words Q/4 .. Q/2 - 1) and the scale word.
+template <int D, typename T>
+__device__ __forceinline__ void encode_half(const uint32_t* row, const WriteSigns<D>& sg, int t, float c,
+                                            uint32_t (&out)[D / 16 + 1]) {
+    constexpr int Q = D / 4;
+    float2 P[Q];
+    rotate_half<D, T>(row, sg, t, c, P);
     // min / max over the rotated vector (exact): this half, then the other
     float mx0 = P[0].x, mx1 = P[0].y, mn0 = P[0].x, mn1 = P[0].y;
 #pragma unroll
@@ -176,6 +184,69 @@ __device__ __forceinline__ void encode_half(const uint32_t* row, const WriteSign
         out[w] = (t ? yw[w] : xw[w]) | other;
     }
     out[Q / 4] = sb | zp;
+}
+
+// INT2 Lloyd-Max mode ("[Feature] Triton INT4 / INT2 per-token-head KV cache quantization",
+// description: four 2-bit codes per byte, Hadamard pre-rotation, centroids of the 4-level Lloyd-Max
+// quantiser of N(0, 1)).  After the INT4 mode's rotation, per vector:
+//   sigma = max(sqrt(fp32(sum y_i^2) / D), 1e-6), the sum of the fp32 squares folded in halves
+//   (a_i + a_{i + D/2}, then + a_{i + D/4}, ...); r = fp32(1 / sigma); z_i = fp32(y_i * r);
+//   code_i = [z_i >= -t] + [z_i >= 0] + [z_i >= t]   (codes 0..3 stand for -b, -a, a, b)
+// stored as D/4 bytes (element 4j + k in bits 2k of byte j), then the bits of sigma.
+// Lloyd-Max outputs a, b and threshold t = (a + b) / 2 of N(0, 1) (J. Max, 1960), fp32-rounded.
+constexpr float kLmA = 0x1.cfa592p-2f;    // 0.45278
+constexpr float kLmB = 0x1.82aabap+0f;    // 1.51042
+constexpr float kLmT = 0x1.f6941ep-1f;    // 0.98160
+
+// Thread t's half (elements of parity t): P[k] holds elements 2k + t and 2(k + Q) + t, so the fold
+// strides D/2 .. 2 stay in the thread (P[k].x with P[k].y, then s[k] with s[k + h]) and the last
+// (elements 0 and 1) pairs the two threads.  Element 2m + t is field 2(m & 1) + t of byte m >> 1:
+// the .x elements fill bytes 0 .. Q/2 - 1 (words 0 .. Q/8 - 1), the .y elements the rest.
+template <int D, typename T>
+__device__ __forceinline__ void encode_half_int2(const uint32_t* row, const WriteSigns<D>& sg, int t, float c,
+                                                 uint32_t (&out)[D / 32 + 1]) {
+    constexpr int Q = D / 4;
+    float2 P[Q];
+    rotate_half<D, T>(row, sg, t, c, P);
+    float sq[Q];
+#pragma unroll
+    for (int k = 0; k < Q; ++k) sq[k] = __fadd_rn(__fmul_rn(P[k].x, P[k].x), __fmul_rn(P[k].y, P[k].y));
+#pragma unroll
+    for (int h = Q / 2; h >= 1; h >>= 1) {
+#pragma unroll
+        for (int k = 0; k < h; ++k) sq[k] = __fadd_rn(sq[k], sq[k + h]);
+    }
+    const float sum = __fadd_rn(sq[0], __shfl_xor_sync(0xffffffffu, sq[0], 1));
+    float sigma = __fsqrt_rn(__fmul_rn(sum, 1.0f / (float)D));   // the power-of-two product is exact
+    if (!(sigma >= 1e-6f)) sigma = 1e-6f;
+    const float r = __frcp_rn(sigma);
+    // two codes per element pair m = 2j, 2j + 1 of a byte: fields t and 2 + t
+    auto code = [&](float y) -> uint32_t {
+        const float z = __fmul_rn(y, r);
+        return (uint32_t)(z >= -kLmT) + (uint32_t)(z >= 0.0f) + (uint32_t)(z >= kLmT);
+    };
+    uint32_t xw[Q / 8], yw[Q / 8];
+#pragma unroll
+    for (int w = 0; w < Q / 8; ++w) {
+        uint32_t ax = 0, ay = 0;
+#pragma unroll
+        for (int by = 0; by < 4; ++by) {
+            const int m = 2 * (4 * w + by);   // the byte's first element pair index
+            ax |= (code(P[m].x) | (code(P[m + 1].x) << 4)) << (8 * by);
+            ay |= (code(P[m].y) | (code(P[m + 1].y) << 4)) << (8 * by);
+        }
+        const uint32_t sh = 2u * (uint32_t)t;
+        xw[w] = ax << sh;
+        yw[w] = ay << sh;
+    }
+#pragma unroll
+    for (int w = 0; w < Q / 8; ++w) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, t ? xw[w] : yw[w], 1);
+        out[w] = (t ? yw[w] : xw[w]) | other;
+    }
+    out[Q / 8] = __float_as_uint(sigma);
+    (void)kLmA;
+    (void)kLmB;
 }
 
 // INT8 per-(token, head) comparator ("tests/quantization/test_per_token_kv_cache.py",
@@ -271,22 +342,24 @@ struct VecIndex {
     }
 };
 
-template <bool INT8>
+// BITS: 4 the INT4 cache, 8 the INT8 comparator, 2 the INT2 Lloyd-Max mode.
+template <int BITS>
 struct WriteShape {
-    static constexpr int kTpv = INT8 ? 1 : 2;          // threads per vector
-    static constexpr int kTileVecs = 32 / kTpv;        // vectors per warp tile
-    static constexpr int kMinBlocks = INT8 ? 3 : 5;    // resident CTAs per SM (register budget)
+    static constexpr int kTpv = BITS == 8 ? 1 : 2;          // threads per vector
+    static constexpr int kTileVecs = 32 / kTpv;             // vectors per warp tile
+    static constexpr int kMinBlocks = BITS == 8 ? 3 : 5;    // resident CTAs per SM (register budget)
 };
 
-template <int D, typename T, bool INT8>
-__global__ void __launch_bounds__(kWriteThreads, WriteShape<INT8>::kMinBlocks)
+template <int D, typename T, int BITS>
+__global__ void __launch_bounds__(kWriteThreads, WriteShape<BITS>::kMinBlocks)
     write_kernel(const __grid_constant__ WriteParams p) {
     using Gm = Geo<D>;
-    using Sh = WriteShape<INT8>;
+    using Sh = WriteShape<BITS>;
+    constexpr bool INT8 = BITS == 8;
     constexpr int TPV = Sh::kTpv, TV = Sh::kTileVecs;
-    constexpr int RB = INT8 ? D + 4 : Gm::RB;       // cache row bytes
-    constexpr int NW = INT8 ? D / 4 : Gm::KW;       // code words per row (then the scale word)
-    constexpr int OW = INT8 ? NW + 1 : D / 16 + 1;  // words one thread stores (the last: the scale word)
+    constexpr int RB = INT8 ? D + 4 : (BITS == 2 ? D / 4 + 4 : Gm::RB);   // cache row bytes
+    constexpr int NW = RB / 4 - 1;                                       // code words per row (then the scale)
+    constexpr int OW = INT8 ? NW + 1 : NW / 2 + 1;   // words one thread stores (the last: the scale word)
     using Sm = WriteSmem<D, TV>;
     extern __shared__ __align__(128) uint8_t smem[];
     // Launched as a programmatic dependent: wait for the previous kernel of the stream (it may
@@ -371,13 +444,14 @@ __global__ void __launch_bounds__(kWriteThreads, WriteShape<INT8>::kMinBlocks)
         } else {
             // every lane runs the encoder (it exchanges values within the lane pair); a vector past
             // the end reads row 0, which every tile holds, and its words are discarded
-            encode_half<D, T>(reinterpret_cast<const uint32_t*>(cur + (live ? vl : 0) * Sm::kRowPad), sgn, part,
-                              p.c, words);
+            const uint32_t* in = reinterpret_cast<const uint32_t*>(cur + (live ? vl : 0) * Sm::kRowPad);
+            if constexpr (BITS == 2) encode_half_int2<D, T>(in, sgn, part, p.c, words);
+            else encode_half<D, T>(in, sgn, part, p.c, words);
             __syncwarp();   // the tile's inputs are consumed; its buffer becomes the output stage
         }
         // this thread's words of the row: all of them (INT8), or the first / second half of the code
-        // words (INT4 parts 0 / 1; part 1 also the scale word)
-        const int w0 = INT8 ? 0 : part * (D / 16);
+        // words (INT4 / INT2 parts 0 / 1; part 1 also the scale word)
+        const int w0 = INT8 ? 0 : part * (NW / 2);
         const int nw = INT8 ? OW : (part ? OW : OW - 1);
         uint32_t tok = 0, h = 0, pl = 0;
         if (live) vx.split(v, tok, h, pl);
@@ -422,16 +496,16 @@ __global__ void __launch_bounds__(kWriteThreads, WriteShape<INT8>::kMinBlocks)
     (void)kRoundMagicBits;
 }
 
-template <int D, typename T, bool INT8>
+template <int D, typename T, int BITS>
 cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
-    using Sh = WriteShape<INT8>;
+    using Sh = WriteShape<BITS>;
     using Sm = WriteSmem<D, Sh::kTileVecs>;
     const int64_t ntiles = (p.num_tokens * p.H * 2 + Sh::kTileVecs - 1) / Sh::kTileVecs;
     int64_t blocks = (ntiles + kWriteWarps - 1) / kWriteWarps;
     const int64_t cap = (int64_t)num_sms() * Sh::kMinBlocks;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    cudaError_t err = opt_in_smem<write_kernel<D, T, INT8>>(Sm::kBytes);
+    cudaError_t err = opt_in_smem<write_kernel<D, T, BITS>>(Sm::kBytes);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -443,29 +517,33 @@ cudaError_t launch_write_t(const WriteParams& p, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, write_kernel<D, T, INT8>, p);
+    return cudaLaunchKernelEx(&cfg, write_kernel<D, T, BITS>, p);
 }
 
 }  // namespace
 
 namespace {
-template <bool INT8>
+template <int BITS>
 cudaError_t launch_write_mode(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
     if (head_size == 128) {
-        return dt == DType::BF16 ? launch_write_t<128, __nv_bfloat16, INT8>(p, stream)
-                                 : launch_write_t<128, __half, INT8>(p, stream);
+        return dt == DType::BF16 ? launch_write_t<128, __nv_bfloat16, BITS>(p, stream)
+                                 : launch_write_t<128, __half, BITS>(p, stream);
     }
-    return dt == DType::BF16 ? launch_write_t<64, __nv_bfloat16, INT8>(p, stream)
-                             : launch_write_t<64, __half, INT8>(p, stream);
+    return dt == DType::BF16 ? launch_write_t<64, __nv_bfloat16, BITS>(p, stream)
+                             : launch_write_t<64, __half, BITS>(p, stream);
 }
 }  // namespace
 
 cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
-    return launch_write_mode<false>(p, head_size, dt, stream);
+    return launch_write_mode<4>(p, head_size, dt, stream);
 }
 
 cudaError_t launch_write_int8(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
-    return launch_write_mode<true>(p, head_size, dt, stream);
+    return launch_write_mode<8>(p, head_size, dt, stream);
+}
+
+cudaError_t launch_write_int2(const WriteParams& p, int head_size, DType dt, cudaStream_t stream) {
+    return launch_write_mode<2>(p, head_size, dt, stream);
 }
 
 }  // namespace kvi4

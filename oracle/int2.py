@@ -84,7 +84,8 @@ def cache_shape(num_blocks: int, block_size: int, num_kv_heads: int, head_size: 
 
 def fold_sum_of_squares(y: np.ndarray) -> np.ndarray:
     """sum_i y_i^2 of each row in fp32, folded in halves (a_i + a_{i + d/2}, then + a_{i + d/4}, ...)."""
-    a = (y * y).astype(np.float32)
+    with np.errstate(over="ignore"):   # squares past fp32 range are inf, as in IEEE arithmetic
+        a = (y * y).astype(np.float32)
     while a.shape[-1] > 1:
         h = a.shape[-1] // 2
         a = (a[..., :h] + a[..., h:]).astype(np.float32)

@@ -19,12 +19,13 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kv_int[48]_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(kv_int[248]_\w+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
     names = _declared_functions()
     assert len(names) >= 8
+    assert {"kv_int2_write", "kv_int2_paged_attention", "kv_int2_row_bytes"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in kv_int4.h but not exported"
 
@@ -61,6 +62,16 @@ def test_host_side_validation(lib):
     assert lib.kv_int8_write(None, None, 1, 0, 2, 128, None, None, 8, 16, None) == 0
     lib.kv_int8_row_bytes.restype = ctypes.c_int32
     assert lib.kv_int8_row_bytes(128) == 132 and lib.kv_int8_row_bytes(64) == 68
+    # the INT2 write takes the INT4 write's arguments and validates them the same way
+    lib.kv_int2_write.restype = ctypes.c_int
+    lib.kv_int2_write.argtypes = lib.kv_int4_write.argtypes
+    assert lib.kv_int2_write(fake, fake, 1, 4, 2, 96, fake, fake, fake, 8, 16, None) == 2
+    assert lib.kv_int2_write(fake, fake, 1, 4, 2, 128, fake, fake, fake, 8, 32, None) == 2
+    assert lib.kv_int2_write(fake, fake, 1, 4, 2, 128, fake, None, fake, 8, 16, None) == 1   # signs required
+    assert lib.kv_int2_write(fake, fake, 1, 4, 2, 128, fake, fake, fake + 4, 8, 16, None) == 3
+    assert lib.kv_int2_write(None, None, 1, 0, 2, 128, None, None, None, 8, 16, None) == 0
+    lib.kv_int2_row_bytes.restype = ctypes.c_int32
+    assert lib.kv_int2_row_bytes(128) == 36 and lib.kv_int2_row_bytes(64) == 20
 
 
 def test_attention_validation_and_workspace_policy(lib):
@@ -131,6 +142,29 @@ def test_int8_attention_validation(lib):
     assert call(cache=None) == 1
     assert call(q=fake + 8) == 3
     assert call(msl=131072, seg=4096, mb=8192) == 4   # the INT4 call's workspace, required and missing
+    assert call(nq=0) == 0
+
+
+def test_int2_attention_validation(lib):
+    f = lib.kv_int2_paged_attention
+    f.restype = ctypes.c_int
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float,
+                  vp, i32, vp, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    fake = 1 << 20
+    base = dict(q=fake, qd=1, nq=2, hq=32, cache=fake, nb=64, h=8, d=128, bs=16, bt=fake, mb=4, sl=fake, qsl=fake,
+                ns=2, mql=1, msl=64, scale=0.088, signs=fake, seg=0, out=fake, od=2, ws=None, wsb=0, st=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(*a.values())
+
+    assert call(mql=2) == 2                # decode only
+    assert call(h=3, hq=24) == 2
+    assert call(d=96) == 2
+    assert call(signs=None) == 1           # rotated: the signs are required
+    assert call(cache=fake + 8) == 3
+    assert call(msl=131072, seg=4096, mb=8192) == 4
     assert call(nq=0) == 0
 
 
