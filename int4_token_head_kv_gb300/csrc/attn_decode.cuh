@@ -31,14 +31,19 @@
 //    copies, and the last consumer warp to finish with a stage issues its next block.  The
 //    rotated-query record of each run of units of one sequence arrives the same way.
 //  * Eight consumer warps: warp w owns kv head w % H (and every (8/H)-th block pair when H < 8).
-//    Split-dot scores over the even and odd nibble streams: each code word is unpacked into the
-//    raw codes as exact fp16 integers (even codes through fp16 1024 + e, odd codes through
-//    1024 + 16 e, both brought back by one constant fp16x2 operation), and
-//    S^T[16 tokens x 8 columns] = Codes[16 x D] . Q'^T comes from mma.sync m16n8k16; the
-//    zero-point is then removed per key with the sum(Q') * zp correction.  (Leaving the 1024
-//    offsets in the mma operands saves the constant operations but costs the scores about 8 bits
-//    of fp32 accumulation precision, which heavy-tailed caches expose.)
+//    Split-dot scores over the even and odd nibble streams: each K code word is masked into its
+//    nibbles as exact fp16 subnormals with no offset (even codes e 2^-24, odd codes 16 o 2^-24:
+//    one logic op per pair), and S^T[16 tokens x 8 columns] = Codes[16 x D] . Q'^T comes from
+//    mma.sync m16n8k16; the query record carries the odd dimensions divided by 16, the logit factor
+//    times 2^24 and sum(Q') over 2^24, so the zero-point is removed per key with the sum(Q') * zp
+//    correction on the same scale.  (The tensor cores accumulate products of subnormal operands
+//    with a few bits less precision, measured about 1e-6 of the sum of |terms| against the query's
+//    operands; an offset left in the operands, such as 1024 + e, would cost about 8 bits, which
+//    heavy-tailed caches expose.)
 //  * P^T is transposed in registers (movmatrix) into the B operand of O^T[D x 8] += Codes_V^T P^T.
+//    The V codes are exact fp16 integers (even codes through fp16 1024 + e, odd codes through
+//    1024 + 16 e, both brought back by one constant fp16x2 operation): against weights whose
+//    magnitudes span many binades, subnormal code operands would lose about 7 bits.
 //    V's per-key scale is folded into P (w = p * s'_V * 2^-E, E a running max exponent, so the
 //    fp16 weights never overflow); w and Q' are carried as fp16 high + low halves.  V's
 //    zero-points leave O through sum(w zp), kept per column alongside O.
@@ -62,12 +67,12 @@ constexpr uint32_t kSmemPerSm = 233472;               // 228 KB of shared memory
 constexpr uint32_t kSmemPerCtaReserved = 1024;
 
 constexpr int kMaxHead = 128;
-constexpr float kLazyMax = 8.0f;     // log2 units the running maximum may fall behind a block's
-constexpr uint32_t kLazyExp = 4;     // binades the V exponent reference may fall behind a V scale
-// unpack_word operands that turn codes into exact fp16 integers: lo nibbles 1024 + e - 1024,
+// unpack_word operands that turn V codes into exact fp16 integers: lo nibbles 1024 + e - 1024,
 // hi nibbles (1024 + 16 e) / 16 - 64
 constexpr uint32_t kCodeLo = 0x64006400u;   // (1024, 1024)
 constexpr uint32_t kCodeHi = 0xD400D400u;   // (-64, -64)
+constexpr float kLazyMax = 8.0f;     // log2 units the running maximum may fall behind a block's
+constexpr uint32_t kLazyExp = 4;     // binades the V exponent reference may fall behind a V scale
 
 // Cached rows: BITS = 4 is the INT4 cache (D/2 code bytes, then the scale word with the zero-point
 // in its low nibble), BITS = 8 the INT8 comparator (D int8 codes, then the fp32 scale), BITS = 2 the
@@ -254,11 +259,13 @@ __global__ void __launch_bounds__(256) qrot_kernel(const __grid_constant__ AttnP
             for (int hh = 0; hh < 2; ++hh) {
                 const int d0 = BITS != 8 ? 8 * W + 2 * hh : 8 * W + 4 * hh;
                 const int s1 = BITS != 8 ? 4 : 1, s2 = BITS != 8 ? 1 : 2;   // second of a pair; next pair
+                // INT4: the odd dimensions meet high nibbles, which unpack as 16 x their code
+                const __half od = __float2half(BITS == 4 ? 0.0625f : 1.0f);
                 w[2 * hh] = live ? pack_halves(qv[d0], qv[d0 + s1]) : 0u;
-                w[2 * hh + 1] = live ? pack_halves(qv[d0 + s2], qv[d0 + s2 + s1]) : 0u;
+                w[2 * hh + 1] = live ? pack_halves(__hmul(qv[d0 + s2], od), __hmul(qv[d0 + s2 + s1], od)) : 0u;
                 if constexpr (WIDE) {
                     w[4 + 2 * hh] = live ? pack_halves(qv2[d0], qv2[d0 + s1]) : 0u;
-                    w[5 + 2 * hh] = live ? pack_halves(qv2[d0 + s2], qv2[d0 + s2 + s1]) : 0u;
+                    w[5 + 2 * hh] = live ? pack_halves(__hmul(qv2[d0 + s2], od), __hmul(qv2[d0 + s2 + s1], od)) : 0u;
                 }
             }
             uint4* dst = reinterpret_cast<uint4*>(rec) + (size_t)idx * (QW / 4);
@@ -593,6 +600,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
             al1 = (WIDE && hb + 1 < G) ? alpha[h * G + hb + 1] : 0.0f;
             qs0 = (hb < G) ? qsum[h * G + hb] : 0.0f;
             qs1 = (WIDE && hb + 1 < G) ? qsum[h * G + hb + 1] : 0.0f;
+            if constexpr (BITS == 4) {   // the scores come out over 2^24 (subnormal code operands)
+                al0 *= 16777216.0f;
+                al1 *= 16777216.0f;
+                qs0 *= 0x1.0p-24f;
+                qs1 *= 0x1.0p-24f;
+            }
             if constexpr (OPTS) {
                 const bool alibi = (p.opts & kOptAlibi) != 0;
                 sl0 = alibi && hb < G ? __ldg(p.alibi + h * G + hb) * kLog2e : 0.0f;
@@ -671,8 +684,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         for (int q = 0; q < Gm::KWPT; ++q) {
                             uint32_t a0[4], a1[4];
                             if constexpr (BITS == 4) {
-                                unpack_word(kr0[t + 4 * q], kCodeLo, kCodeHi, a0);
-                                unpack_word(kr1[t + 4 * q], kCodeLo, kCodeHi, a1);
+                                unpack_word_sub(kr0[t + 4 * q], a0);
+                                unpack_word_sub(kr1[t + 4 * q], a1);
                             } else if constexpr (BITS == 2) {   // 16-bit groups of 8 dims
                                 unpack_u2(reinterpret_cast<const uint16_t*>(kr0)[t + 4 * q], a0);
                                 unpack_u2(reinterpret_cast<const uint16_t*>(kr1)[t + 4 * q], a1);

@@ -283,6 +283,18 @@ __device__ __forceinline__ void unpack_word_pair(uint32_t wa, uint32_t wb, uint3
     }
 }
 
+// The same 8 nibbles with no offset to remove: a masked nibble is already an exact fp16 number, the
+// subnormal n 2^-24 (low nibbles) or 16 n 2^-24 = n 2^-20 (high nibbles).  The caller folds the 2^24
+// and the extra 16 of the odd dimensions (the high nibbles) into the other operand and the results.
+// Pairs as unpack_word: o[0] = dims (0, 4), o[1] = (1, 5) x 16, o[2] = (2, 6), o[3] = (3, 7) x 16.
+__device__ __forceinline__ void unpack_word_sub(uint32_t w, uint32_t (&o)[4]) {
+    const uint32_t w8 = w >> 8;
+    o[0] = w & 0x000F000Fu;
+    o[1] = w & 0x00F000F0u;
+    o[2] = w8 & 0x000F000Fu;
+    o[3] = w8 & 0x00F000F0u;
+}
+
 // ----------------------------------------------------------------------- int8 code unpacking
 // Four int8 codes of a word as offset binary x + 128 (the sign bit flipped) under the fp16 exponent
 // byte 0x64 give 1024 + x + 128 exactly; subtracting 1152 leaves x.
