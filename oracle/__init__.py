@@ -210,7 +210,7 @@ def gather_rows(cache: np.ndarray, block_table_row: np.ndarray, seq_len: int, pl
 
 def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softmax_scale, signs,
                     seqs=None, kv_heads=None, window_left=-1, softcap=0.0, alibi_slopes=None,
-                    row_decoder=None) -> np.ndarray:
+                    row_decoder=None, qq_bias=None) -> np.ndarray:
     """Causal softmax attention over the dequantised, un-rotated paged cache, in fp64.
 
     query [Nq, Hq, d] (original domain); sequence b owns query rows
@@ -226,7 +226,12 @@ def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softm
     s_j = softmax_scale * q . k_j of key j for a query at position pos:
       softcap > 0:           s_j <- softcap * tanh(s_j / softcap)
       alibi_slopes [Hq]:     s_j <- s_j + slope_g * (j - pos)
+      qq_bias [Q, Q]:        s_j <- s_j + qq_bias[t, j - c] for the keys of the query chunk itself
+                             (c = seq_len - q_len <= j, j - c < Q), t the query's index in its chunk
       window_left >= 0:      key j is visible only if pos - j <= window_left (besides j <= pos).
+    The page lists qq_bias among the shared helpers without defining it; this reading is the
+    query-to-query bias of the unified-attention interface: one [Q, Q] matrix for every sequence and
+    head, row t for the chunk's t-th query, column u for the chunk's u-th token as a key.
     """
     q = _as_f32_array(query).astype(np.float64)
     nq, hq, d = q.shape
@@ -258,6 +263,11 @@ def paged_attention(query, cache, block_tables, seq_lens, query_start_loc, softm
                         s = softcap * np.tanh(s / softcap)
                     if alibi_slopes is not None:
                         s = s + float(alibi_slopes[g]) * (np.arange(first, nkeys) - pos)
+                    if qq_bias is not None:
+                        bias = np.asarray(qq_bias, dtype=np.float64)
+                        u = np.arange(first, nkeys) - (L - qlen)
+                        inside = (u >= 0) & (u < bias.shape[1])
+                        s = s + np.where(inside, bias[t, np.clip(u, 0, bias.shape[1] - 1)], 0.0)
                     w = np.exp(s - s.max())
                     out[q0 + t, g] = (w @ vhat[first:nkeys]) / w.sum()
     return out

@@ -86,9 +86,10 @@ def test_identical_keys_give_the_mean_value():
     np.testing.assert_allclose(out[0, 1], vhat.mean(0), atol=1e-12)
 
 
-def _brute_force(wl, cache, bias=None):
+def _brute_force(wl, cache, bias=None, chunk_bias=None):
     """Independent restatement: scipy's Hadamard and softmax, explicit per-key loops.  bias(g, j,
-    pos, s) -> the logit of key j (None: masked) overrides the plain scaled dot product."""
+    pos, s) -> the logit of key j (None: masked) overrides the plain scaled dot product;
+    chunk_bias(t, u) is added to the logit of the chunk's u-th token as a key, for its t-th query."""
     d = wl.head_size
     hm = scipy.linalg.hadamard(d).astype(np.float64)
     G = wl.num_q_heads // wl.num_kv_heads
@@ -119,6 +120,10 @@ def _brute_force(wl, cache, bias=None):
                     ks.append(vecs[0])
                     vs.append(vecs[1])
                 logits = wl.softmax_scale * np.array(ks) @ q[q0 + t, g]
+                if chunk_bias is not None:
+                    start = L - (q1 - q0)
+                    for j in range(start, pos + 1):
+                        logits[j] += chunk_bias(t, j - start)
                 if bias is not None:
                     kept = [(bias(g, j, pos, float(logits[j])), j) for j in range(pos + 1)]
                     kept = [(x, j) for x, j in kept if x is not None]
@@ -228,6 +233,36 @@ def test_alibi_matches_brute_force_and_limits():
     # a steep slope leaves only the newest key
     steep = _run(wl, cache, alibi_slopes=np.full(6, 1e4))
     np.testing.assert_allclose(steep, _run(wl, cache, window_left=0), atol=1e-12)
+
+
+def test_qq_bias_matches_brute_force_and_closed_forms():
+    wl = workloads.make_attention_workload("t", [21, 9, 40], [5, 1, 8], 4, 2, 64, seed=26)
+    cache = _cache_for(wl)
+    r = np.random.default_rng(26)
+    bias = r.uniform(-3, 3, (8, 8))
+    ref = _brute_force(wl, cache, chunk_bias=lambda t, u: bias[t, u])
+    np.testing.assert_allclose(_run(wl, cache, qq_bias=bias), ref, rtol=1e-10, atol=1e-12)
+    # a zero bias changes nothing; a larger matrix than the chunks reads only its leading block
+    np.testing.assert_allclose(_run(wl, cache, qq_bias=np.zeros((8, 8))), _run(wl, cache), atol=0)
+    big = np.full((12, 12), 99.0)
+    big[:8, :8] = bias
+    np.testing.assert_allclose(_run(wl, cache, qq_bias=big), _run(wl, cache, qq_bias=bias), atol=0)
+    # -inf off the diagonal: each query sees the context before its chunk and itself only; with a
+    # one-query chunk (sequence 1) the bias only moves the query's own key, by bias[0, 0]
+    diag = np.where(np.eye(8) > 0, 0.0, -np.inf)
+    out = _run(wl, cache, qq_bias=diag)
+    for b in (0, 2):
+        L = int(wl.seq_lens[b])
+        q0, q1 = int(wl.query_start_loc[b]), int(wl.query_start_loc[b + 1])
+        start = L - (q1 - q0)
+        for t in range(q1 - q0):
+            keep = lambda g, j, pos, s, t=t, start=start: s if (j < start or j == start + t) else None  # noqa: E731
+            one = _brute_force(wl, cache, bias=keep)
+            np.testing.assert_allclose(out[q0 + t], one[q0 + t], rtol=1e-10, atol=1e-12)
+    shift = np.zeros((8, 8))
+    shift[0, 0] = 1.5
+    own = _brute_force(wl, cache, bias=lambda g, j, pos, s: s + 1.5 if j == pos else s)
+    np.testing.assert_allclose(_run(wl, cache, qq_bias=shift)[5], own[5], rtol=1e-10, atol=1e-12)
 
 
 def test_options_compose_in_order():
