@@ -229,21 +229,29 @@ kv_int4_status kv_int4_paged_attention(const void* q, kv_int4_dtype q_dtype, int
 /*
  * kv_int4_paged_attention_ex -- kv_int4_paged_attention with the unified-attention interface's
  * options ("tests/quantization/test_per_token_kv_cache.py", the window_size and softcap arguments
- * of unified_attention; the PR #40633 description lists sliding window, softcap and ALiBi among
- * the helpers the packed read path shares).  On the scaled logit s_j = softmax_scale * q . x_K,j
- * of key j for a query at position pos, in this order:
+ * of unified_attention; the PR #40633 description lists sliding window, softcap, ALiBi and qq_bias
+ * among the helpers the packed read path shares).  On the scaled logit s_j = softmax_scale *
+ * q . x_K,j of key j for a query at position pos, the t-th query of a chunk whose first query sits
+ * at position c = seq_len - q_len, in this order:
  *   softcap > 0            s_j <- softcap * tanh(s_j / softcap)
  *   alibi_slopes != NULL   s_j <- s_j + alibi_slopes[g] * (j - pos), g the query head
+ *   qq_bias != NULL        s_j <- s_j + qq_bias[t * qq_bias_stride + (j - c)] for c <= j
+ *                          (j - c < qq_bias_stride; keys before the chunk take no bias)
  *   window_left >= 0       key j is visible only if pos - j <= window_left (besides j <= pos)
- * options NULL, or window_left < 0, softcap 0 and alibi_slopes NULL: exactly
- * kv_int4_paged_attention.  alibi_slopes: DEVICE fp32 [num_q_heads], 4-byte aligned.
- * Returns KV_INT4_EINVAL for a negative or non-finite softcap; everything else as
- * kv_int4_paged_attention (same workspace).  The options are read at the call.
+ * options NULL, or window_left < 0, softcap 0, alibi_slopes NULL and qq_bias NULL: exactly
+ * kv_int4_paged_attention.  alibi_slopes: DEVICE fp32 [num_q_heads]; qq_bias: DEVICE fp32, row t at
+ * qq_bias + t * qq_bias_stride, at least max_query_len rows (one matrix for every sequence and
+ * head; the query-to-query bias reading of the page's "qq_bias"), a -inf entry masks its key.
+ * Returns KV_INT4_EINVAL for a negative or non-finite softcap or a qq_bias_stride below
+ * max_query_len; everything else as kv_int4_paged_attention (same workspace).  The options are
+ * read at the call.
  */
 typedef struct {
     int32_t window_left;        /* < 0: no window */
     float softcap;              /* 0: none */
     const float* alibi_slopes;  /* NULL: none */
+    const float* qq_bias;       /* NULL: none */
+    int32_t qq_bias_stride;     /* elements per qq_bias row, >= max_query_len */
 } kv_int4_attn_options;
 
 kv_int4_status kv_int4_paged_attention_ex(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,

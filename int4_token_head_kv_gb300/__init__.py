@@ -24,8 +24,10 @@ _DTYPES = {torch.float16: KV_INT4_F16, torch.bfloat16: KV_INT4_BF16, torch.float
 
 class AttnOptions(ctypes.Structure):
     """kv_int4_attn_options: window_left (< 0: none), softcap (0: none), alibi_slopes (device
-    pointer to fp32 [num_q_heads], or None)."""
-    _fields_ = [("window_left", ctypes.c_int32), ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p)]
+    pointer to fp32 [num_q_heads], or None), qq_bias (device pointer to fp32 rows of
+    qq_bias_stride elements, or None)."""
+    _fields_ = [("window_left", ctypes.c_int32), ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
+                ("qq_bias", ctypes.c_void_p), ("qq_bias_stride", ctypes.c_int32)]
 
 
 class KVInt4Error(RuntimeError):
@@ -205,9 +207,11 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
                             seq_lens: torch.Tensor, query_start_loc: torch.Tensor, softmax_scale: float,
                             rht_signs: torch.Tensor, max_query_len: int, max_seq_len: int, out=None,
                             out_dtype=None, segment_len: int = 0, workspace=None, stream=None,
-                            window_left: int = -1, softcap: float = 0.0, alibi_slopes=None) -> torch.Tensor:
+                            window_left: int = -1, softcap: float = 0.0, alibi_slopes=None,
+                            qq_bias=None) -> torch.Tensor:
     """Causal paged attention of ``query`` [Nq, Hq, d] over the INT4 cache; returns ``out``.  With
-    ``window_left >= 0``, ``softcap > 0`` or ``alibi_slopes`` (fp32 [Hq] on the device) the call
+    ``window_left >= 0``, ``softcap > 0``, ``alibi_slopes`` (fp32 [Hq] on the device) or ``qq_bias``
+    (fp32 [rows >= max_query_len, stride >= max_query_len] on the device, contiguous rows) the call
     goes through kv_int4_paged_attention_ex."""
     _cuda(query, "query", (torch.float16, torch.bfloat16))
     _cuda(kv_cache, "kv_cache", (torch.uint8,))
@@ -236,13 +240,19 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
             block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
             float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype], ws_ptr,
             ws_bytes, _stream(stream))
-    if window_left >= 0 or softcap != 0.0 or alibi_slopes is not None:
+    if window_left >= 0 or softcap != 0.0 or alibi_slopes is not None or qq_bias is not None:
         if alibi_slopes is not None:
             _cuda(alibi_slopes, "alibi_slopes", (torch.float32,))
             if alibi_slopes.shape != (Hq,):
                 raise ValueError("alibi_slopes must be [num_q_heads]")
+        if qq_bias is not None:
+            _cuda(qq_bias, "qq_bias", (torch.float32,))
+            if qq_bias.dim() != 2 or qq_bias.stride(1) != 1 or qq_bias.shape[0] < max_query_len:
+                raise ValueError("qq_bias must be a row-contiguous [rows >= max_query_len, cols] matrix")
         opts = AttnOptions(int(window_left), float(softcap),
-                           alibi_slopes.data_ptr() if alibi_slopes is not None else None)
+                           alibi_slopes.data_ptr() if alibi_slopes is not None else None,
+                           qq_bias.data_ptr() if qq_bias is not None else None,
+                           int(qq_bias.stride(0)) if qq_bias is not None else 0)
         st = load().kv_int4_paged_attention_ex(*args, ctypes.byref(opts))
         _check("kv_int4_paged_attention_ex", st)
     else:

@@ -249,6 +249,7 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
     if (segment_len % kBlockSize != 0 || num_seqs > 65535) return KV_INT4_EUNSUPPORTED;
     if (!(softmax_scale == softmax_scale)) return KV_INT4_EINVAL;
     if (options && !(options->softcap >= 0.0f && options->softcap <= 3.0e38f)) return KV_INT4_EINVAL;
+    if (options && options->qq_bias && options->qq_bias_stride < std::max(1, max_query_len)) return KV_INT4_EINVAL;
     if (num_q_tokens == 0 || num_seqs == 0) return KV_INT4_OK;
     if (!q || !cache || !block_tables || !seq_lens || !query_start_loc || (bits != 8 && !rht_signs) || !out)
         return KV_INT4_EINVAL;
@@ -306,6 +307,8 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
     p.cap_l2 = 0.0f;
     p.inv_cap_l2 = 0.0f;
     p.alibi = nullptr;
+    p.qq_bias = nullptr;
+    p.qq_stride = 0;
     if (options) {
         if (options->window_left >= 0) {
             p.opts |= kOptWindow;
@@ -319,6 +322,11 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
         if (options->alibi_slopes) {
             p.opts |= kOptAlibi;
             p.alibi = options->alibi_slopes;
+        }
+        if (options->qq_bias) {
+            p.opts |= kOptQQ;
+            p.qq_bias = options->qq_bias;
+            p.qq_stride = options->qq_bias_stride;
         }
     }
 

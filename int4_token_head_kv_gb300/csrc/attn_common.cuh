@@ -39,14 +39,19 @@ __device__ __forceinline__ void store_elem<float>(void* base, int64_t i, float x
 
 // The attention options on one visible key's logit x (log2 units) for a query at position pos and
 // key j: softcap C tanh(x / C) (tanh(y) = 1 - 2 / (e^{2y} + 1)), then the ALiBi bias
-// slope_l2 (j - pos), then the window (-inf when pos - j > window_left).  Masked keys stay -inf.
-__device__ __forceinline__ float apply_opts(float x, int j, int pos, float slope_l2, const AttnParams& p) {
+// slope_l2 (j - pos), then the query-to-query bias of the keys in the query chunk (cs: position of
+// the chunk's first query), then the window (-inf when pos - j > window_left).  Masked keys stay -inf.
+__device__ __forceinline__ float apply_opts(float x, int j, int pos, float slope_l2, const AttnParams& p, int cs) {
     if (!(x > -INFINITY)) return x;
     if (p.opts & kOptSoftcap) {
         const float e = fast_exp2(2.0f * kLog2e * (x * p.inv_cap_l2));   // e^{2y}, y = x / C
         x = p.cap_l2 * (1.0f - 2.0f / (e + 1.0f));
     }
     if (p.opts & kOptAlibi) x = fmaf(slope_l2, (float)(j - pos), x);
+    if (p.opts & kOptQQ) {
+        const int u = j - cs, r = pos - cs;   // key and query indices in the chunk (r < max_query_len)
+        if (u >= 0 && u < p.qq_stride && r >= 0) x = fmaf(__ldg(p.qq_bias + (int64_t)r * p.qq_stride + u), kLog2e, x);
+    }
     if ((p.opts & kOptWindow) && pos - j > p.window_left) x = -INFINITY;
     return x;
 }

@@ -680,15 +680,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     float c2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     if (ok[b]) {
+                        uint32_t nx0[4], nx1[4];   // INT2: the next group's operands, unpacked with this one
+                        (void)nx0;
+                        (void)nx1;
 #pragma unroll
                         for (int q = 0; q < Gm::KWPT; ++q) {
                             uint32_t a0[4], a1[4];
                             if constexpr (BITS == 4) {
                                 unpack_word_sub(kr0[t + 4 * q], a0);
                                 unpack_word_sub(kr1[t + 4 * q], a1);
-                            } else if constexpr (BITS == 2) {   // 16-bit groups of 8 dims
+                            } else if constexpr (BITS == 2 && WIDE) {   // 16-bit groups of 8 dims
                                 unpack_u2(reinterpret_cast<const uint16_t*>(kr0)[t + 4 * q], a0);
                                 unpack_u2(reinterpret_cast<const uint16_t*>(kr1)[t + 4 * q], a1);
+                            } else if constexpr (BITS == 2) {
+                                // two groups at a time, t + 4q and t + 4q + 4 (with eight query heads
+                                // per kv head the extra registers would spill)
+                                if ((q & 1) == 0) {
+                                    const uint16_t* g0 = reinterpret_cast<const uint16_t*>(kr0) + t + 4 * q;
+                                    const uint16_t* g1 = reinterpret_cast<const uint16_t*>(kr1) + t + 4 * q;
+                                    unpack_u2_x2((uint32_t)g0[0] | ((uint32_t)g0[4] << 16), a0, nx0);
+                                    unpack_u2_x2((uint32_t)g1[0] | ((uint32_t)g1[4] << 16), a1, nx1);
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        a0[e] = nx0[e];
+                                        a1[e] = nx1[e];
+                                    }
+                                }
                             } else {
                                 unpack_i8(kr0[2 * (t + 4 * q)], kr0[2 * (t + 4 * q) + 1], a0);
                                 unpack_i8(kr1[2 * (t + 4 * q)], kr1[2 * (t + 4 * q) + 1], a1);
@@ -724,11 +742,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     }
                     if constexpr (OPTS) {   // window / softcap / ALiBi
                         const int jb = u.y * kBlockSize + tb;   // position of this block's first token
-                        x[b][0] = apply_opts(x[b][0], jb + tk0, posd, sl0, p);
-                        x[b][2] = apply_opts(x[b][2], jb + tk1, posd, sl0, p);
+                        x[b][0] = apply_opts(x[b][0], jb + tk0, posd, sl0, p, posd);
+                        x[b][2] = apply_opts(x[b][2], jb + tk1, posd, sl0, p, posd);
                         if constexpr (WIDE) {
-                            x[b][1] = apply_opts(x[b][1], jb + tk0, posd, sl1, p);
-                            x[b][3] = apply_opts(x[b][3], jb + tk1, posd, sl1, p);
+                            x[b][1] = apply_opts(x[b][1], jb + tk0, posd, sl1, p, posd);
+                            x[b][3] = apply_opts(x[b][3], jb + tk1, posd, sl1, p, posd);
                         }
                     }
                     const uint32_t* vg0 = reinterpret_cast<const uint32_t*>(vp[b] + (tk0 * H + h) * Rw::RB);

@@ -482,8 +482,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                         const int key = key0 + 8 * i + 2 * t4 + e;
                         float xa = kk > 0.0f && key <= pos_a ? __uint_as_float(s[4 * i + e]) * kk : -INFINITY;
                         float xb = kk > 0.0f && key <= pos_b ? __uint_as_float(s[4 * i + 2 + e]) * kk : -INFINITY;
-                        xa = apply_opts(xa * rs_a, key, pos_a, sla, p) * irs_a;
-                        xb = apply_opts(xb * rs_b, key, pos_b, slb, p) * irs_b;
+                        xa = apply_opts(xa * rs_a, key, pos_a, sla, p, pos0) * irs_a;
+                        xb = apply_opts(xb * rs_b, key, pos_b, slb, p, pos0) * irs_b;
                         s[4 * i + e] = __float_as_uint(xa);
                         s[4 * i + 2 + e] = __float_as_uint(xb);
                         bma = fmaxf(bma, xa);

@@ -327,26 +327,39 @@ __device__ __forceinline__ void unpack_i8_pair(uint32_t a0, uint32_t a1, uint32_
 constexpr uint32_t kU2Lo = 0xB73FBE0Bu;   // (-b, -a)
 constexpr uint32_t kU2Hi = 0x3E0B373Fu;   // (a, b)
 
-// The codes at bits 0-1 and 8-9 of v (other bits ignored) -> their centroids as an fp16 pair.  The
-// selector's nibbles are 2c0, 2c0 + 1, 2c1, 2c1 + 1: (c0 | c1 << 8) * 0x22 + 0x1010.
-__device__ __forceinline__ uint32_t u2_lookup(uint32_t v) {
-    return prmt(kU2Lo, kU2Hi, (v & 0x0303u) * 0x22u + 0x1010u);
+// Selectors of field k of all four bytes of x at once: byte b of the result is the selector pair
+// (2c, 2c + 1) of that byte's code c, so its low half looks up bytes 0 and 1, its high half bytes
+// 2 and 3 (no carries cross a byte: 0x22 c + 0x10 <= 0x76).
+__device__ __forceinline__ uint32_t u2_selectors(uint32_t x, int k) {
+    return ((x >> (2 * k)) & 0x03030303u) * 0x22u + 0x10101010u;
 }
 
-// The 8 codes of a 16-bit group h (dims 0..3 in byte 0, 4..7 in byte 1, dim 4j + k at bits 2k of
-// byte j) -> 4 fp16 pairs (dim k, dim k + 4), k = 0..3: the order unpack_word gives INT4 nibbles.
+// One 16-bit group h -> its 4 fp16 pairs (dim k, dim k + 4), one selector per pair.
 __device__ __forceinline__ void unpack_u2(uint32_t h, uint32_t (&o)[4]) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = u2_lookup(h >> (2 * k));
+    for (int k = 0; k < 4; ++k) o[k] = prmt(kU2Lo, kU2Hi, u2_selectors(h, k));
 }
 
-// The same 8 dims of two rows a and b: o[i] = (a's dim i, b's dim i), i = 0..7.
-__device__ __forceinline__ void unpack_u2_pair(uint32_t ha, uint32_t hb, uint32_t (&o)[8]) {
-    const uint32_t y0 = prmt(ha, hb, 0x0040u), y1 = prmt(ha, hb, 0x0051u);   // (a.byte j, b.byte j)
+// Two 16-bit groups packed in x (group a in the low half, b in the high half; dims 0..3 of a group
+// in its byte 0, 4..7 in its byte 1, dim 4j + k at bits 2k of byte j) -> 4 fp16 pairs each, (dim k,
+// dim k + 4), k = 0..3: the order unpack_word gives INT4 nibbles.
+__device__ __forceinline__ void unpack_u2_x2(uint32_t x, uint32_t (&oa)[4], uint32_t (&ob)[4]) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        o[k] = u2_lookup(y0 >> (2 * k));
-        o[4 + k] = u2_lookup(y1 >> (2 * k));
+        const uint32_t s = u2_selectors(x, k);
+        oa[k] = prmt(kU2Lo, kU2Hi, s);
+        ob[k] = prmt(kU2Lo, kU2Hi, s >> 16);
+    }
+}
+
+// The same 8 dims of two rows a and b (16-bit groups ha, hb): o[i] = (a's dim i, b's dim i).
+__device__ __forceinline__ void unpack_u2_pair(uint32_t ha, uint32_t hb, uint32_t (&o)[8]) {
+    const uint32_t y = prmt(ha, hb, 0x5140u);   // a.byte 0, b.byte 0, a.byte 1, b.byte 1
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t s = u2_selectors(y, k);
+        o[k] = prmt(kU2Lo, kU2Hi, s);
+        o[4 + k] = prmt(kU2Lo, kU2Hi, s >> 16);
     }
 }
 

@@ -60,15 +60,18 @@ struct AttnParams {
     float softmax_scale;
     float c;                  // fp32(1 / sqrt(head_size))
     // options of the unified-attention interface, on the scaled logit s of key j at query position
-    // pos, in log2 units (x = s log2 e): x <- C tanh(x / C), x <- x + slope log2e (j - pos), key
-    // visible only if pos - j <= window_left
-    int opts;                 // kOptWindow | kOptSoftcap | kOptAlibi
+    // pos, in log2 units (x = s log2 e): x <- C tanh(x / C), x <- x + slope log2e (j - pos),
+    // x <- x + qq_bias[pos - c][j - c] log2e for the keys j >= c of the query chunk (c its first
+    // position), key visible only if pos - j <= window_left
+    int opts;                 // kOptWindow | kOptSoftcap | kOptAlibi | kOptQQ
     int window_left;
     float cap_l2;             // C = softcap log2 e
     float inv_cap_l2;         // 1 / C
     const float* alibi;       // [Hq] slopes (natural-log units)
+    const float* qq_bias;     // [rows >= max_query_len][qq_stride] (natural-log units)
+    int qq_stride;            // elements per row, >= max_query_len
 };
-constexpr int kOptWindow = 1, kOptSoftcap = 2, kOptAlibi = 4;
+constexpr int kOptWindow = 1, kOptSoftcap = 2, kOptAlibi = 4, kOptQQ = 8;
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_write(const WriteParams& p, int head_size, DType dt, cudaStream_t stream);

@@ -122,6 +122,31 @@ def test_attention_validation_and_workspace_policy(lib):
     assert lib.kv_int4_attention_segment_len(4096, 1 << 20, 0) == 4096   # ceiling
 
 
+def test_options_validation(lib):
+    class Opts(ctypes.Structure):
+        _fields_ = [("window_left", ctypes.c_int32), ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
+                    ("qq_bias", ctypes.c_void_p), ("qq_bias_stride", ctypes.c_int32)]
+
+    f = lib.kv_int4_paged_attention_ex
+    f.restype = ctypes.c_int
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp, i32, i32, i32, ctypes.c_float,
+                  vp, i32, vp, ctypes.c_int, vp, ctypes.c_size_t, vp, ctypes.POINTER(Opts)]
+    fake = 1 << 20
+    base = dict(q=fake, qd=1, nq=16, hq=32, cache=fake, nb=64, h=8, d=128, bs=16, bt=fake, mb=4, sl=fake, qsl=fake,
+                ns=2, mql=8, msl=64, scale=0.088, signs=fake, seg=0, out=fake, od=2, ws=None, wsb=0, st=None)
+
+    def call(opts, **kw):
+        a = dict(base, **kw)
+        return f(*a.values(), ctypes.byref(opts))
+
+    assert call(Opts(-1, -1.0, None, None, 0)) == 1                 # negative softcap
+    assert call(Opts(-1, float("nan"), None, None, 0)) == 1         # non-finite softcap
+    assert call(Opts(-1, 0.0, None, fake, 7)) == 1                  # qq_bias rows shorter than the chunks
+    assert call(Opts(-1, 0.0, None, fake, 8), q=None) == 1          # stride accepted, then the usual checks
+    assert call(Opts(-1, 0.0, None, fake, 8), nq=0) == 0
+
+
 def test_int8_attention_validation(lib):
     f = lib.kv_int8_paged_attention
     f.restype = ctypes.c_int

@@ -249,11 +249,11 @@ def test_contexts_longer_than_max_seq_len_are_clamped_alike():
     assert_attention_close(out, oracle_attention(wl, ref_cache), "clamped contexts")
 
 
-# ------------------------------------------------------------------- window / softcap / ALiBi options
+# ------------------------------------------------------------ window / softcap / ALiBi / qq_bias options
 # kv_int4_paged_attention_ex against the oracle's definition of the same options (decode split-KV
 # walker and prefill kernel alike; several segments per sequence so the options meet the combine).
 
-def _run_opts(wl, window_left=-1, softcap=0.0, slopes=None, segment_len=None):
+def _run_opts(wl, window_left=-1, softcap=0.0, slopes=None, segment_len=None, qq_bias=None):
     import int4_token_head_kv_gb300 as kv
     from gpu_helpers import assert_attention_close, dev, gpu_cache, gpu_write, oracle_cache, status
     cache = gpu_cache(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_size)
@@ -265,12 +265,13 @@ def _run_opts(wl, window_left=-1, softcap=0.0, slopes=None, segment_len=None):
         wl.softmax_scale, torch.from_numpy(wl.signs).to(dev()), max_query_len=wl.max_query_len,
         max_seq_len=wl.max_seq_len, out_dtype=torch.float32, segment_len=seg, window_left=window_left,
         softcap=softcap, alibi_slopes=None if slopes is None else torch.tensor(slopes, dtype=torch.float32,
-                                                                                 device=dev()))
+                                                                                 device=dev()),
+        qq_bias=None if qq_bias is None else torch.from_numpy(np.ascontiguousarray(qq_bias, np.float32)).to(dev()))
     torch.cuda.synchronize()
     import oracle
     ref = oracle.paged_attention(wl.query, oracle_cache(wl), wl.block_tables, wl.seq_lens, wl.query_start_loc,
                                  wl.softmax_scale, wl.signs, window_left=window_left, softcap=softcap,
-                                 alibi_slopes=slopes)
+                                 alibi_slopes=slopes, qq_bias=None if qq_bias is None else np.asarray(qq_bias, np.float32))
     assert_attention_close(out, ref, wl.name + " (options)")
     st = status()
     assert not any(st.values()), st
@@ -302,7 +303,20 @@ def test_alibi(G):
     _run_opts(wl, slopes=slopes)
 
 
+@pytest.mark.parametrize("G", [4, 8])
+def test_qq_bias(G):
+    # a random bias over the 200-query chunks, -inf entries (masked keys) included; decode
+    # sequences take bias[0, 0] on their own key
+    wl = _opts_workload(G, 35)
+    r = np.random.default_rng(35)
+    bias = r.uniform(-4, 4, (200, 208)).astype(np.float32)
+    bias[r.random(bias.shape) < 0.05] = -np.inf
+    np.fill_diagonal(bias, 0.5)   # every query keeps a visible key of its own
+    _run_opts(wl, qq_bias=bias)
+
+
 def test_options_together():
     wl = _opts_workload(4, 34)
     wl.query = (wl.query.float() * 4.0).to(wl.query.dtype)
-    _run_opts(wl, window_left=150, softcap=8.0, slopes=[0.03 * (i + 1) for i in range(32)])
+    _run_opts(wl, window_left=150, softcap=8.0, slopes=[0.03 * (i + 1) for i in range(32)],
+              qq_bias=np.random.default_rng(36).uniform(-2, 2, (200, 200)))
