@@ -199,12 +199,13 @@ namespace {
 
 // Workspace of the decode path, in 256-byte-aligned regions:
 //   meta  [num_seqs + 1] int32             first unit of each sequence
+//   ptile [num_seqs + 1] int32             first prefill query tile of each sequence
 //   q     [num_seqs, qrec_words]           rotated-query records
 //   po    [units, 8, po_floats]            unnormalised partial outputs
 //   pml   [units, 8, 16] fp32              partial (max, sum) per column
 // units <= num_seqs * ceil(max_seq_len / segment_len).
 struct WsLayout {
-    size_t meta, q, po, pml, total;
+    size_t meta, ptile, q, po, pml, total;
     int64_t records;   // most partial records of one (sequence, kv head)
 };
 
@@ -219,7 +220,8 @@ bool ws_layout(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int
     const int64_t max_units = (int64_t)num_seqs * seg_per_seq;
     w->records = seg_per_seq * (8 / num_kv_heads);
     w->meta = 0;
-    w->q = align256((size_t)(num_seqs + 1) * 4);
+    w->ptile = align256((size_t)(num_seqs + 1) * 4);
+    w->q = w->ptile + align256((size_t)(num_seqs + 1) * 4);
     w->po = w->q + align256((size_t)num_seqs * decode_qrec_words(head_size, num_kv_heads, G) * 4);
     w->pml = w->po + align256((size_t)max_units * 8 * decode_po_floats(head_size, G) * 4);
     w->total = w->pml + (size_t)max_units * 8 * 16 * 4;
@@ -277,6 +279,7 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
     p.out = out;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.ws_meta = reinterpret_cast<int32_t*>(ws + w.meta);
+    p.ws_ptile = reinterpret_cast<int32_t*>(ws + w.ptile);
     p.ws_q = reinterpret_cast<uint32_t*>(ws + w.q);
     p.qrec_words = (int)decode_qrec_words(head_size, num_kv_heads, G);
     p.ws_po = reinterpret_cast<float*>(ws + w.po);
@@ -300,6 +303,16 @@ kv_int4_status paged_attention_impl(int bits, const void* q, kv_int4_dtype q_dty
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.seg_len = seg;
     p.len_cap = (int)len_cap;
+    {   // prefill grid: at most num_q_tokens / 2 sequences have two or more queries, and their
+        // tiles of BQ tokens cover at most num_q_tokens queries.  When one grid slice per sequence
+        // is not much larger than that bound, it needs no tile lookup and is taken.
+        const int64_t bq = 128 / G;
+        const int64_t per_seq = ((int64_t)max_query_len + bq - 1) / bq;
+        const int64_t npf = std::min<int64_t>(num_seqs, num_q_tokens / 2);
+        const int64_t bound = std::max<int64_t>(1, std::min((num_q_tokens + npf * (bq - 1)) / bq, npf * per_seq));
+        const int64_t sliced = (int64_t)num_seqs * per_seq;
+        p.pf_tiles_cap = (sliced <= bound + bound / 4 || bound > (1 << 24)) ? 0 : (int)bound;
+    }
     p.softmax_scale = softmax_scale;
     p.c = (float)(1.0 / std::sqrt((double)head_size));
     p.opts = 0;

@@ -528,6 +528,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
         if (blk >= 0 && (int64_t)blk < p.num_blocks) bulk_prefetch_l2(p.cache + (int64_t)blk * stage_bytes, stage_bytes);
     }
     griddep_wait();   // the query records, and through them the cache, come from earlier kernels
+    if (blockIdx.x == 0 && p.max_query_len > 1 && p.pf_tiles_cap > 0) {
+        // The prefill's tile index: sequence b's first query tile among the batch's prefill tiles
+        // (tiles of 128 / G tokens over its first min(q_len, max_query_len) queries; none for q_len
+        // <= 1).  Clamped to the grid the host launches, which bounds the total from the query
+        // count; a batch past it (inconsistent metadata) is counted.
+        const int bq = kPrefillRows / G;
+        auto tiles_of = [&](int b) -> uint32_t {
+            const int ql = __ldg(p.qsl + b + 1) - __ldg(p.qsl + b);
+            return ql > 1 ? (uint32_t)((min(ql, p.max_query_len) + bq - 1) / bq) : 0u;
+        };
+        uint32_t mine = 0;
+        for (int b = b0; b < b1; ++b) mine += tiles_of(b);
+        unsigned long long total;
+        uint32_t t = (uint32_t)block_exclusive_scan(mine, wsum, &total);
+        const uint32_t cap = (uint32_t)p.pf_tiles_cap;
+        for (int b = b0; b < b1; ++b) {
+            p.ws_ptile[b] = (int)min(t, cap);
+            t += tiles_of(b);
+        }
+        if (threadIdx.x == 0) {
+            p.ws_ptile[N] = (int)min((uint32_t)total, cap);
+            if (total > cap) count_status(p.status, 2);
+        }
+    }
     if (blockIdx.x == 0) {   // the combine's sequence index
         uint32_t ub = ub_t;
         for (int b = b0; b < b1; ++b) {

@@ -49,7 +49,7 @@
 namespace kvi4 {
 namespace {
 
-constexpr int kPfRows = 128;                  // query rows per CTA (the MMA M)
+constexpr int kPfRows = kPrefillRows;         // query rows per CTA (the MMA M)
 constexpr int kPfKeys = 128;                  // keys per tile (the S MMA N, the P.V MMA K)
 constexpr int kPfPairs = 2;                   // fp16 K/V tile pairs in shared memory
 constexpr int kPfKRing = 4;                   // key-tile records (K scales, "K converted") in flight
@@ -214,7 +214,10 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // swizzle the tensor-core descriptors expect: the chunk index is XOR-ed with r mod 8.
 __device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
-template <int D, typename QT, typename OT, bool OPTS>
+// TILED: the grid covers the batch's prefill query tiles through the walker's tile index (a batch
+// of many decode sequences); otherwise one grid slice per sequence.  Separate instantiations keep the
+// per-sequence grid's indices plain block coordinates.
+template <int D, typename QT, typename OT, bool OPTS, bool TILED>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap qmap) {
     using Gm = Geo<D>;
     using Ly = PfLayout<D>;
@@ -224,10 +227,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- the CTA's rows; everything up to the barrier set-up exits uniformly
-    const int ntile = (int)(gridDim.x / (unsigned)p.H);
-    const int qtile = ntile - 1 - (int)(blockIdx.x / (unsigned)p.H), h = (int)(blockIdx.x % (unsigned)p.H);
-    const int seq = blockIdx.z;
+    // ---- the CTA's rows; everything up to the barrier set-up exits uniformly.  A sequence's
+    // tiles run in descending order, so its longest rows start first.  Two grids:
+    //  * pf_tiles_cap > 0: tile v of the batch's prefill query tiles (ws_ptile: each sequence's
+    //    first tile), found by a 32-way search in each warp;
+    //  * otherwise one grid slice (blockIdx.z) per sequence, ntile tiles each.
+    const int v = (int)(blockIdx.x / (unsigned)p.H), h = (int)(blockIdx.x % (unsigned)p.H);
+    int seq, qtile;
+    if constexpr (TILED) {
+        const int32_t* ptile = p.ws_ptile;
+        int lo = 0, hi = p.num_seqs + 1;   // ptile[lo] <= v < ptile[hi], ptile[num_seqs + 1] = infinity
+        while (hi - lo > 1) {
+            const int step = (hi - lo + 31) / 32;
+            const int idx = lo + step * lane;
+            const unsigned le = __ballot_sync(0xffffffffu, idx < hi && __ldg(ptile + idx) <= v);
+            lo += step * (31 - __clz(le));   // lane 0 (ptile[lo] <= v) is always set
+            hi = min(hi, lo + step);
+        }
+        if (lo >= p.num_seqs) return;   // past the batch's last tile (ptile[num_seqs] = the total)
+        seq = lo;
+        qtile = __ldg(ptile + seq + 1) - 1 - v;
+    } else {
+        seq = blockIdx.z;
+        qtile = (int)(gridDim.x / (unsigned)p.H) - 1 - v;
+    }
     const int q0 = __ldg(p.qsl + seq);
     const int qlen = __ldg(p.qsl + seq + 1) - q0;
     if (qlen <= 1) return;   // decode sequences (and empty ones) are not this kernel's
@@ -900,19 +923,26 @@ cudaError_t query_map(const AttnParams& p, CUtensorMap* map) {
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, typename QT, typename OT, bool OPTS>
-cudaError_t launch_prefill_t(const AttnParams& p, int max_query_len, cudaStream_t stream) {
+template <int D, typename QT, typename OT, bool OPTS, bool TILED>
+cudaError_t launch_prefill_grid(const AttnParams& p, int max_query_len, cudaStream_t stream) {
     const size_t smem = PfLayout<D>::kBytes;
-    cudaError_t err = opt_in_smem<prefill_kernel<D, QT, OT, OPTS>>(smem);
+    cudaError_t err = opt_in_smem<prefill_kernel<D, QT, OT, OPTS, TILED>>(smem);
     if (err != cudaSuccess) return err;
     if (p.num_q_tokens <= 0 || kPfRows % p.G != 0) return cudaErrorInvalidValue;
     CUtensorMap qmap;
     err = query_map<D, QT>(p, &qmap);
     if (err != cudaSuccess) return err;
     const int BQ = kPfRows / p.G;
-    dim3 grid((unsigned)(((max_query_len + BQ - 1) / BQ) * p.H), 1, p.num_seqs);
-    prefill_kernel<D, QT, OT, OPTS><<<grid, kPfThreads, smem, stream>>>(p, qmap);
+    const dim3 grid = TILED ? dim3((unsigned)p.pf_tiles_cap * (unsigned)p.H)   // the walker's tile index
+                            : dim3((unsigned)(((max_query_len + BQ - 1) / BQ) * p.H), 1, p.num_seqs);
+    prefill_kernel<D, QT, OT, OPTS, TILED><<<grid, kPfThreads, smem, stream>>>(p, qmap);
     return cudaGetLastError();
+}
+
+template <int D, typename QT, typename OT, bool OPTS>
+cudaError_t launch_prefill_t(const AttnParams& p, int max_query_len, cudaStream_t stream) {
+    return p.pf_tiles_cap > 0 ? launch_prefill_grid<D, QT, OT, OPTS, true>(p, max_query_len, stream)
+                              : launch_prefill_grid<D, QT, OT, OPTS, false>(p, max_query_len, stream);
 }
 
 template <int D, typename QT, bool OPTS>

@@ -9,6 +9,7 @@
 namespace kvi4 {
 
 constexpr int kBlockSize = 16;   // tokens per cache block
+constexpr int kPrefillRows = 128;   // query rows (tokens x q heads of one kv head) per prefill CTA
 
 // Upper bound of every pipeline wait inside a kernel (ns).  A wait that runs out records
 // KV_INT4_STAT_WAIT_TIMEOUT and the kernel winds down instead of spinning forever.
@@ -38,6 +39,8 @@ struct AttnParams {
     const float* signs;
     void* out;
     int32_t* ws_meta;         // [num_seqs + 1] first split-KV unit of each sequence (exclusive prefix)
+    int32_t* ws_ptile;        // [num_seqs + 1] first prefill query tile of each sequence (exclusive
+                              // prefix, written by the walker's CTA 0 when pf_tiles_cap > 0)
     uint32_t* ws_q;           // [num_seqs, qrec_words] rotated-query records of the decode sequences
     float* ws_po;             // [units, 8 warps, po_floats] unnormalised partial outputs (fragment order)
     float* ws_pml;            // [units, 8 warps, 8 columns, 2] partial (max in log2 units, sum)
@@ -52,6 +55,9 @@ struct AttnParams {
     int max_blocks_per_seq;
     int seg_len;              // decode split-KV segment (unit) length in tokens, a multiple of 16
     int len_cap;              // decode context lengths are clamped to this (max_seq_len, block table)
+    int pf_tiles_cap;         // > 0: the prefill grid covers this many query tiles per kv head (a
+                              // bound on the batch's total) through ws_ptile; 0: one grid slice per
+                              // sequence (few empty slices, no lookup)
     int combine_warps;        // combine warps per (sequence, kv head): a power of two, 1..16
     int qrec_words;           // 32-bit words of one rotated-query record
     uint32_t seg_rcp;         // floor(2^32 / seg_len), for fast_div

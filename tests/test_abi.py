@@ -103,14 +103,14 @@ def test_attention_validation_and_workspace_policy(lib):
     def a256(x):
         return (x + 255) // 256 * 256
 
-    # 8 seqs x 131072 tokens in segments of 4096: per sequence its first segment index and its
-    # rotated-query record (8 kv heads x 128 x 8 (G = 8) or 4 fp16x2 words, then Hq logit factors
+    # 8 seqs x 131072 tokens in segments of 4096: per sequence its first segment index, its first
+    # prefill query tile and its rotated-query record (8 kv heads x 128 x 8 (G = 8) or 4 fp16x2 words, then Hq logit factors
     # and Hq query sums); per segment 8 warps x (1024 accumulators for G = 8, 512 otherwise) and
     # 8 (max, sum) pairs
     units = 8 * 32
     for hq, acc, qw in ((64, 1024, 8), (32, 512, 4)):
         rec = (8 * 128 * qw + 2 * hq) * 4
-        assert ws(hq, 8, 128, 8, 131072, 4096) == (a256(9 * 4) + a256(8 * rec) + a256(units * 8 * acc * 4)
+        assert ws(hq, 8, 128, 8, 131072, 4096) == (2 * a256(9 * 4) + a256(8 * rec) + a256(units * 8 * acc * 4)
                                                    + units * 8 * 16 * 4)
     assert ws(32, 8, 128, 0, 4096, 0) == 0          # no sequences
     assert ws(32, 3, 128, 8, 4096, 0) == 0          # heads do not group

@@ -55,6 +55,22 @@ def _run_case(wl, out_dtype=torch.float32, segment_len=None, seqs=None, kv_heads
     return out, err
 
 
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_prefill_chunks_among_many_decodes(G):
+    # a few ragged prefill chunks scattered through a large decode batch: the prefill grid covers the
+    # batch's query tiles, found through the walker's per-sequence tile index, not every sequence
+    r = np.random.default_rng(40 + G)
+    n = 150
+    qlens = np.ones(n, dtype=np.int64)
+    qlens[[3, 77, 149]] = [100, 33, 257]
+    qlens[120] = 0 if G == 4 else 1     # an empty query range in the middle
+    lens = r.integers(1, 300, n)
+    lens = np.maximum(lens, qlens + r.integers(0, 40, n) * (qlens > 1))
+    wl = workloads.make_attention_workload("pf_scatter", lens.tolist(), qlens.tolist(), 2 * G, 2, 128, seed=40 + G,
+                                           segment_len=64)
+    _run_case(wl)
+
+
 def test_tiny_write_decode():
     wl = workloads.tiny_write_decode()
     _run_case(wl)
