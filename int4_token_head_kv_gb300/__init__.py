@@ -65,6 +65,9 @@ def _load():
     lib.kv_int4_paged_attention.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp,
                                             i32, i32, i32, f32, vp, i32, vp, ctypes.c_int, vp, szt, vp]
     lib.kv_int4_paged_attention.restype = ctypes.c_int
+    lib.kv_int4_paged_attention_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp,
+                                                    vp, i32, i32, i32, f32, vp, i32, vp, ctypes.c_int, vp]
+    lib.kv_int4_paged_attention_noalloc.restype = ctypes.c_int
     lib.kv_int4_paged_attention_ex.argtypes = lib.kv_int4_paged_attention.argtypes + [ctypes.POINTER(AttnOptions)]
     lib.kv_int4_paged_attention_ex.restype = ctypes.c_int
     lib.kv_int8_paged_attention.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp,
@@ -258,6 +261,39 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
     else:
         st = load().kv_int4_paged_attention(*args)
         _check("kv_int4_paged_attention", st)
+    return out
+
+
+def kv_int4_paged_attention_noalloc(query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,
+                                    seq_lens: torch.Tensor, query_start_loc: torch.Tensor, softmax_scale: float,
+                                    rht_signs: torch.Tensor, max_query_len: int, max_seq_len: int, out=None,
+                                    out_dtype=None, segment_len: int = 0, stream=None) -> torch.Tensor:
+    """kv_int4_paged_attention without a workspace: the split-KV partials live in the library's fixed
+    device scratch array (calls that overlap on the GPU must be serialised).  ``out`` is allocated
+    here when not given; pass it to keep the call free of allocations."""
+    _cuda(query, "query", (torch.float16, torch.bfloat16))
+    _cuda(kv_cache, "kv_cache", (torch.uint8,))
+    _cuda(block_tables, "block_tables", (torch.int32,))
+    _cuda(seq_lens, "seq_lens", (torch.int32,))
+    _cuda(query_start_loc, "query_start_loc", (torch.int32,))
+    _cuda(rht_signs, "rht_signs", (torch.float32,))
+    Nq, Hq, d = query.shape
+    NB, two, bs, H, rb = kv_cache.shape
+    S = seq_lens.shape[0]
+    if two != 2 or rb != kv_int4_row_bytes(d) or rht_signs.shape != (d,):
+        raise ValueError("kv_cache / rht_signs do not match the query's head size")
+    if query_start_loc.shape != (S + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and query_start_loc [num_seqs + 1]")
+    if out is None:
+        out = torch.empty((Nq, Hq, d), dtype=out_dtype or query.dtype, device=query.device)
+    _cuda(out, "out", tuple(_DTYPES))
+    if out.shape != query.shape:
+        raise ValueError("out must have the query's shape")
+    st = load().kv_int4_paged_attention_noalloc(
+        query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs, block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
+        float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype], _stream(stream))
+    _check("kv_int4_paged_attention_noalloc", st)
     return out
 
 

@@ -157,3 +157,21 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
                t["tables"].data_ptr(), 1, t["lens"].data_ptr(), t["qsl"].data_ptr(), 4096, 1, 32768,
                wl.softmax_scale, t["signs"].data_ptr(), seg, out.data_ptr(), 2, torch.cuda.current_stream().cuda_stream)
         assert rc == KV_INT4_EWORKSPACE
+
+
+def test_python_binding_matches_regular_entry_point():
+    # the binding's kv_int4_paged_attention_noalloc marshals the same call: bit-identical output
+    import int4_token_head_kv_gb300 as kv
+    from gpu_helpers import dev, gpu_attention, gpu_cache, gpu_write
+    wl = workloads.make_attention_workload("noalloc_py", [900, 40, 2500], [1, 1, 1], 16, 4, 128, seed=23,
+                                           segment_len=256)
+    cache = gpu_cache(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_size)
+    gpu_write(wl.key, wl.value, wl.slot_mapping, wl.signs, cache)
+    ref = gpu_attention(wl, cache, out_dtype=torch.float32, segment_len=256)
+    got = kv.kv_int4_paged_attention_noalloc(
+        wl.query.to(dev()), cache, torch.from_numpy(wl.block_tables).to(dev()),
+        torch.from_numpy(wl.seq_lens).to(dev()), torch.from_numpy(wl.query_start_loc).to(dev()),
+        wl.softmax_scale, torch.from_numpy(wl.signs).to(dev()), max_query_len=wl.max_query_len,
+        max_seq_len=wl.max_seq_len, out_dtype=torch.float32, segment_len=256)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
