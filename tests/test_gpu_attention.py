@@ -331,6 +331,19 @@ def test_qq_bias(G):
     _run_opts(wl, qq_bias=bias)
 
 
+@pytest.mark.parametrize("tiled", [True, False])
+def test_options_head64(tiled):
+    # head size 64 with every option; many decode sequences put the prefill on its tile grid, a
+    # prefill-only batch on one slice per sequence
+    lens, qlens = ([400, 90, 1200, 33, 700, 64, 250, 900], [1, 1, 130, 1, 1, 64, 1, 1]) if tiled else \
+        ([400, 1200, 300], [100, 130, 64])
+    wl = workloads.make_attention_workload("opts64", lens, qlens, 16, 4, 64, seed=37, segment_len=128)
+    wl.query = (wl.query.float() * 3.0).to(wl.query.dtype)
+    r = np.random.default_rng(37)
+    _run_opts(wl, window_left=200, softcap=10.0, slopes=[0.05 * (i + 1) for i in range(16)],
+              qq_bias=r.uniform(-1.5, 1.5, (130, 136)))
+
+
 def test_options_together():
     wl = _opts_workload(4, 34)
     wl.query = (wl.query.float() * 4.0).to(wl.query.dtype)
