@@ -46,6 +46,12 @@ def test_int8_write_page_shapes_bit_exact(num_tokens, num_heads, head_size, dtyp
     _check(wl, fill=0xA5)
 
 
+@pytest.mark.parametrize("num_heads", [3, 16, 64])
+def test_int8_write_other_head_counts(num_heads):
+    wl = workloads.random_write(37, num_heads, 128, seed=60 + num_heads)
+    _check(wl, fill=0x5A)
+
+
 def test_int8_write_throughput_workload_full_size():
     _check(workloads.write_throughput())
 

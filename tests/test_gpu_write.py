@@ -47,6 +47,14 @@ def test_write_page_shapes_bit_exact(num_tokens, num_heads, head_size, dtype):
     _check_write(wl, fill=0xA5)   # canary: untouched slots must keep it
 
 
+@pytest.mark.parametrize("num_heads", [2, 3, 16, 64])
+def test_write_other_head_counts(num_heads):
+    # up to 64 kv heads: 3 takes the general vector index, 16 the grouped bulk stores at their
+    # limit, 64 the per-thread stores
+    wl = workloads.random_write(37, num_heads, 128, seed=50 + num_heads)
+    _check_write(wl, fill=0x5A)
+
+
 @pytest.mark.parametrize("num_tokens", [1, 16])
 def test_write_round_trip_shape(num_tokens):
     wl = workloads.random_write(num_tokens, 4, 128, seed=42, scale=0.5)
