@@ -11,7 +11,9 @@ the whole cache (query rotation, split-KV walker, segment combine).
             (1.14 GB) is larger than L2, so no flush is needed between steps.
   e2e       the same bytes over a step timed through the public API from pinned host buffers: each
             step copies its new K/V, slots, queries and tables host->device (one copy of the packed
-            step inputs) and the output device->host, replayed as one CUDA graph per step.
+            step inputs) and its output device->host.  The copies run on two copy streams beside the
+            compute (one CUDA graph per step), double-buffered as a serving loop runs them;
+            serial_value keeps the in-order figure.
   roofline  the attention call (query rotation + walker + combine) timed back to back on its stream,
             algorithmic bytes per call over its CUDA-event time, against MEASURED_PEAKS.json's HBM
             copy bandwidth; ``traffic`` is the ncu DRAM byte count per call from profiles/traffic.json,
@@ -316,12 +318,97 @@ def _decode_steps(torch, kv, wl, dev, args, replicas, world, with_e2e=False, sam
         for i in range(args.warmup):
             e2e_graphs[i % replicas].replay()
         barrier()
-        e2e_ms = _timed(torch, stream, lambda i: e2e_graphs[i % replicas].replay(), args.steps) / args.steps
+        e2e_serial_ms = _timed(torch, stream, lambda i: e2e_graphs[i % replicas].replay(), args.steps) / args.steps
         barrier()
-        res.update(e2e_ms=max_over_ranks(e2e_ms, dev), e2e_eager_ms=e2e_eager_ms, h2d=h2d, d2h=d2h)
+        del e2e_graphs
+        e2e_ms = _pipelined_e2e(torch, kv, wl, t, caches, replicas, seg, ws, out, host, args, barrier)
+        res.update(e2e_ms=max_over_ranks(e2e_ms, dev), e2e_serial_ms=max_over_ranks(e2e_serial_ms, dev),
+                   e2e_eager_ms=e2e_eager_ms, h2d=h2d, d2h=d2h)
     del caches, ws, t
     torch.cuda.empty_cache()
     return res
+
+
+def _pipelined_e2e(torch, kv, wl, t, caches, replicas, seg, ws, out, host, args, barrier):
+    """End-to-end steps as a serving loop runs them: the inputs of a step go up on one copy stream and
+    the output of the step before comes back on another while the current step computes (two device
+    input buffers and two output buffers, pinned host buffers, the compute of each step one CUDA
+    graph).  Every step's upload and read-back lies inside the timed region, which ends when the last
+    read-back has landed.  Returns ms per step."""
+    dev = out.device
+    compute = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    base = t["_buf"]
+    bufs = [base, torch.empty_like(base)]
+    names = ("k", "v", "slots", "q", "tables", "lens", "qsl")
+    views = []
+    for b in bufs:
+        vw = {}
+        for n in names:
+            off = t[n].data_ptr() - base.data_ptr()
+            nb = t[n].numel() * t[n].element_size()
+            vw[n] = b[off:off + nb].view(t[n].dtype).view(t[n].shape)
+        views.append(vw)
+    outs = [out, torch.empty_like(out)]
+    host_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    bufs[1].copy_(host)
+    torch.cuda.synchronize()
+
+    def step(r, b):
+        v = views[b]
+        kv.kv_int4_write(v["k"], v["v"], v["slots"], t["signs"], caches[r])
+        kv.kv_int4_paged_attention(v["q"], caches[r], v["tables"], v["lens"], v["qsl"], wl.softmax_scale, t["signs"],
+                                   max_query_len=1, max_seq_len=wl.max_seq_len, out=outs[b], segment_len=seg,
+                                   workspace=ws)
+
+    graphs = {}
+    for r in range(replicas):
+        for b in range(2):
+            step(r, b)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(r, b)
+            graphs[r, b] = g
+    ev = lambda: torch.cuda.Event()   # noqa: E731
+    uploaded, computed, landed = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def run(n, timed):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if timed:
+            start.record(compute)
+        up.wait_stream(compute)
+        down.wait_stream(compute)
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(computed[b])          # step i - 2 has read input buffer b
+                bufs[b].copy_(host, non_blocking=True)
+                uploaded[b].record(up)
+            compute.wait_event(uploaded[b])
+            if i >= 2:
+                compute.wait_event(landed[b])           # step i - 2's output has left buffer b
+            graphs[i % replicas, b].replay()
+            computed[b].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[b])
+                host_outs[b].copy_(outs[b], non_blocking=True)
+                landed[b].record(down)
+        compute.wait_stream(up)
+        compute.wait_stream(down)
+        if timed:
+            end.record(compute)
+        return start, end
+
+    run(max(3, args.warmup), False)
+    barrier()
+    start, end = run(args.steps, True)
+    end.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    barrier()
+    del graphs
+    return ms
 
 
 def _gbs(nbytes, ms):
@@ -371,7 +458,12 @@ def _gpu_arm(args):
                    "eager_value": round(_gbs(attn_bytes * world, r["eager_ms"]), 2)},
         "e2e": {"value": round(_gbs(attn_bytes * world, r["e2e_ms"]), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 5),
-                "timing": "one CUDA graph per step: packed input upload, write, attention, output read-back",
+                "serial_ms_per_step": round(r["e2e_serial_ms"], 5),
+                "serial_value": round(_gbs(attn_bytes * world, r["e2e_serial_ms"]), 2),
+                "timing": "serving loop: each step's packed inputs uploaded and the previous step's output read "
+                          "back on two copy streams while the step (write + attention, one CUDA graph) computes; "
+                          "double-buffered pinned host and device buffers; every copy inside the timed region. "
+                          "serial_*: upload, write, attention and read-back in order in one graph per step",
                 "eager_ms_per_step": round(r["e2e_eager_ms"], 5),
                 "eager_value": round(_gbs(attn_bytes * world, r["e2e_eager_ms"]), 2)},
         "roofline": _roof(_gbs(attn_bytes, r["attn_ms"]), hbm, kind, _traffic("long_context_decode"),
