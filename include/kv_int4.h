@@ -359,6 +359,24 @@ kv_int4_status kv_int4_paged_attention_noalloc(const void* q, kv_int4_dtype q_dt
                                                kv_int4_dtype out_dtype, kv_int4_stream_t stream);
 
 /*
+ * kv_int4_paged_attention_noalloc_ex -- the no-allocation attention with the options of
+ * kv_int4_paged_attention_ex (options NULL: exactly kv_int4_paged_attention_noalloc).  Segment
+ * length, scratch array and error behaviour as kv_int4_paged_attention_noalloc; the options as
+ * kv_int4_paged_attention_ex.
+ */
+kv_int4_status kv_int4_paged_attention_noalloc_ex(const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens,
+                                                  int32_t num_q_heads, const uint8_t* cache,
+                                                  int64_t num_blocks, int32_t num_kv_heads,
+                                                  int32_t head_size, int32_t block_size,
+                                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                  const int32_t* seq_lens, const int32_t* query_start_loc,
+                                                  int32_t num_seqs, int32_t max_query_len,
+                                                  int32_t max_seq_len, float softmax_scale,
+                                                  const float* rht_signs, int32_t segment_len, void* out,
+                                                  kv_int4_dtype out_dtype, kv_int4_stream_t stream,
+                                                  const kv_int4_attn_options* options);
+
+/*
  * Copy the current device's status counters (KV_INT4_STAT_COUNT uint32 values) to the HOST array
  * counts.  Synchronises the stream first.  The counters keep counting until cleared.
  */

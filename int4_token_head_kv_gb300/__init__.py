@@ -68,6 +68,9 @@ def _load():
     lib.kv_int4_paged_attention_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp,
                                                     vp, i32, i32, i32, f32, vp, i32, vp, ctypes.c_int, vp]
     lib.kv_int4_paged_attention_noalloc.restype = ctypes.c_int
+    lib.kv_int4_paged_attention_noalloc_ex.argtypes = lib.kv_int4_paged_attention_noalloc.argtypes + [
+        ctypes.POINTER(AttnOptions)]
+    lib.kv_int4_paged_attention_noalloc_ex.restype = ctypes.c_int
     lib.kv_int4_paged_attention_ex.argtypes = lib.kv_int4_paged_attention.argtypes + [ctypes.POINTER(AttnOptions)]
     lib.kv_int4_paged_attention_ex.restype = ctypes.c_int
     lib.kv_int8_paged_attention.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, i32, i32, i32, vp, i32, vp, vp,
@@ -206,6 +209,24 @@ def kv_int4_attention_workspace_bytes(num_q_heads: int, num_kv_heads: int, head_
                                                       max_seq_len, segment_len))
 
 
+def _options(Hq, max_query_len, window_left, softcap, alibi_slopes, qq_bias):
+    """kv_int4_attn_options for the given keywords, or None when none is set."""
+    if window_left < 0 and softcap == 0.0 and alibi_slopes is None and qq_bias is None:
+        return None
+    if alibi_slopes is not None:
+        _cuda(alibi_slopes, "alibi_slopes", (torch.float32,))
+        if alibi_slopes.shape != (Hq,):
+            raise ValueError("alibi_slopes must be [num_q_heads]")
+    if qq_bias is not None:
+        _cuda(qq_bias, "qq_bias", (torch.float32,))
+        if qq_bias.dim() != 2 or qq_bias.stride(1) != 1 or qq_bias.shape[0] < max_query_len:
+            raise ValueError("qq_bias must be a row-contiguous [rows >= max_query_len, cols] matrix")
+    return AttnOptions(int(window_left), float(softcap),
+                       alibi_slopes.data_ptr() if alibi_slopes is not None else None,
+                       qq_bias.data_ptr() if qq_bias is not None else None,
+                       int(qq_bias.stride(0)) if qq_bias is not None else 0)
+
+
 def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,
                             seq_lens: torch.Tensor, query_start_loc: torch.Tensor, softmax_scale: float,
                             rht_signs: torch.Tensor, max_query_len: int, max_seq_len: int, out=None,
@@ -243,19 +264,8 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
             block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
             float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype], ws_ptr,
             ws_bytes, _stream(stream))
-    if window_left >= 0 or softcap != 0.0 or alibi_slopes is not None or qq_bias is not None:
-        if alibi_slopes is not None:
-            _cuda(alibi_slopes, "alibi_slopes", (torch.float32,))
-            if alibi_slopes.shape != (Hq,):
-                raise ValueError("alibi_slopes must be [num_q_heads]")
-        if qq_bias is not None:
-            _cuda(qq_bias, "qq_bias", (torch.float32,))
-            if qq_bias.dim() != 2 or qq_bias.stride(1) != 1 or qq_bias.shape[0] < max_query_len:
-                raise ValueError("qq_bias must be a row-contiguous [rows >= max_query_len, cols] matrix")
-        opts = AttnOptions(int(window_left), float(softcap),
-                           alibi_slopes.data_ptr() if alibi_slopes is not None else None,
-                           qq_bias.data_ptr() if qq_bias is not None else None,
-                           int(qq_bias.stride(0)) if qq_bias is not None else 0)
+    opts = _options(Hq, max_query_len, window_left, softcap, alibi_slopes, qq_bias)
+    if opts is not None:
         st = load().kv_int4_paged_attention_ex(*args, ctypes.byref(opts))
         _check("kv_int4_paged_attention_ex", st)
     else:
@@ -267,10 +277,12 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
 def kv_int4_paged_attention_noalloc(query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,
                                     seq_lens: torch.Tensor, query_start_loc: torch.Tensor, softmax_scale: float,
                                     rht_signs: torch.Tensor, max_query_len: int, max_seq_len: int, out=None,
-                                    out_dtype=None, segment_len: int = 0, stream=None) -> torch.Tensor:
+                                    out_dtype=None, segment_len: int = 0, stream=None, window_left: int = -1,
+                                    softcap: float = 0.0, alibi_slopes=None, qq_bias=None) -> torch.Tensor:
     """kv_int4_paged_attention without a workspace: the split-KV partials live in the library's fixed
     device scratch array (calls that overlap on the GPU must be serialised).  ``out`` is allocated
-    here when not given; pass it to keep the call free of allocations."""
+    here when not given; pass it to keep the call free of allocations.  The options as for
+    kv_int4_paged_attention (through kv_int4_paged_attention_noalloc_ex)."""
     _cuda(query, "query", (torch.float16, torch.bfloat16))
     _cuda(kv_cache, "kv_cache", (torch.uint8,))
     _cuda(block_tables, "block_tables", (torch.int32,))
@@ -289,11 +301,15 @@ def kv_int4_paged_attention_noalloc(query: torch.Tensor, kv_cache: torch.Tensor,
     _cuda(out, "out", tuple(_DTYPES))
     if out.shape != query.shape:
         raise ValueError("out must have the query's shape")
-    st = load().kv_int4_paged_attention_noalloc(
-        query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs, block_tables.data_ptr(),
-        block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
-        float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype], _stream(stream))
-    _check("kv_int4_paged_attention_noalloc", st)
+    args = (query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs, block_tables.data_ptr(),
+            block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
+            float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype],
+            _stream(stream))
+    opts = _options(Hq, max_query_len, window_left, softcap, alibi_slopes, qq_bias)
+    if opts is None:
+        _check("kv_int4_paged_attention_noalloc", load().kv_int4_paged_attention_noalloc(*args))
+    else:
+        _check("kv_int4_paged_attention_noalloc_ex", load().kv_int4_paged_attention_noalloc_ex(*args, ctypes.byref(opts)))
     return out
 
 

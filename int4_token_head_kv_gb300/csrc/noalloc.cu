@@ -51,12 +51,12 @@ int32_t scratch_segment_len(int32_t num_q_heads, int32_t num_kv_heads, int32_t h
 
 }  // namespace
 
-extern "C" kv_int4_status kv_int4_paged_attention_noalloc(
+extern "C" kv_int4_status kv_int4_paged_attention_noalloc_ex(
     const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens, int32_t num_q_heads, const uint8_t* cache,
     int64_t num_blocks, int32_t num_kv_heads, int32_t head_size, int32_t block_size, const int32_t* block_tables,
     int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
     int32_t max_query_len, int32_t max_seq_len, float softmax_scale, const float* rht_signs, int32_t segment_len,
-    void* out, kv_int4_dtype out_dtype, kv_int4_stream_t stream) {
+    void* out, kv_int4_dtype out_dtype, kv_int4_stream_t stream, const kv_int4_attn_options* options) {
     size_t need = 0;
     const int32_t seg = scratch_segment_len(num_q_heads, num_kv_heads, head_size, num_seqs, max_seq_len,
                                             segment_len, &need);
@@ -66,9 +66,21 @@ extern "C" kv_int4_status kv_int4_paged_attention_noalloc(
         scratch = scratch_address();
         if (scratch == nullptr) return KV_INT4_ECUDA;
     }
-    return kv_int4_paged_attention(q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads,
-                                   head_size, block_size, block_tables, max_blocks_per_seq, seq_lens,
-                                   query_start_loc, num_seqs, max_query_len, max_seq_len, softmax_scale, rht_signs,
-                                   seg, out, out_dtype, scratch,
-                                   need > 0 ? (size_t)KV_INT4_NOALLOC_SCRATCH_BYTES : 0, stream);
+    return kv_int4_paged_attention_ex(q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads,
+                                      head_size, block_size, block_tables, max_blocks_per_seq, seq_lens,
+                                      query_start_loc, num_seqs, max_query_len, max_seq_len, softmax_scale, rht_signs,
+                                      seg, out, out_dtype, scratch,
+                                      need > 0 ? (size_t)KV_INT4_NOALLOC_SCRATCH_BYTES : 0, stream, options);
+}
+
+extern "C" kv_int4_status kv_int4_paged_attention_noalloc(
+    const void* q, kv_int4_dtype q_dtype, int64_t num_q_tokens, int32_t num_q_heads, const uint8_t* cache,
+    int64_t num_blocks, int32_t num_kv_heads, int32_t head_size, int32_t block_size, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+    int32_t max_query_len, int32_t max_seq_len, float softmax_scale, const float* rht_signs, int32_t segment_len,
+    void* out, kv_int4_dtype out_dtype, kv_int4_stream_t stream) {
+    return kv_int4_paged_attention_noalloc_ex(q, q_dtype, num_q_tokens, num_q_heads, cache, num_blocks, num_kv_heads,
+                                              head_size, block_size, block_tables, max_blocks_per_seq, seq_lens,
+                                              query_start_loc, num_seqs, max_query_len, max_seq_len, softmax_scale,
+                                              rht_signs, segment_len, out, out_dtype, stream, nullptr);
 }

@@ -175,3 +175,31 @@ def test_python_binding_matches_regular_entry_point():
         max_seq_len=wl.max_seq_len, out_dtype=torch.float32, segment_len=256)
     torch.cuda.synchronize()
     assert torch.equal(got, ref)
+
+
+def test_python_binding_with_options_matches_regular_entry_point():
+    # every option (window, softcap, ALiBi, qq_bias) through kv_int4_paged_attention_noalloc_ex on a
+    # batch of decodes and a prefill chunk: bit-identical to kv_int4_paged_attention_ex
+    import int4_token_head_kv_gb300 as kv
+    from gpu_helpers import dev, gpu_cache, gpu_write, status
+    wl = workloads.make_attention_workload("noalloc_opts", [900, 40, 2500, 300], [1, 1, 1, 120], 16, 4, 128,
+                                           seed=24, segment_len=256)
+    wl.query = (wl.query.float() * 3.0).to(wl.query.dtype)
+    cache = gpu_cache(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_size)
+    gpu_write(wl.key, wl.value, wl.slot_mapping, wl.signs, cache)
+    r = np.random.default_rng(24)
+    opts = dict(window_left=500, softcap=10.0,
+                alibi_slopes=torch.tensor([0.02 * (i + 1) for i in range(16)], dtype=torch.float32, device=dev()),
+                qq_bias=torch.from_numpy(r.uniform(-1.5, 1.5, (120, 128)).astype(np.float32)).to(dev()))
+    args = (wl.query.to(dev()), cache, torch.from_numpy(wl.block_tables).to(dev()),
+            torch.from_numpy(wl.seq_lens).to(dev()), torch.from_numpy(wl.query_start_loc).to(dev()),
+            wl.softmax_scale, torch.from_numpy(wl.signs).to(dev()))
+    kw = dict(max_query_len=wl.max_query_len, max_seq_len=wl.max_seq_len, out_dtype=torch.float32, segment_len=256)
+    ref = kv.kv_int4_paged_attention(*args, **kw, **opts)
+    got = kv.kv_int4_paged_attention_noalloc(*args, **kw, **opts)
+    plain = kv.kv_int4_paged_attention_noalloc(*args, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    assert not torch.equal(plain, ref)   # the options reached the kernels
+    st = status()
+    assert not any(st.values()), st
