@@ -109,6 +109,15 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _one_device(*tensors) -> torch.device:
+    """The device all the given CUDA tensors (None entries skipped) are on; the library launches on the
+    current device, so the calls below make it this one."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one CUDA device, got {sorted(map(str, devs))}")
+    return devs.pop()
+
+
 def _cuda(t: torch.Tensor, name: str, dtypes=None) -> torch.Tensor:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -148,9 +157,10 @@ def _rotated_write(fn, row_bytes, key, value, slot_mapping, rht_signs, kv_cache,
     if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.shape[3] != H or \
             kv_cache.shape[4] != row_bytes(d):
         raise ValueError(f"kv_cache must be (NB, 2, bs, {H}, {row_bytes(d)})")
-    st = getattr(load(), fn)(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
-                             rht_signs.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2],
-                             _stream(stream))
+    with torch.cuda.device(_one_device(key, value, slot_mapping, rht_signs, kv_cache)):
+        st = getattr(load(), fn)(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d,
+                                 slot_mapping.data_ptr(), rht_signs.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0],
+                                 kv_cache.shape[2], _stream(stream))
     _check(fn, st)
 
 
@@ -178,8 +188,10 @@ def kv_int8_write(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Te
     if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.shape[3] != H or \
             kv_cache.shape[4] != kv_int8_row_bytes(d):
         raise ValueError(f"kv_cache must be {kv_int8_cache_shape('NB', 'bs', H, d)}")
-    st = load().kv_int8_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d, slot_mapping.data_ptr(),
-                            kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], _stream(stream))
+    with torch.cuda.device(_one_device(key, value, slot_mapping, kv_cache)):
+        st = load().kv_int8_write(key.data_ptr(), value.data_ptr(), _DTYPES[key.dtype], T, H, d,
+                                  slot_mapping.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2],
+                                  _stream(stream))
     _check("kv_int8_write", st)
 
 
@@ -260,17 +272,18 @@ def kv_int4_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    args = (query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs, block_tables.data_ptr(),
-            block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
-            float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype], ws_ptr,
-            ws_bytes, _stream(stream))
     opts = _options(Hq, max_query_len, window_left, softcap, alibi_slopes, qq_bias)
-    if opts is not None:
-        st = load().kv_int4_paged_attention_ex(*args, ctypes.byref(opts))
-        _check("kv_int4_paged_attention_ex", st)
-    else:
-        st = load().kv_int4_paged_attention(*args)
-        _check("kv_int4_paged_attention", st)
+    with torch.cuda.device(_one_device(query, kv_cache, block_tables, seq_lens, query_start_loc, rht_signs, out,
+                                       workspace, alibi_slopes, qq_bias)):
+        args = (query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs,
+                block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S,
+                max_query_len, max_seq_len, float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(),
+                _DTYPES[out.dtype], ws_ptr, ws_bytes, _stream(stream))
+        if opts is not None:
+            st, fn = load().kv_int4_paged_attention_ex(*args, ctypes.byref(opts)), "kv_int4_paged_attention_ex"
+        else:
+            st, fn = load().kv_int4_paged_attention(*args), "kv_int4_paged_attention"
+    _check(fn, st)
     return out
 
 
@@ -301,15 +314,19 @@ def kv_int4_paged_attention_noalloc(query: torch.Tensor, kv_cache: torch.Tensor,
     _cuda(out, "out", tuple(_DTYPES))
     if out.shape != query.shape:
         raise ValueError("out must have the query's shape")
-    args = (query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs, block_tables.data_ptr(),
-            block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
-            float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(), _DTYPES[out.dtype],
-            _stream(stream))
     opts = _options(Hq, max_query_len, window_left, softcap, alibi_slopes, qq_bias)
-    if opts is None:
-        _check("kv_int4_paged_attention_noalloc", load().kv_int4_paged_attention_noalloc(*args))
-    else:
-        _check("kv_int4_paged_attention_noalloc_ex", load().kv_int4_paged_attention_noalloc_ex(*args, ctypes.byref(opts)))
+    with torch.cuda.device(_one_device(query, kv_cache, block_tables, seq_lens, query_start_loc, rht_signs, out,
+                                       alibi_slopes, qq_bias)):
+        args = (query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H, d, bs,
+                block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(), S,
+                max_query_len, max_seq_len, float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(),
+                _DTYPES[out.dtype], _stream(stream))
+        if opts is None:
+            st, fn = load().kv_int4_paged_attention_noalloc(*args), "kv_int4_paged_attention_noalloc"
+        else:
+            st, fn = (load().kv_int4_paged_attention_noalloc_ex(*args, ctypes.byref(opts)),
+                      "kv_int4_paged_attention_noalloc_ex")
+    _check(fn, st)
     return out
 
 
@@ -341,11 +358,12 @@ def kv_int8_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = load().kv_int8_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H,
-                                      d, bs, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
-                                      query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
-                                      float(softmax_scale), segment_len, out.data_ptr(), _DTYPES[out.dtype], ws_ptr,
-                                      ws_bytes, _stream(stream))
+    with torch.cuda.device(_one_device(query, kv_cache, block_tables, seq_lens, query_start_loc, out, workspace)):
+        st = load().kv_int8_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB,
+                                          H, d, bs, block_tables.data_ptr(), block_tables.shape[1],
+                                          seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len,
+                                          max_seq_len, float(softmax_scale), segment_len, out.data_ptr(),
+                                          _DTYPES[out.dtype], ws_ptr, ws_bytes, _stream(stream))
     _check("kv_int8_paged_attention", st)
     return out
 
@@ -379,11 +397,13 @@ def kv_int2_paged_attention(query: torch.Tensor, kv_cache: torch.Tensor, block_t
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = load().kv_int2_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB, H,
-                                      d, bs, block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
-                                      query_start_loc.data_ptr(), S, max_query_len, max_seq_len,
-                                      float(softmax_scale), rht_signs.data_ptr(), segment_len, out.data_ptr(),
-                                      _DTYPES[out.dtype], ws_ptr, ws_bytes, _stream(stream))
+    with torch.cuda.device(_one_device(query, kv_cache, block_tables, seq_lens, query_start_loc, rht_signs, out,
+                                       workspace)):
+        st = load().kv_int2_paged_attention(query.data_ptr(), _DTYPES[query.dtype], Nq, Hq, kv_cache.data_ptr(), NB,
+                                          H, d, bs, block_tables.data_ptr(), block_tables.shape[1],
+                                          seq_lens.data_ptr(), query_start_loc.data_ptr(), S, max_query_len,
+                                          max_seq_len, float(softmax_scale), rht_signs.data_ptr(), segment_len,
+                                          out.data_ptr(), _DTYPES[out.dtype], ws_ptr, ws_bytes, _stream(stream))
     _check("kv_int2_paged_attention", st)
     return out
 

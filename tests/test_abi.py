@@ -208,3 +208,13 @@ def test_package_never_touches_the_oracle():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), fn
                 assert "kv_int4_oracle" not in src, fn
+
+
+def test_binding_requires_one_device():
+    # the binding launches on its tensors' device, so tensors on two devices are refused before any call
+    import torch
+    from int4_token_head_kv_gb300 import _one_device
+    a, b = torch.empty(2), torch.empty(2, device="meta")
+    assert _one_device(a, None, a) == a.device
+    with pytest.raises(ValueError):
+        _one_device(a, b)
