@@ -4,8 +4,9 @@
 // "PR #40835 report", get_kv_cache_shape).
 //
 // Two threads (a lane pair) encode one (token, head, plane) vector in registers.  Every arithmetic
-// step is an explicit round-to-nearest-even operation (intrinsics or packed fp32x2 builtins), so the
-// bytes are bit-exact with the definition in kv_int4.h regardless of how the compiler schedules them:
+// step is an explicit round-to-nearest-even operation (intrinsics, packed fp32x2 builtins, or a
+// mixed-precision FMA that reads a bf16 input in place: fp32 result, one rounding), so the bytes
+// are bit-exact with the definition in kv_int4.h regardless of how the compiler schedules them:
 //   butterflies at strides 1, 2, ..., D/2 (fixed order) -> multiply by c -> min/max ->
 //   s = (max - min) / 15 floored at 1e-6 -> s' = s with the low 4 mantissa bits cleared ->
 //   zp = clamp(rint(-min / s'), 0, 15) -> code = clamp(N(y * (1/s') + zp), 0, 15).
@@ -47,15 +48,33 @@ __device__ __forceinline__ float2 upcast_pair<__half>(uint32_t w) {
     return __half22float2(h);
 }
 
-// Sign tables of the half-vector encoder, per element parity t (shared memory, built once per CTA):
-//   xmask[t][m]  XOR mask for input pair m: bit 31 = sign of element 2m + 1 times (t ? -1 : +1);
-//                bit 15 = sign of element 2m for fp16 inputs (bf16 inputs take it from even[]);
-//   even[k]      (sign of element 2k, sign of element 2(k + D/4)) as +-1.0f.
+// Sign tables of the half-vector encoder (shared memory, built once per CTA):
+//   xmask[t][m]  XOR mask for input pair m and element parity t: bit 31 = sign of element 2m + 1
+//                times (t ? -1 : +1); bit 15 = sign of element 2m for fp16 inputs (bf16 inputs take
+//                it from esign[]);
+//   esign[k + i] (k a multiple of 4) the signs of elements 2m and 2m + 2 as bf16 +-1.0 (low, high
+//                half), m = k + 2(i & 1) in the first half of the pairs (i < 2) or the second
+//                (i >= 2, m + D/4): one 16-byte load gives the even signs of pairs k .. k + 3 of both.
 template <int D>
 struct WriteSigns {
     uint32_t xmask[2][D / 2];
-    float2 even[D / 4];
+    uint32_t esign[D / 4];
 };
+
+// RN(a * b + c) with a the low bf16 half of a2, b the low (HI_B false) or high bf16 half of b2 and c
+// fp32, in one mixed-precision FMA: the bf16 operands are read in place, with no upcast.  With b =
+// +-1 the product is exact and the one rounding is that of the fp32 sum.
+template <bool HI_B>
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a2, uint32_t b2, float c) {
+    float d;
+    if constexpr (!HI_B)
+        asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, al, bl, %3; }"
+            : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    else
+        asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, al, bh, %3; }"
+            : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    return d;
+}
 
 // One thread's half of a rotated vector.  row: the vector's D/2 input pairs (pair m = elements 2m,
 // 2m + 1, low half first) in shared memory; t: this thread's element parity.  With Q = D/4, thread t
@@ -72,20 +91,23 @@ __device__ __forceinline__ void rotate_half(const uint32_t* row, const WriteSign
     for (int k = 0; k < Q; k += 4) {
         const uint4 lo = *reinterpret_cast<const uint4*>(row + k);
         const uint4 hi = *reinterpret_cast<const uint4*>(row + k + Q);
+        const uint4 mlo = *reinterpret_cast<const uint4*>(xm + k);
+        const uint4 mhi = *reinterpret_cast<const uint4*>(xm + k + Q);
         const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
-        const uint32_t ml[4] = {xm[k], xm[k + 1], xm[k + 2], xm[k + 3]};
-        const uint32_t mh[4] = {xm[k + Q], xm[k + Q + 1], xm[k + Q + 2], xm[k + Q + 3]};
+        const uint32_t ml[4] = {mlo.x, mlo.y, mlo.z, mlo.w}, mh[4] = {mhi.x, mhi.y, mhi.z, mhi.w};
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
             // odd element: its sign (and the parity's -1) by XOR while masking out the even half (one
-            // logic op); even element: its bits moved up, the sign applied by the (exact) product of
-            // the FMA
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 a = make_float2(__uint_as_float(wl[e] * 65536u), __uint_as_float(wh[e] * 65536u));
-                const float2 b = make_float2(__uint_as_float((wl[e] ^ ml[e]) & 0xFFFF0000u),
-                                             __uint_as_float((wh[e] ^ mh[e]) & 0xFFFF0000u));
-                P[k + e] = fma_f32x2(a, sg.even[k + e], b);
-            }
+            // logic op); even element: read in place by a mixed-precision FMA with its bf16 sign
+            const uint4 es = *reinterpret_cast<const uint4*>(sg.esign + k);
+            auto odd = [](uint32_t w, uint32_t m) { return __uint_as_float((w ^ m) & 0xFFFF0000u); };
+            P[k] = make_float2(fma_bf16_lo<false>(wl[0], es.x, odd(wl[0], ml[0])),
+                               fma_bf16_lo<false>(wh[0], es.z, odd(wh[0], mh[0])));
+            P[k + 1] = make_float2(fma_bf16_lo<true>(wl[1], es.x, odd(wl[1], ml[1])),
+                                   fma_bf16_lo<true>(wh[1], es.z, odd(wh[1], mh[1])));
+            P[k + 2] = make_float2(fma_bf16_lo<false>(wl[2], es.y, odd(wl[2], ml[2])),
+                                   fma_bf16_lo<false>(wh[2], es.w, odd(wh[2], mh[2])));
+            P[k + 3] = make_float2(fma_bf16_lo<true>(wl[3], es.y, odd(wl[3], ml[3])),
+                                   fma_bf16_lo<true>(wh[3], es.w, odd(wh[3], mh[3])));
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -383,8 +405,12 @@ __global__ void __launch_bounds__(kWriteThreads, WriteShape<BITS>::kMinBlocks)
                            ((__float_as_uint(s1) >> 31) << 31);
         sgn.xmask[0][j] = m;
         sgn.xmask[1][j] = m ^ 0x80000000u;
-        float* ev = reinterpret_cast<float*>(sgn.even);   // element 2j: lane j / Q of pair j % Q
-        ev[2 * (j % (D / 4)) + j / (D / 4)] = s0 < 0.0f ? -1.0f : 1.0f;
+        if ((j & 1) == 0) {   // the bf16 signs of elements 2j and 2j + 2
+            const float s2 = p.signs[2 * j + 2];
+            const int kk = j % (D / 4), half = j / (D / 4);
+            sgn.esign[(kk & ~3) + ((kk >> 1) & 1) + 2 * half] =
+                (s0 < 0.0f ? 0xBF80u : 0x3F80u) | ((s2 < 0.0f ? 0xBF80u : 0x3F80u) << 16);
+        }
         if (blockIdx.x == 0 && ((fabsf(s0) != 1.0f) || (fabsf(s1) != 1.0f))) count_status(p.status, 4);
     }
     __syncthreads();
