@@ -841,7 +841,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                     // weights w = p * s'_V * 2^-E (invisible tokens: 0)
                     const float wa0 = pr[b][0] * sv0, wa1 = pr[b][1] * sv0;   // token tk0
                     const float wb0 = pr[b][2] * sv1, wb1 = pr[b][3] * sv1;   // token tk1
-                    const float zv0 = BITS == 4 ? nibble_to_float(vs0[b]) : 0.0f, zv1 = BITS == 4 ? nibble_to_float(vs1[b]) : 0.0f;
                     uint32_t bb0, bb1;
                     if constexpr (WIDE) {
                         // All eight columns are heads: plain fp16 weights (they are not exponentiated
@@ -849,13 +848,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                         // takes the same rounded weights: the codes' mean is far from zero, so the
                         // rounding errors cancel only against the zero-points they were made with.
                         const uint32_t pa = pack_f16x2(wa0, wa1), pb = pack_f16x2(wb0, wb1);
-                        const float2 ra = __half22float2(*reinterpret_cast<const __half2*>(&pa));
-                        const float2 rb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
-                        WZ0 = fmaf(ra.x, zv0, fmaf(rb.x, zv1, WZ0));
-                        WZ1 = fmaf(ra.y, zv0, fmaf(rb.y, zv1, WZ1));
+                        if constexpr (BITS == 4) {
+                            // mixed-precision FMAs read the weights in place; a masked zero-point
+                            // nibble is the fp16 subnormal zp 2^-24, so WZ runs scaled by 2^-24.  The
+                            // products are exact and at least 2^-48, so the scaling changes no
+                            // rounding unless a rescale drives the sum below 2^-126.
+                            const uint32_t zh0 = vs0[b] & 15u, zh1 = vs1[b] & 15u;
+                            WZ0 = fma_f16_f32<false>(pa, zh0, fma_f16_f32<false>(pb, zh1, WZ0));
+                            WZ1 = fma_f16_f32<true>(pa, zh0, fma_f16_f32<true>(pb, zh1, WZ1));
+                        }
                         bb0 = movmatrix_trans(pa);
                         bb1 = movmatrix_trans(pb);
                     } else {
+                        const float zv0 = BITS == 4 ? nibble_to_float(vs0[b]) : 0.0f;
+                        const float zv1 = BITS == 4 ? nibble_to_float(vs1[b]) : 0.0f;
                         // head hb's weight as fp16 high (column 2t) + low (column 2t + 1) halves
                         WZ0 = fmaf(wa0, zv0, fmaf(wb0, zv1, WZ0));
                         bb0 = movmatrix_trans(hi_lo_f16x2(wa0));
@@ -921,6 +927,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 l1 += __shfl_xor_sync(0xffffffffu, l1, off);
                 WZ1 += __shfl_xor_sync(0xffffffffu, WZ1, off);
             }
+        }
+        if constexpr (WIDE && BITS == 4) {   // sum(w zp) was carried scaled by 2^-24
+            WZ0 *= 16777216.0f;
+            WZ1 *= 16777216.0f;
         }
         const float es = eref ? __uint_as_float(eref << 23) : 0.0f;   // 2^(eref - 127)
         const size_t recn = (size_t)u.z * kConsumerWarps + warp;

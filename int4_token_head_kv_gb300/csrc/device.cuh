@@ -211,6 +211,20 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     return y;
 }
 
+// RN(a * b + c): a the low (HI_A false) or high fp16 half of a2, b the low fp16 half of b2, c fp32,
+// in one mixed-precision FMA that reads the fp16 operands in place (exact upcasts, one rounding).
+template <bool HI_A>
+__device__ __forceinline__ float fma_f16_f32(uint32_t a2, uint32_t b2, float c) {
+    float d;
+    if constexpr (!HI_A)
+        asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, al, bl, %3; }"
+            : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    else
+        asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, ah, bl, %3; }"
+            : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
